@@ -1,0 +1,445 @@
+#!/usr/bin/env python3
+"""Benchmark: decoded bf16 GB/s of the k3huf GPU decoder on GB300, its HBM
+roofline fraction, and the compression ratio of the workload.
+
+A step is one pass of the whole decode path over one layer container that
+is already resident in HBM: host-side header validation and launch, the
+per-CTA table build, chunk seek, Huffman decode of the high bytes, merge
+with the raw low bytes, integrity check.  ``e2e`` repeats the step through
+the same C ABI with host buffers: pinned host container -> HBM, decode,
+decoded weights -> pinned host, all inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
+                       [--workload projection|tiny|heavy_tail|trunk_layer|ring]
+                       [--impl reference]
+For N > 1 run under torchrun: every rank decodes its own replica (the path
+has no exchange step), timing is the max over ranks and ``value`` counts
+the bytes all ranks decoded.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "decoded bf16 GB/s on 1 GB300 and % of HBM roofline; compression ratio"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="projection",
+                    choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring"])
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--variant", type=int, default=0, help="0 double-symbol table, 1 single-symbol")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ring-layers", type=int, default=14)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def describe(name):
+    d = {"workload": name, "recipe": workloads.WORKLOADS[name]}
+    return d
+
+
+def make_layer(name):
+    """(tensors, container) of a named single-layer workload."""
+    import lossless_bf16_weight_k3huf_gb300 as k3
+    tensors = workloads.workload(name)
+    blob = k3.encode_layer(tensors)
+    return tensors, blob
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_src_sha():
+    p = os.path.join(ROOT, "lossless_bf16_weight_k3huf_gb300", "csrc", "k3huf_decode.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            t = json.load(f).get(workload)
+        if t and t.get("kernel_src_sha") == kernel_src_sha():
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *a):
+        time.sleep(0.25)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(blob, budget_s=12.0):
+    """The oracle's bit-serial decoder (single thread), timed on a bounded
+    sample: whole chunks of the workload's stripes, in order, until the
+    time budget is used."""
+    import oracle
+    info = oracle.layer_info(blob)
+    out = np.zeros(info["out_bytes"], dtype=np.uint8)
+    cs = info["chunk_syms"]
+    sdir = 64 + 256 * info["n_tables"] + 32 * info["n_tensors"]
+    values = 0
+    chunks = 0
+    t0 = time.perf_counter()
+    step = 64
+    done = False
+    for s in range(info["n_stripes"]):
+        e = sdir + 32 * s
+        nv = int.from_bytes(blob[e + 24:e + 28].tobytes(), "little")
+        nch = -(-nv // cs)
+        for c in range(0, nch, step):
+            n = min(step, nch - c)
+            rc = oracle.decode_chunks(blob, s, c, n, out)
+            if rc != 0:
+                raise RuntimeError(f"oracle decode failed: {rc}")
+            values += min(nv, (c + n) * cs) - c * cs
+            chunks += n
+            if time.perf_counter() - t0 > budget_s:
+                done = True
+                break
+        if done:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(2 * values / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{chunks} chunks of {cs} values ({2 * values / 2**20:.1f} MiB decoded) in {dt:.1f} s, "
+                      f"bit-serial oracle decoder, one thread"}
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores: each step decodes a
+    bounded sample (a fixed set of whole chunks) of the workload."""
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    name = args.workload if args.workload != "ring" else "trunk_layer"
+    tensors, blob = make_layer(name)
+    info = oracle.layer_info(blob)
+    out = np.zeros(info["out_bytes"], dtype=np.uint8)
+    cs = info["chunk_syms"]
+    sdir = 64 + 256 * info["n_tables"] + 32 * info["n_tensors"]
+    nv0 = int.from_bytes(blob[sdir + 24:sdir + 28].tobytes(), "little")
+    n_chunks = min(-(-nv0 // cs), 256)           # 1 Mi values of stripe 0 per step
+    sample_values = min(nv0, n_chunks * cs)
+
+    def step():
+        rc = oracle.decode_chunks(blob, 0, 0, n_chunks, out)
+        if rc:
+            raise RuntimeError(rc)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = 2 * sample_values * args.steps / dt / 1e9
+    sample = f"first {n_chunks} chunks ({sample_values} values) of stripe 0 per step, bit-serial oracle, one thread"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": describe(name),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import lossless_bf16_weight_k3huf_gb300 as k3
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    k3._build.build()
+    k3.set_decoder_variant(args.variant)
+    if args.workload == "ring":
+        return bench_ring(args, rank, world, local, dev)
+
+    tensors, blob = make_layer(args.workload)
+    info = k3.layer_info(blob)
+    hdr = blob[: info["hdr_bytes"]].copy()
+    raw = info["raw_bytes"]
+    d_blob = torch.from_numpy(blob).to(dev)
+    d_out = torch.empty(info["out_bytes"], dtype=torch.uint8, device=dev)
+    d_st = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    launches_per_step = -(-info["n_stripes"] // 64)
+    l2_note = ("inputs larger than L2" if info["blob_bytes"] + info["out_bytes"] > 2 * L2_BYTES
+               else "L2 flushed between steps")
+    flush = None if info["blob_bytes"] + info["out_bytes"] > 2 * L2_BYTES else \
+        torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        if flush is not None:
+            flush.fill_(1)
+        k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    stream.synchronize()
+    # correctness of the benchmarked output (bytes equal the original tensors)
+    ok = d_st.item() == 0
+    for t, x in zip(range(info["n_tensors"]), tensors):
+        ti = k3.tensor_info(hdr, t)
+        a = ti["out_offset"]
+        ref = torch.from_numpy(np.asarray(x, np.uint16).reshape(-1).view(np.int16)).to(dev)
+        ok = ok and torch.equal(d_out[a:a + 2 * ti["n_values"]].view(torch.int16), ref)
+        del ref
+    if not ok:
+        raise SystemExit("decode output differs from the input tensors")
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(args.steps):
+                if flush is not None:
+                    flush.fill_(1)
+                ev[i][0].record(stream)
+                k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream)
+                ev[i][1].record(stream)
+            t_end.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    kernel_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = t_start.elapsed_time(t_end)
+    dev_ms = sum(kernel_ms)                      # decode time only (excludes any L2 flush)
+    if world > 1:
+        t = torch.tensor([dev_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        dev_ms = float(t.item())
+    ms_per_step = dev_ms / args.steps
+    value = raw * world * args.steps / (dev_ms / 1e3) / 1e9
+
+    # end to end through the C ABI with host buffers
+    e2e = bench_e2e(k3, blob, hdr, info, dev, stream, max(3, min(args.steps, 20)))
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = measured_peak()
+    alg = info["blob_bytes"] + info["raw_bytes"]
+    avg_launch_ms = statistics.mean(kernel_ms) / launches_per_step
+    achieved = alg / launches_per_step / (avg_launch_ms / 1e3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {**describe(args.workload), "values": raw // 2, "raw_bytes": raw,
+                   "blob_bytes": info["blob_bytes"], "compression_ratio": round(raw / info["blob_bytes"], 4),
+                   "compression_rate": round(info["blob_bytes"] / raw, 4), "stripes": info["n_stripes"],
+                   "chunk_syms": info["chunk_syms"], "decoder": ["double-symbol", "single-symbol"][args.variant],
+                   "l2": l2_note, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": traffic, "algorithmic_bytes_per_launch": alg // launches_per_step,
+                     "frac_of_8TBs": round(achieved / 8000.0, 4)},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "timed_region_ms": round(total_ms, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(blob)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def bench_e2e(k3, blob, hdr, info, dev, stream, steps):
+    """Pinned host container -> HBM, decode, decoded bytes -> pinned host;
+    every step, timed with events on the launching stream."""
+    import torch
+    h_blob = torch.from_numpy(blob).pin_memory()
+    h_out = torch.empty(info["out_bytes"], dtype=torch.uint8).pin_memory()
+    d_blob = torch.empty(blob.size, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(info["out_bytes"], dtype=torch.uint8, device=dev)
+    d_st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def one():
+        d_blob.copy_(h_blob, non_blocking=True)
+        k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            one()
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"value": round(info["raw_bytes"] / (ms / 1e3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(blob.size), "d2h_bytes_per_step": int(info["out_bytes"]),
+            "ms_per_step": round(ms, 4), "steps": steps}
+
+
+def bench_ring(args, rank, world, local, dev):
+    """Streaming ring: 14 trunk layers compressed into pinned host memory,
+    double-buffered H2D copies overlapped with the decode."""
+    import torch
+    import lossless_bf16_weight_k3huf_gb300 as k3
+    seeds = workloads.ring_layers(n_layers=args.ring_layers)
+    h_layers, infos = [], []
+    for s in seeds:
+        tensors = workloads.trunk_layer(seed=s)
+        blob = k3.encode_layer(tensors)
+        infos.append(k3.layer_info(blob))
+        h_layers.append(torch.from_numpy(blob).pin_memory())
+        del tensors, blob
+    out_bytes = max(i["out_bytes"] for i in infos)
+    # two output slots, as a consumer would reuse them layer after layer
+    outs = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_outs = [outs[i % 2] for i in range(len(h_layers))]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ring = k3.Ring(max(h.numel() for h in h_layers), 2)
+    for _ in range(max(1, args.warmup)):
+        ring.run(h_layers, d_outs, st)
+    if st.item() != 0:
+        raise SystemExit("ring decode reported a fault")
+    stats = []
+    with ClockSampler(dev.index) as clk:
+        for _ in range(args.steps):
+            stats.append(ring.run(h_layers, d_outs, st))
+    ring.close()
+    raw = sum(i["raw_bytes"] for i in infos)
+    blob_total = sum(i["blob_bytes"] for i in infos)
+    tot = sum(s["total_ms"] for s in stats)
+    dec = sum(s["decode_ms"] for s in stats)
+    cp = sum(s["copy_ms"] for s in stats)
+    value = raw * args.steps / (tot / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    launches = sum(-(-i["n_stripes"] // 64) for i in infos)
+    achieved = (blob_total + raw) / (dec / args.steps / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {**describe("ring"), "layers": len(h_layers), "raw_bytes": raw, "blob_bytes": blob_total,
+                   "compression_ratio": round(raw / blob_total, 4),
+                   "decode_only_gbs": round(raw * args.steps / (dec / 1e3) / 1e9, 2),
+                   "copy_only_gbs_h2d": round(blob_total * args.steps / (cp / 1e3) / 1e9, 2),
+                   "exposed_copy_ms_per_step": round((tot - dec) / args.steps, 3),
+                   "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": None},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": blob_total, "d2h_bytes_per_step": 0},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

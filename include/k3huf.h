@@ -1,0 +1,204 @@
+/*
+ * k3huf.h -- C ABI of the k3_huf bf16 weight codec on GB300 (sm_103a).
+ *
+ * The codec: the high byte (sign and exponent) of every little-endian bf16
+ * value -- the odd byte offset -- is coded with a canonical, longest-first
+ * Huffman code whose lengths are capped at 12 bits; the low (mantissa) byte
+ * -- the even offset -- is stored raw.  Decoding is exact: the output bytes
+ * equal the original bytes.  Source: the article "Kimi K3 纯 CPU 推理中的无损
+ * Trunk 压缩：一次被解码速度判死刑的 Huffman 压缩实验", sections 核心思想
+ * (byte-plane split), 已实现的部分 (container, 64 MiB stripes, 12-bit cap,
+ * 4096-entry symbol/length table) and 规范码分配与 Kraft 校验 (table check
+ * and canonical assignment).
+ *
+ * Conventions for every call:
+ *  - the return value is K3HUF_OK (0) or a negative K3HUF_E_* code; no call
+ *    throws, aborts or prints;
+ *  - the caller owns every buffer and every stream; the decode calls
+ *    allocate nothing (only k3huf_ring_create allocates, once);
+ *  - "d_" pointers are device pointers on the current CUDA device and must
+ *    be 16-byte aligned; "h_" pointers are host pointers;
+ *  - decode calls are asynchronous on the given cudaStream_t (passed as
+ *    void*, NULL = the legacy default stream).  Faults that the host can
+ *    see (bad header, bad table, sizes, alignment) are returned at once;
+ *    faults inside the compressed streams are OR-ed into *d_status (a
+ *    device uint32 the caller zeroes beforehand and reads after the stream
+ *    is synchronised); the output bytes are unspecified when it is nonzero;
+ *  - no kernel of this library traps, asserts or waits without bound.
+ *
+ * Container, format version 1 (little-endian; all offsets in bytes):
+ *  layer header, 64 B: u32 magic 'K3HF' | u16 version | u16 maxlen (12) |
+ *    u32 chunk_syms | u32 n_tables | u32 n_tensors | u32 n_stripes |
+ *    u64 raw_bytes | u64 blob_bytes | u32 stripe_values (2^25) |
+ *    u32 hdr_bytes | u64 out_bytes | 8 B zero
+ *  codelen[256] per table; tensor directory, 32 B per tensor:
+ *    u32 table, u32 first_stripe, u32 n_stripes, u32 0, u64 n_values,
+ *    u64 out_offset; stripe directory, 32 B per stripe: u64 blob_offset,
+ *    u64 stripe_bytes, u64 out_offset, u32 n_values, u32 table; zero
+ *    padding up to hdr_bytes (a multiple of 256).
+ *  stripe (256-B aligned; <= 2^25 values of one tensor):
+ *    u32 magic 'K3HS' | u32 table | u32 n_values | u32 n_chunks |
+ *    u64 huff_bits | u32 bits_offset | u32 even_offset, then
+ *    u32 chunk_bitoff[n_chunks] (bit offset of the first code of every run
+ *    of chunk_syms values), the bit stream at bits_offset =
+ *    align16(32 + 4 n_chunks), read most-significant bit first, zero padded
+ *    to align16(ceil(huff_bits/8)) + 32 bytes; the n raw low bytes at
+ *    even_offset = bits_offset + that padded size, zero padded to a
+ *    multiple of 16.  Tensor outputs start at 256-B aligned offsets of the
+ *    layer output (out_offset).
+ */
+#ifndef K3HUF_H
+#define K3HUF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define K3HUF_MAXLEN         12          /* longest code, bits */
+#define K3HUF_TABLE_ENTRIES  4096        /* 1 << K3HUF_MAXLEN */
+#define K3HUF_STRIPE_VALUES  33554432u   /* 64 MiB of bf16 per stripe */
+#define K3HUF_FORMAT_VERSION 1
+#define K3HUF_LAYER_HDR_BYTES 64
+#define K3HUF_STRIPE_HDR_BYTES 32
+
+/* return codes */
+#define K3HUF_OK         0
+#define K3HUF_E_ARG     -1   /* bad argument: null, size, alignment */
+#define K3HUF_E_EMPTY   -2   /* code table with no symbol */
+#define K3HUF_E_OVERSUB -3   /* code table over-subscribed (Kraft sum > 2^12) */
+#define K3HUF_E_BADLEN  -4   /* a code length above 12 */
+#define K3HUF_E_FORMAT  -5   /* container malformed: magic, version, sizes, offsets */
+#define K3HUF_E_CUDA    -6   /* a CUDA runtime call failed; see k3huf_last_cuda_error */
+#define K3HUF_E_NOMEM   -7   /* host allocation failed (encoder / ring only) */
+
+/* bits OR-ed into *d_status by the decode kernels */
+#define K3HUF_ST_BADCODE  1u  /* a bit pattern that starts no code */
+#define K3HUF_ST_OVERRUN  2u  /* a chunk read past the end of its stripe's stream */
+#define K3HUF_ST_INDEX    4u  /* a chunk did not end at the next chunk's recorded offset */
+#define K3HUF_ST_HEADER   8u  /* a device-side stripe header disagrees with the layer header */
+
+typedef struct {
+    uint32_t chunk_syms, n_tables, n_tensors, n_stripes;
+    uint64_t raw_bytes;      /* sum of 2 * n_values over tensors */
+    uint64_t blob_bytes;     /* container size */
+    uint64_t out_bytes;      /* decoded layer size, including alignment gaps */
+    uint32_t hdr_bytes;      /* bytes of header + tables + directories (padded) */
+    uint32_t stripe_values;
+} k3huf_layer_info_t;
+
+typedef struct {
+    uint32_t table, first_stripe, n_stripes, reserved;
+    uint64_t n_values, out_offset;
+} k3huf_tensor_info_t;
+
+/* Build the decoder's 4096-entry table from code lengths (host, pure).
+ * Article section 规范码分配与 Kraft 校验: the Kraft sum
+ * sum_s 2^(12 - codelen[s]) over used symbols must be at most 4096 (full or
+ * under-full) and nonzero; codes are assigned longest-first,
+ * first[l] = code; code = ceil((code + count[l]) / 2) for l = 12 .. 1, and
+ * symbols of one length take consecutive codes in symbol order.  Entry i of
+ * sym_len is (s << 4) | codelen[s] for the symbol s whose code is a prefix
+ * of the 12-bit value i, 0 where no code is (incomplete tables).
+ * codelen: 256 bytes, 0 = unused symbol.  sym_len: 4096 uint16 written by
+ * the call (may be NULL to only check the table).
+ * Returns K3HUF_OK, K3HUF_E_BADLEN, K3HUF_E_EMPTY, K3HUF_E_OVERSUB or
+ * K3HUF_E_ARG (codelen NULL). */
+int k3huf_build(const uint8_t codelen[256], uint16_t sym_len[4096]);
+
+/* Parse and validate a layer header (host copy of the first hdr_bytes of
+ * the container, or more): magic, version, maxlen, every table
+ * (k3huf_build), the directories (stripe ranges inside blob_bytes, 256-B
+ * alignment, tensor/stripe consistency).  Returns K3HUF_E_FORMAT with
+ * info untouched when bytes < hdr_bytes.  The call reads only h_layer. */
+int k3huf_layer_info(const void *h_layer, size_t bytes, k3huf_layer_info_t *info);
+
+/* Directory entry of tensor t of a validated header. */
+int k3huf_tensor_info(const void *h_layer, size_t bytes, uint32_t t, k3huf_tensor_info_t *out);
+
+/* Decode a whole layer on the GPU.
+ *  h_layer_hdr / hdr_bytes: host copy of at least the header part of the
+ *    container (the same bytes as the device copy's first hdr_bytes);
+ *  d_layer / layer_bytes: the whole container in device memory;
+ *  d_out / out_bytes: decoded output (>= info.out_bytes); tensor t's bf16
+ *    values land at d_out + out_offset(t); alignment gaps are not written;
+ *  d_status: device uint32, OR-ed with K3HUF_ST_* bits;
+ *  stream: cudaStream_t.
+ * One kernel launch per 64 stripes.  Returns K3HUF_OK once launched. */
+int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes,
+                       const void *d_layer, size_t layer_bytes,
+                       void *d_out, size_t out_bytes,
+                       uint32_t *d_status, void *stream);
+
+/* Decode one stripe on the GPU (the article's per-stripe decode).
+ *  codelen: host copy of the stripe's table (validated with k3huf_build);
+ *  chunk_syms: values per indexed chunk, as in the layer header;
+ *  d_stripe / stripe_bytes: the stripe in device memory, from its header;
+ *  n_values: values in the stripe (<= 2^25); d_out receives 2 n_values
+ *  bytes of bf16.  The kernel checks the device-side stripe header against
+ *  n_values / chunk_syms / stripe_bytes and sets K3HUF_ST_HEADER if they
+ *  disagree. */
+int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms,
+                        const void *d_stripe, size_t stripe_bytes,
+                        uint32_t n_values, void *d_out,
+                        uint32_t *d_status, void *stream);
+
+/* Select the decode kernel variant for later decode calls in this process:
+ * 0 = double-symbol table (default; two codes per lookup when both fit in
+ * the 12-bit window, article section 如果将来重启), 1 = single-symbol table
+ * (one code per lookup, the article's shelved decoder's scheme).  Both give
+ * identical output.  Returns K3HUF_E_ARG for any other value. */
+int k3huf_set_decoder_variant(int variant);
+
+/* Pack-time encoder (host, multi-threaded), producing the container above
+ * byte for byte as specified: per table, the histogram of the high bytes,
+ * Huffman code lengths from a min-heap keyed (count, id) with leaves
+ * id = symbol and internal nodes 256 + creation order (one used symbol gets
+ * length 1), the 12-bit limit (clamp, then while the Kraft sum exceeds 4096
+ * lengthen the code of lowest count among those shorter than 12, ties to
+ * the larger symbol), the canonical assignment of k3huf_build.
+ *  h_tensors[t]: n_values[t] (>= 1) little-endian bf16 values;
+ *  chunk_syms: values per indexed chunk (>= 1);
+ *  shared_table: nonzero = one table for the whole layer, else one per tensor;
+ *  n_threads: worker threads (0 = hardware concurrency);
+ *  h_blob / blob_cap: output; with h_blob NULL only *blob_bytes is set. */
+int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tensors, const uint64_t *n_values,
+                       uint32_t chunk_syms, int shared_table, int n_threads,
+                       void *h_blob, size_t blob_cap, size_t *blob_bytes);
+
+/* Streaming ring: layers held in pinned host memory are copied to device
+ * slots with cudaMemcpyAsync on a copy stream while the previous layer is
+ * decoded on a compute stream, double buffered (the article's trunk ring,
+ * "a second slot is what overlaps reads with compute").
+ * k3huf_ring_create allocates n_slots device slots of slot_bytes each and
+ * the streams/events it needs. */
+typedef struct k3huf_ring k3huf_ring;
+
+typedef struct {
+    float total_ms;      /* first copy issued -> last decode finished */
+    float decode_ms;     /* sum of the decode kernels' event times */
+    float copy_ms;       /* sum of the copies' event times */
+    uint64_t h2d_bytes;  /* bytes copied host -> device */
+    uint64_t out_bytes;  /* bytes decoded */
+} k3huf_ring_stats_t;
+
+int k3huf_ring_create(size_t slot_bytes, int n_slots, k3huf_ring **ring);
+/* Decode n_layers containers h_layers[i] (pinned host memory, layer_bytes[i]
+ * bytes each, <= slot_bytes) into d_outs[i] (out_bytes[i] each).  Blocks
+ * until all work is done; fills *stats when non-NULL. */
+int k3huf_ring_run(k3huf_ring *ring, int n_layers, const void *const *h_layers, const size_t *layer_bytes,
+                   void *const *d_outs, const size_t *out_bytes, uint32_t *d_status,
+                   k3huf_ring_stats_t *stats);
+int k3huf_ring_destroy(k3huf_ring *ring);
+
+/* Last CUDA error code seen by this library on the calling thread. */
+int k3huf_last_cuda_error(void);
+/* Static description of a K3HUF_E_* code. */
+const char *k3huf_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* K3HUF_H */

@@ -1,0 +1,327 @@
+"""GPU parity: the CUDA decode (through the C ABI) against the CPU oracle.
+
+Decoding is exact, so the bar is bit-exact bytes: the GPU output equals the
+oracle's bit-serial decode of the same container, element by element, and
+both equal the original tensor.  Small cases compare whole outputs; the
+full-size workloads (launched exactly as the benchmark launches them)
+compare every byte with the original tensor and sampled chunks with the
+oracle's decode of those chunks."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+k3 = pytest.importorskip("lossless_bf16_weight_k3huf_gb300")
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+SENTINEL = 0xA5
+GUARD = 4096
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    k3._build.build()
+    yield
+    k3.set_decoder_variant(0)
+
+
+def gpu_decode(blob, variant=0, stream=None, status_init=0):
+    """Decode on the GPU; returns (output bytes, status, guard intact)."""
+    info = k3.layer_info(blob)
+    d_blob = torch.from_numpy(np.ascontiguousarray(blob)).cuda()
+    n = info["out_bytes"]
+    buf = torch.full((n + 2 * GUARD,), SENTINEL, dtype=torch.uint8, device="cuda")
+    d_out = buf[GUARD:GUARD + n]
+    st = torch.full((1,), status_init, dtype=torch.int32, device="cuda")
+    k3.set_decoder_variant(variant)
+    k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, d_out, st, stream=stream)
+    torch.cuda.synchronize()
+    h = buf.cpu().numpy()
+    guard_ok = bool((h[:GUARD] == SENTINEL).all() and (h[GUARD + n:] == SENTINEL).all())
+    return h[GUARD:GUARD + n], int(st.item()), guard_ok
+
+
+def tensor_regions(blob):
+    info = k3.layer_info(blob)
+    return [k3.tensor_info(blob, t) for t in range(info["n_tensors"])]
+
+
+def check_parity(tensors, variant=0, **enc):
+    blob = oracle.encode_layer(tensors, **enc)
+    out, st, guard_ok = gpu_decode(blob, variant)
+    assert st == 0 and guard_ok
+    rc, ref = oracle.decode_layer(blob)
+    assert rc == 0
+    covered = np.zeros(out.size, dtype=bool)
+    for t, x in zip(tensor_regions(blob), tensors):
+        a, b = t["out_offset"], t["out_offset"] + 2 * t["n_values"]
+        got = out[a:b]
+        assert np.array_equal(got, ref[a:b]), f"first mismatch at byte {int(np.argmax(got != ref[a:b]))}"
+        assert np.array_equal(got.view(np.uint16), np.asarray(x, np.uint16).reshape(-1))
+        covered[a:b] = True
+    assert (out[~covered] == SENTINEL).all()           # alignment gaps untouched
+    return blob
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_tiny(variant):
+    check_parity([workloads.tiny()], variant)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 4095, 4096, 4097, 8191, 12289,
+                               128 * 4096 - 1, 128 * 4096 + 1, 100_003])
+@pytest.mark.parametrize("variant", [0, 1])
+def test_ragged_sizes(n, variant):
+    check_parity([workloads.normal_tensor((n,), 0.02, seed=n)], variant)
+
+
+@pytest.mark.parametrize("chunk_syms", [1, 7, 8, 64, 256, 1000, 4096, 65536])
+def test_chunk_sizes(chunk_syms):
+    check_parity([workloads.normal_tensor((70_001,), 0.05, seed=9)], chunk_syms=chunk_syms)
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_degenerate_planes(variant):
+    check_parity([workloads.single_symbol(50_001)], variant)
+    check_parity([workloads.two_symbol(50_001)], variant)
+    check_parity([workloads.uniform_bytes(300_000)], variant)
+
+
+def test_limiter_fired_alphabet():
+    x = workloads.heavy_tail(n=1 << 22)
+    blob = check_parity([x])
+    assert k3.layer_info(blob)["n_tables"] == 1
+    assert oracle.huffman_lengths(oracle.histogram(x)).max() > 12
+
+
+def test_multi_tensor_and_shared_table():
+    ts = [workloads.normal_tensor((64, 96), 0.1, 3, 0), workloads.normal_tensor((5,), 0.3, 3, 1),
+          workloads.normal_tensor((96, 640), 0.04, 3, 2), workloads.normal_tensor((33,), 0.01, 3, 3)]
+    check_parity(ts)
+    check_parity(ts, shared_table=True)
+
+
+def test_multi_stripe_tensor():
+    n = (1 << 25) + 5003
+    x = np.tile(workloads.tiny(), n // (1 << 21) + 1)[:n]
+    blob = check_parity([x])
+    assert k3.layer_info(blob)["n_stripes"] == 2
+
+
+def test_many_stripes_span_launches():
+    """More stripes than one launch carries (64): 70 small tensors."""
+    ts = [workloads.normal_tensor((4096 + 17 * i,), 0.02, 500 + i) for i in range(70)]
+    check_parity(ts)
+
+
+def test_decode_stripe_entry():
+    n = (1 << 25) + 70_000
+    x = np.tile(workloads.tiny(), n // (1 << 21) + 1)[:n]
+    blob = k3.encode_layer([x])
+    info = k3.layer_info(blob)
+    sdir = 64 + 256 * info["n_tables"] + 32 * info["n_tensors"]
+    d_blob = torch.from_numpy(blob).cuda()
+    for s in range(2):
+        e = sdir + 32 * s
+        off = int.from_bytes(blob[e:e + 8].tobytes(), "little")
+        sb = int.from_bytes(blob[e + 8:e + 16].tobytes(), "little")
+        nv = int.from_bytes(blob[e + 24:e + 28].tobytes(), "little")
+        out = torch.zeros(2 * nv, dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        k3.decode_stripe(blob[64:64 + 256], info["chunk_syms"], d_blob[off:], sb, nv, out, st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert np.array_equal(out.cpu().numpy().view(np.uint16), x[s * (1 << 25): s * (1 << 25) + nv])
+
+
+def test_status_is_or_ed():
+    _, st, _ = gpu_decode(oracle.encode_layer([workloads.tiny()]), status_init=0x40)
+    assert st == 0x40
+
+
+def test_on_a_side_stream():
+    blob = oracle.encode_layer([workloads.tiny()])
+    s = torch.cuda.Stream()
+    out, st, ok = gpu_decode(blob, stream=s)
+    assert st == 0 and ok
+    assert np.array_equal(out.view(np.uint16)[: 1 << 21], workloads.tiny())
+
+
+# --- corrupt streams: a status bit, never a fault ----------------------------------
+
+def _stripe0(blob):
+    info = k3.layer_info(blob)
+    sdir = 64 + 256 * info["n_tables"] + 32 * info["n_tensors"]
+    return int.from_bytes(blob[sdir:sdir + 8].tobytes(), "little")
+
+
+def _decode_device_copy(host_hdr_blob, device_blob):
+    info = k3.layer_info(host_hdr_blob)
+    d_blob = torch.from_numpy(np.ascontiguousarray(device_blob)).cuda()
+    buf = torch.full((info["out_bytes"] + 2 * GUARD,), SENTINEL, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3.decode_layer(host_hdr_blob[: info["hdr_bytes"]], d_blob, buf[GUARD:GUARD + info["out_bytes"]], st)
+    torch.cuda.synchronize()
+    h = buf.cpu().numpy()
+    assert (h[:GUARD] == SENTINEL).all() and (h[GUARD + info["out_bytes"]:] == SENTINEL).all()
+    return int(st.item())
+
+
+def test_fault_chunk_index():
+    blob = oracle.encode_layer([workloads.normal_tensor((20_000,), 0.02, 6)])
+    bad = blob.copy()
+    o = _stripe0(blob)
+    bad[o + 32 + 4] ^= 1                                # chunk 1 starts one bit off
+    assert oracle.decode_layer(bad)[0] != 0
+    st = _decode_device_copy(blob, bad)
+    assert st & k3.ST_INDEX
+
+
+def test_fault_undecodable_window():
+    x = np.array([0x0000, 0x0100, 0x0000, 0x0000] * 3, dtype=np.uint16)
+    blob = oracle.encode_layer([x])
+    o = _stripe0(blob)
+    bits_off = int.from_bytes(blob[o + 24:o + 28].tobytes(), "little")
+    # incomplete table {0:1, 1:2}: sym1 = 00, sym0 = 1; 12 symbols = 0,1,0,0 x3
+    blob[64 + 1] = 2
+    blob[o + 16:o + 24] = np.frombuffer((15).to_bytes(8, "little"), np.uint8)
+    blob[o + bits_off:o + bits_off + 2] = [0b10011100, 0b11100110]
+    assert oracle.decode_layer(blob)[0] == 0
+    out, st, _ = gpu_decode(blob)
+    assert st == 0 and np.array_equal(out[:24].view(np.uint16), x)
+    bad = blob.copy()
+    bad[o + bits_off] = 0b01011100                     # starts with 01: no code
+    assert oracle.decode_layer(bad)[0] != 0
+    st = _decode_device_copy(blob, bad)
+    assert st & (k3.ST_BADCODE | k3.ST_INDEX)
+
+
+def test_fault_device_header_mismatch():
+    blob = oracle.encode_layer([workloads.normal_tensor((20_000,), 0.02, 7)])
+    o = _stripe0(blob)
+    for off, val in [(o, 0), (o + 8, 0x21), (o + 12, 9), (o + 28, 0x11)]:
+        bad = blob.copy()
+        bad[off] = val
+        assert _decode_device_copy(blob, bad) & k3.ST_HEADER, off
+
+
+def test_fault_device_table_oversubscribed():
+    blob = oracle.encode_layer([workloads.normal_tensor((20_000,), 0.02, 8)])
+    bad = blob.copy()
+    bad[64:64 + 256] = 1
+    assert _decode_device_copy(blob, bad) & k3.ST_HEADER
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_fault_random_bitstream(seed):
+    blob = oracle.encode_layer([workloads.normal_tensor((50_000,), 0.02, 10 + seed)])
+    o = _stripe0(blob)
+    bits_off = int.from_bytes(blob[o + 24:o + 28].tobytes(), "little")
+    even_off = int.from_bytes(blob[o + 28:o + 32].tobytes(), "little")
+    bad = blob.copy()
+    rng = np.random.default_rng(seed)
+    bad[o + bits_off:o + even_off] = rng.integers(0, 256, even_off - bits_off, dtype=np.uint8)
+    assert _decode_device_copy(blob, bad) != 0
+
+
+def test_host_side_errors_raise():
+    blob = oracle.encode_layer([workloads.tiny()])
+    info = k3.layer_info(blob)
+    d_blob = torch.from_numpy(blob).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    small = torch.zeros(info["out_bytes"] - 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(k3.K3HufError):
+        k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, small, st)
+    out = torch.zeros(info["out_bytes"] + 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(k3.K3HufError):
+        k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, out[1:], st, out_bytes=info["out_bytes"])
+
+
+# --- streaming ring ------------------------------------------------------------------
+
+def test_ring_small_layers():
+    layers = [[workloads.normal_tensor((3000 + i, 64), 0.05, 40 + i)] for i in range(5)]
+    layers.append([workloads.normal_tensor((7,), 0.3, 99), workloads.normal_tensor((4097,), 0.02, 98)])
+    blobs = [k3.encode_layer(ts) for ts in layers]
+    h = [torch.from_numpy(b).pin_memory() for b in blobs]
+    outs = [torch.zeros(k3.layer_info(b)["out_bytes"], dtype=torch.uint8, device="cuda") for b in blobs]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ring = k3.Ring(max(b.size for b in blobs), 2)
+    stats = ring.run(h, outs, st)
+    ring.close()
+    assert st.item() == 0
+    assert stats["h2d_bytes"] == sum(b.size for b in blobs)
+    for ts, b, o in zip(layers, blobs, outs):
+        oc = o.cpu().numpy()
+        for t, x in zip(tensor_regions(b), ts):
+            a = t["out_offset"]
+            assert np.array_equal(oc[a:a + 2 * t["n_values"]].view(np.uint16), x.reshape(-1))
+
+
+# --- full-size workloads, launched as the benchmark launches them -------------------
+
+def _sampled_parity(blob, tensors, out_dev, n_sample=24, seed=0):
+    """Every output byte equals the original tensor (checked on the GPU);
+    sampled chunks equal the oracle's bit-serial decode of those chunks."""
+    info = k3.layer_info(blob)
+    regions = tensor_regions(blob)
+    for t, x in zip(regions, tensors):
+        a = t["out_offset"]
+        ref = torch.from_numpy(np.asarray(x, np.uint16).reshape(-1).view(np.int16)).cuda()
+        got = out_dev[a:a + 2 * t["n_values"]].view(torch.int16)
+        assert torch.equal(got, ref)
+        del ref
+    out_host = None
+    rng = np.random.default_rng(seed)
+    cs = info["chunk_syms"]
+    sdir = 64 + 256 * info["n_tables"] + 32 * info["n_tensors"]
+    for s in range(info["n_stripes"]):
+        e = sdir + 32 * s
+        nv = int.from_bytes(blob[e + 24:e + 28].tobytes(), "little")
+        sout = int.from_bytes(blob[e + 16:e + 24].tobytes(), "little")
+        nch = -(-nv // cs)
+        picks = sorted(set([0, nch - 1] + list(rng.integers(0, nch, n_sample))))
+        for c in picks:
+            scratch = np.zeros(info["out_bytes"], dtype=np.uint8) if out_host is None else out_host
+            out_host = scratch
+            assert oracle.decode_chunks(blob, s, c, 1, scratch) == 0
+            a = sout + 2 * c * cs
+            b = sout + 2 * min(nv, (c + 1) * cs)
+            got = out_dev[a:b].cpu().numpy()
+            assert np.array_equal(got, scratch[a:b]), (s, c)
+
+
+def _full_size(tensors):
+    blob = k3.encode_layer(tensors)
+    info = k3.layer_info(blob)
+    d_blob = torch.from_numpy(blob).cuda()
+    out = torch.empty(info["out_bytes"], dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3.set_decoder_variant(0)
+    k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, out, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    _sampled_parity(blob, tensors, out)
+    # the oracle encoder's tables equal the product encoder's
+    for t, x in zip(tensor_regions(blob), tensors):
+        assert np.array_equal(blob[64 + 256 * t["table"]: 64 + 256 * (t["table"] + 1)],
+                              oracle.code_lengths(oracle.histogram(x)).astype(np.uint8))
+
+
+@pytest.mark.slow
+def test_full_projection():
+    _full_size([workloads.projection()])
+
+
+@pytest.mark.slow
+def test_full_heavy_tail():
+    _full_size([workloads.heavy_tail()])
+
+
+@pytest.mark.slow
+def test_full_trunk_layer():
+    _full_size(workloads.trunk_layer())
