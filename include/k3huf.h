@@ -30,7 +30,7 @@
  *  layer header, 64 B: u32 magic 'K3HF' | u16 version | u16 maxlen (12) |
  *    u32 chunk_syms | u32 n_tables | u32 n_tensors | u32 n_stripes |
  *    u64 raw_bytes | u64 blob_bytes | u32 stripe_values (2^25) |
- *    u32 hdr_bytes | u64 out_bytes | 8 B zero
+ *    u32 hdr_bytes | u64 out_bytes | u32 sub_syms | 4 B zero
  *  codelen[256] per table; tensor directory, 32 B per tensor:
  *    u32 table, u32 first_stripe, u32 n_stripes, u32 0, u64 n_values,
  *    u64 out_offset; stripe directory, 32 B per stripe: u64 blob_offset,
@@ -40,8 +40,12 @@
  *    u32 magic 'K3HS' | u32 table | u32 n_values | u32 n_chunks |
  *    u64 huff_bits | u32 bits_offset | u32 even_offset, then
  *    u32 chunk_bitoff[n_chunks] (bit offset of the first code of every run
- *    of chunk_syms values), the bit stream at bits_offset =
- *    align16(32 + 4 n_chunks), read most-significant bit first, zero padded
+ *    of chunk_syms values), u16 sub_bitoff[n_chunks][S-1] with
+ *    S = chunk_syms / sub_syms (entry k-1 of chunk c: bit offset, relative
+ *    to the chunk's first bit, of the code of value min(k sub_syms, len_c)
+ *    of the chunk -- S independent sub-streams per chunk; S = 1 when
+ *    chunk_syms * 12 > 65535), the bit stream at bits_offset =
+ *    align16(32 + 4 n_chunks + 2 n_chunks (S-1)), read most-significant bit first, zero padded
  *    to align16(ceil(huff_bits/8)) + 32 bytes; the n raw low bytes at
  *    even_offset = bits_offset + that padded size, zero padded to a
  *    multiple of 16.  Tensor outputs start at 256-B aligned offsets of the
@@ -79,6 +83,7 @@ extern "C" {
 #define K3HUF_ST_OVERRUN  2u  /* a chunk read past the end of its stripe's stream */
 #define K3HUF_ST_INDEX    4u  /* a chunk did not end at the next chunk's recorded offset */
 #define K3HUF_ST_HEADER   8u  /* a device-side stripe header disagrees with the layer header */
+#define K3HUF_ST_TIMEOUT 16u  /* a bounded wait for an asynchronous copy gave up (work skipped) */
 
 typedef struct {
     uint32_t chunk_syms, n_tables, n_tensors, n_stripes;
@@ -87,6 +92,8 @@ typedef struct {
     uint64_t out_bytes;      /* decoded layer size, including alignment gaps */
     uint32_t hdr_bytes;      /* bytes of header + tables + directories (padded) */
     uint32_t stripe_values;
+    uint32_t sub_syms;       /* values per independently decodable sub-stream */
+    uint32_t reserved;
 } k3huf_layer_info_t;
 
 typedef struct {
@@ -134,22 +141,24 @@ int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes,
 
 /* Decode one stripe on the GPU (the article's per-stripe decode).
  *  codelen: host copy of the stripe's table (validated with k3huf_build);
- *  chunk_syms: values per indexed chunk, as in the layer header;
+ *  chunk_syms, sub_syms: values per indexed chunk and per sub-stream, as
+ *    in the layer header;
  *  d_stripe / stripe_bytes: the stripe in device memory, from its header;
  *  n_values: values in the stripe (<= 2^25); d_out receives 2 n_values
  *  bytes of bf16.  The kernel checks the device-side stripe header against
  *  n_values / chunk_syms / stripe_bytes and sets K3HUF_ST_HEADER if they
  *  disagree. */
-int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms,
+int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms, uint32_t sub_syms,
                         const void *d_stripe, size_t stripe_bytes,
                         uint32_t n_values, void *d_out,
                         uint32_t *d_status, void *stream);
 
 /* Select the decode kernel variant for later decode calls in this process:
- * 0 = double-symbol table (default; two codes per lookup when both fit in
- * the 12-bit window, article section 如果将来重启), 1 = single-symbol table
- * (one code per lookup, the article's shelved decoder's scheme).  Both give
- * identical output.  Returns K3HUF_E_ARG for any other value. */
+ * the most codes one table lookup may emit.  0 = default (3), 1 = one code
+ * per lookup (the article's shelved decoder's scheme), 2 = the article's
+ * double-symbol table (section 如果将来重启), 3 = up to three codes when
+ * they fit in the 12-bit window.  All give identical output.  Returns
+ * K3HUF_E_ARG for any other value. */
 int k3huf_set_decoder_variant(int variant);
 
 /* Pack-time encoder (host, multi-threaded), producing the container above
@@ -161,11 +170,13 @@ int k3huf_set_decoder_variant(int variant);
  * the larger symbol), the canonical assignment of k3huf_build.
  *  h_tensors[t]: n_values[t] (>= 1) little-endian bf16 values;
  *  chunk_syms: values per indexed chunk (>= 1);
+ *  sub_syms: values per sub-stream of a chunk (a divisor of chunk_syms;
+ *    0, a non-divisor, or chunk_syms * 12 > 65535 give one sub-stream);
  *  shared_table: nonzero = one table for the whole layer, else one per tensor;
  *  n_threads: worker threads (0 = hardware concurrency);
  *  h_blob / blob_cap: output; with h_blob NULL only *blob_bytes is set. */
 int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tensors, const uint64_t *n_values,
-                       uint32_t chunk_syms, int shared_table, int n_threads,
+                       uint32_t chunk_syms, uint32_t sub_syms, int shared_table, int n_threads,
                        void *h_blob, size_t blob_cap, size_t *blob_bytes);
 
 /* Streaming ring: layers held in pinned host memory are copied to device

@@ -20,7 +20,7 @@ import numpy as np
 from . import _build
 
 OK, E_ARG, E_EMPTY, E_OVERSUB, E_BADLEN, E_FORMAT, E_CUDA, E_NOMEM = 0, -1, -2, -3, -4, -5, -6, -7
-ST_BADCODE, ST_OVERRUN, ST_INDEX, ST_HEADER = 1, 2, 4, 8
+ST_BADCODE, ST_OVERRUN, ST_INDEX, ST_HEADER, ST_TIMEOUT = 1, 2, 4, 8, 16
 MAXLEN = 12
 STRIPE_VALUES = 1 << 25
 
@@ -43,7 +43,8 @@ class K3HufError(RuntimeError):
 class LayerInfo(ctypes.Structure):
     _fields_ = [("chunk_syms", ctypes.c_uint32), ("n_tables", ctypes.c_uint32), ("n_tensors", ctypes.c_uint32),
                 ("n_stripes", ctypes.c_uint32), ("raw_bytes", ctypes.c_uint64), ("blob_bytes", ctypes.c_uint64),
-                ("out_bytes", ctypes.c_uint64), ("hdr_bytes", ctypes.c_uint32), ("stripe_values", ctypes.c_uint32)]
+                ("out_bytes", ctypes.c_uint64), ("hdr_bytes", ctypes.c_uint32), ("stripe_values", ctypes.c_uint32),
+                ("sub_syms", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 class TensorInfo(ctypes.Structure):
@@ -79,10 +80,11 @@ def _lib():
             L.k3huf_layer_info.argtypes = [_vp, _sz, ctypes.POINTER(LayerInfo)]
             L.k3huf_tensor_info.argtypes = [_vp, _sz, ctypes.c_uint32, ctypes.POINTER(TensorInfo)]
             L.k3huf_decode_layer.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp, _vp]
-            L.k3huf_decode_stripe.argtypes = [_vp, ctypes.c_uint32, _vp, _sz, ctypes.c_uint32, _vp, _vp, _vp]
+            L.k3huf_decode_stripe.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32, _vp, _sz, ctypes.c_uint32, _vp,
+                                              _vp, _vp]
             L.k3huf_set_decoder_variant.argtypes = [ctypes.c_int]
             L.k3huf_encode_layer.argtypes = [ctypes.c_uint32, ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint64),
-                                             ctypes.c_uint32, ctypes.c_int, ctypes.c_int, _vp, _sz,
+                                             ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, ctypes.c_int, _vp, _sz,
                                              ctypes.POINTER(_sz)]
             L.k3huf_ring_create.argtypes = [_sz, ctypes.c_int, ctypes.POINTER(_vp)]
             L.k3huf_ring_run.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(_vp), ctypes.POINTER(_sz),
@@ -164,8 +166,9 @@ def tensor_info(hdr, t: int) -> dict:
 
 
 def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, threads: int = 0,
-                 out: np.ndarray | None = None) -> np.ndarray:
-    """Container bytes of a layer of bf16 tensors (numpy uint16 / torch bf16 CPU)."""
+                 out: np.ndarray | None = None, sub_syms: int = 512) -> np.ndarray:
+    """Container bytes of a layer of bf16 tensors (numpy uint16 / torch bf16
+    CPU); chunk_syms values per indexed chunk, sub_syms per sub-stream."""
     arrs = []
     for t in tensors:
         if hasattr(t, "view") and hasattr(t, "dtype") and str(getattr(t, "dtype", "")) == "torch.bfloat16":
@@ -177,14 +180,14 @@ def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, th
     nv = (ctypes.c_uint64 * n)(*[a.size for a in arrs])
     size = _sz(0)
     L = _lib()
-    _check(L.k3huf_encode_layer(n, ptrs, nv, chunk_syms, int(shared_table), threads, None, 0, ctypes.byref(size)),
-           "k3huf_encode_layer")
+    _check(L.k3huf_encode_layer(n, ptrs, nv, chunk_syms, sub_syms, int(shared_table), threads, None, 0,
+                                ctypes.byref(size)), "k3huf_encode_layer")
     if out is None:
         out = np.empty(size.value, dtype=np.uint8)
     elif out.size < size.value:
         raise ValueError("output buffer too small")
-    _check(L.k3huf_encode_layer(n, ptrs, nv, chunk_syms, int(shared_table), threads, out.ctypes.data, out.size,
-                                ctypes.byref(size)), "k3huf_encode_layer")
+    _check(L.k3huf_encode_layer(n, ptrs, nv, chunk_syms, sub_syms, int(shared_table), threads, out.ctypes.data,
+                                out.size, ctypes.byref(size)), "k3huf_encode_layer")
     return out[: size.value]
 
 
@@ -198,16 +201,16 @@ def decode_layer(hdr, d_layer, d_out, d_status, stream=None, layer_bytes: int | 
                                      _dptr(d_status), _stream(stream)), "k3huf_decode_layer")
 
 
-def decode_stripe(codelen, chunk_syms: int, d_stripe, stripe_bytes: int, n_values: int, d_out, d_status,
-                  stream=None) -> None:
+def decode_stripe(codelen, chunk_syms: int, sub_syms: int, d_stripe, stripe_bytes: int, n_values: int, d_out,
+                  d_status, stream=None) -> None:
     cl = np.zeros(256, dtype=np.uint8)
     cl[: len(codelen)] = np.asarray(codelen, dtype=np.uint8)
-    _check(_lib().k3huf_decode_stripe(cl.ctypes.data, chunk_syms, _dptr(d_stripe), stripe_bytes, n_values,
+    _check(_lib().k3huf_decode_stripe(cl.ctypes.data, chunk_syms, sub_syms, _dptr(d_stripe), stripe_bytes, n_values,
                                       _dptr(d_out), _dptr(d_status), _stream(stream)), "k3huf_decode_stripe")
 
 
 def set_decoder_variant(variant: int) -> None:
-    """0 = double-symbol table (default), 1 = single-symbol table."""
+    """Most codes per table lookup: 0 = default (3), 1, 2 or 3."""
     _check(_lib().k3huf_set_decoder_variant(variant), "k3huf_set_decoder_variant")
 
 

@@ -13,19 +13,25 @@
 // chunk, thousands per stripe) and a double-symbol table (two symbols per
 // lookup when both codes fit in the 12-bit window).
 //
-// GPU mapping (no tensor cores: this is a bit-serial scan, bound by HBM):
-//  - a CTA of 4 warps decodes 128 consecutive chunks of one stripe; lane
-//    = chunk.  The CTA first builds the single- and double-symbol tables in
-//    shared memory from the stripe's codelen[256];
-//  - each lane reads its chunk's bits with 16-byte read-only loads, one
-//    block ahead, into a 64-bit MSB-first accumulator;
-//  - decoded high bytes are packed four at a time in registers and stored
-//    to a per-lane ring in shared memory; every 64 values the warp merges
-//    its 32 chunks' high bytes with their raw low bytes (8-byte loads
-//    issued one round early) into coalesced 16-byte bf16 stores;
-//  - a chunk that ends away from the next chunk's recorded bit offset, or
-//    an undecodable window, sets a status bit; loops are bounded by the
-//    value counts and every load is clamped inside the stripe.
+// GPU mapping (no tensor cores: a bit-serial scan bound by HBM bandwidth):
+//  - the sub-stream index splits every chunk into independently decodable
+//    sub-streams; lane = sub-stream.  A work item is 128 consecutive
+//    sub-streams (a CTA of 4 warps); their bits are one contiguous range of
+//    the stripe's stream, staged into shared memory by one TMA bulk copy
+//    (cp.async.bulk + mbarrier, bounded wait).  A persistent grid walks
+//    contiguous item ranges and rebuilds the code table only when it changes;
+//  - each lookup reads the 12-bit window at its bit position with a funnel
+//    shift of two shared words (no per-lane refill branch) and emits up to
+//    three codes from a multi-symbol table; the warp loops on a warp-uniform
+//    condition, so lanes never diverge;
+//  - decoded high bytes go to a per-lane row in shared memory; every 64
+//    values the warp merges its 32 sub-streams' high bytes with their raw
+//    low bytes (8-byte loads issued one round early) into coalesced 16-byte
+//    bf16 stores;
+//  - a sub-stream that ends away from the next recorded bit offset, or an
+//    undecodable window, sets a status bit; every loop is bounded by value
+//    counts, every shared/global read index is clamped, and the only wait
+//    (the bulk copy's mbarrier) has an iteration limit.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -42,21 +48,24 @@ void set_cuda_error(int code) { g_last_cuda_error = code; }
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
+constexpr int kThreads = 32 * kWarps;         // sub-streams per work item
 constexpr int kRound = 64;                    // values per lane between merges
-constexpr int kRingWords = 2 * kRound / 4;    // per-lane ring of two rounds, in 32-bit words
-constexpr int kLaneStride = 192;              // bytes per lane row of the ring (bank spread)
+constexpr int kRowBytes = 132;                // per-lane high-byte row: 2 rounds + 2 spill + pad (33 words)
+constexpr int kRowLimit = 2 * kRound - 1;     // a lane decodes only while its row has room for 3 more bytes
+constexpr uint32_t kBitBuf = 32768;           // bytes of staged bit stream per pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
-
-// double-symbol entry: [7:0] sym1 [15:8] sym2 [19:16] len1 [23:20] bits used
-// [25:24] symbols emitted (1 or 2) [31] no code starts at this window
-constexpr uint32_t kBad = 1u << 31;
 constexpr int kMaxDevices = 64;
+constexpr int kMinBlocksPerSm = 3;
+constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
 
-constexpr size_t kSmemLut2 = 4096 * sizeof(uint32_t);
-constexpr size_t kSmemLut1 = 4096 * sizeof(uint16_t);
-constexpr size_t kSmemRing = size_t(kWarps) * 32 * kLaneStride;
-constexpr size_t kSmemBytes = kSmemLut2 + kSmemLut1 + kSmemRing;
+// Multi-symbol table entry:
+//   [23:0] up to three symbols, first in the low byte
+//   [25:24] number of symbols (1..3)  [29:26] bits consumed  [30] no code here
+constexpr uint32_t kBad = 1u << 30;
+
+constexpr size_t kSmemLut = 4096 * sizeof(uint32_t);
+constexpr size_t kSmemRows = size_t(kThreads) * kRowBytes;
+constexpr size_t kSmemBytes = kSmemLut + kBitBuf + 16 + kSmemRows;
 
 struct StripeTask {
     const uint8_t *stripe;      // device: stripe header
@@ -64,7 +73,7 @@ struct StripeTask {
     uint64_t stripe_bytes;
     uint32_t n_values;
     uint32_t table;
-    uint32_t cta_begin;         // first CTA of this stripe in the launch
+    uint32_t item_begin;        // first work item of this stripe in the launch
     uint32_t reserved;
 };
 
@@ -73,15 +82,56 @@ struct DecodeParams {
     uint32_t *status;
     uint32_t n_tasks;
     uint32_t chunk_syms;
+    uint32_t sub_syms;
+    uint32_t n_items;
     uint8_t inline_table[256];
     StripeTask task[kMaxTasks];
 };
 
 __device__ __forceinline__ uint32_t bswap32(uint32_t x) { return __byte_perm(x, 0, 0x0123); }
 
-// 64-bit MSB-first bit window over one chunk's stream, refilled 32 bits at a
-// time from a queue of 16-byte blocks read one block ahead.
-struct BitReader {
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// global -> shared bulk copy (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 64-bit MSB-first bit window over one sub-stream read straight from
+// global memory (16-byte read-only loads, one block ahead) -- used for
+// sub-streams too long to stage in shared memory.
+struct GlobalBits {
     uint64_t acc;            // valid bits at the top
     int cnt;                 // number of valid bits in acc
     uint4 q;                 // current block, front word in q.x
@@ -89,7 +139,8 @@ struct BitReader {
     uint4 nxt;               // prefetched next block
     const uint4 *p;          // block after nxt
     const uint4 *last;       // last block inside the stripe's stream
-    uint32_t nref;           // 32-bit refills done (for the end position)
+    uint32_t nref;           // 32-bit refills done
+    uint32_t start;          // first bit
 
     __device__ __forceinline__ uint4 load(const uint4 *b) const { return __ldg(b <= last ? b : last); }
 
@@ -109,6 +160,7 @@ struct BitReader {
 
     __device__ __forceinline__ void init(const uint4 *blocks, const uint4 *last_block, uint32_t bitoff) {
         last = last_block;
+        start = bitoff;
         const uint4 *b = blocks + (bitoff >> 7);
         q = load(b);
         nxt = load(b + 1);
@@ -123,26 +175,34 @@ struct BitReader {
         nref = 0;
     }
 
-    __device__ __forceinline__ void refill() {
+    // top 32 bits of the window, with at least 32 valid bits
+    __device__ __forceinline__ uint32_t window() {
         if (cnt <= 32) {
             acc |= uint64_t(pop()) << (32 - cnt);
             cnt += 32;
             ++nref;
         }
+        return uint32_t(acc >> 32);
+    }
+
+    __device__ __forceinline__ void advance(uint32_t t) {
+        acc <<= t;
+        cnt -= int(t);
     }
 
     // absolute bit position of the next unread bit
-    __device__ __forceinline__ uint32_t position(uint32_t bitoff) const {
-        return bitoff + 64u - (bitoff & 31u) + 32u * nref - uint32_t(cnt);
+    __device__ __forceinline__ uint32_t position() const {
+        return start + 64u - (start & 31u) + 32u * nref - uint32_t(cnt);
     }
 };
 
-// Build the single-symbol table (uint16 (sym << 4) | len, 0 = no code) and
-// the double-symbol table in shared memory from codelen[256].  Returns
-// false (uniformly across the CTA) when the table fails the Kraft check.
-template <bool kDouble>
-__device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *lut1, uint32_t *lut2) {
-    __shared__ uint8_t s_len[256];
+// Build the multi-symbol table in shared memory from codelen[256]; the
+// single-symbol table (sym << 4) | len is built first in `scratch` (8 KB).
+// s_len keeps the code lengths for the end-of-stream fix-up.  Returns
+// false, uniformly across the CTA, when the table fails the Kraft check.
+// All threads of the CTA must call it.
+template <int kSyms>
+__device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *lut1, uint32_t *lut, uint8_t *s_len) {
     __shared__ uint8_t s_rank[256];
     __shared__ uint8_t s_sorted[256];
     __shared__ uint32_t s_first[K3HUF_MAXLEN + 1], s_count[K3HUF_MAXLEN + 1], s_off[K3HUF_MAXLEN + 2];
@@ -215,32 +275,38 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
         }
     }
     __syncthreads();
+    // multi-symbol table: follow up to kSyms codes inside the 12-bit window
     for (uint32_t e = tid; e < 4096u; e += kThreads) {
-        const uint32_t a = lut1[e];
-        const uint32_t l1 = a & 15u;
+        uint32_t a = lut1[e];
+        uint32_t used = a & 15u;
         uint32_t ent;
-        if (l1 == 0) {
-            ent = kBad | (1u << 24) | (1u << 20) | (1u << 16);
+        if (used == 0) {
+            ent = kBad | (1u << 24) | (1u << 26);          // emit symbol 0, consume one bit
         } else {
-            ent = (a >> 4) | (l1 << 16) | (l1 << 20) | (1u << 24);
-            if (kDouble) {
-                const uint32_t b = lut1[(e << l1) & 4095u];
-                const uint32_t l2 = b & 15u;
-                if (l2 != 0 && l1 + l2 <= K3HUF_MAXLEN)
-                    ent = (a >> 4) | ((b >> 4) << 8) | (l1 << 16) | ((l1 + l2) << 20) | (2u << 24);
+            uint32_t syms = a >> 4, n = 1;
+#pragma unroll
+            for (int k = 1; k < kSyms; ++k) {
+                const uint32_t b = lut1[(e << used) & 4095u];
+                const uint32_t l = b & 15u;
+                if (n == uint32_t(k) && l != 0 && used + l <= K3HUF_MAXLEN) {
+                    syms |= (b >> 4) << (8 * k);
+                    used += l;
+                    n += 1;
+                }
             }
+            ent = syms | (n << 24) | (used << 26);
         }
-        lut2[e] = ent;
+        lut[e] = ent;
     }
     __syncthreads();
     return true;
 }
 
-__device__ __forceinline__ uint32_t find_task(const DecodeParams &P, uint32_t cta) {
+__device__ __forceinline__ uint32_t find_task(const DecodeParams &P, uint32_t item) {
     uint32_t lo = 0, hi = P.n_tasks - 1;
     while (lo < hi) {
         const uint32_t mid = (lo + hi + 1) >> 1;
-        if (P.task[mid].cta_begin <= cta) lo = mid; else hi = mid - 1;
+        if (P.task[mid].item_begin <= item) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
@@ -248,231 +314,339 @@ __device__ __forceinline__ uint32_t find_task(const DecodeParams &P, uint32_t ct
 __device__ __forceinline__ uint32_t interleave_lo(uint32_t even4, uint32_t hi4) { return __byte_perm(even4, hi4, 0x5140); }
 __device__ __forceinline__ uint32_t interleave_hi(uint32_t even4, uint32_t hi4) { return __byte_perm(even4, hi4, 0x7362); }
 
-template <bool kDouble, bool kVec>
-__global__ void __launch_bounds__(kThreads)
-decode_kernel(const __grid_constant__ DecodeParams P) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint32_t *lut2 = reinterpret_cast<uint32_t *>(smem);
-    uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemLut2);
-    uint8_t *ring_base = smem + kSmemLut2 + kSmemLut1;
-    __shared__ uint32_t s_hdr[8];
-    __shared__ int s_hdr_ok;
-
-    const uint32_t ti = find_task(P, blockIdx.x);
-    const StripeTask &T = P.task[ti];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t chunk_syms = P.chunk_syms;
-
-    // stripe header (device copy) against the host's expectations
-    if (tid == 0) {
-        const uint32_t *h = reinterpret_cast<const uint32_t *>(T.stripe);
-        for (int i = 0; i < 8; ++i) s_hdr[i] = h[i];
-        const uint32_t n = T.n_values;
-        const uint32_t nch = (n + chunk_syms - 1) / chunk_syms;
-        const uint64_t huff_bits = uint64_t(s_hdr[4]) | (uint64_t(s_hdr[5]) << 32);
-        const uint32_t bits_off = s_hdr[6], even_off = s_hdr[7];
-        const uint64_t bits_need = ((huff_bits + 7) / 8 + 15) / 16 * 16 + kBitsSlack;
-        bool ok = s_hdr[0] == kStripeMagic && s_hdr[2] == n && s_hdr[3] == nch &&
-                  bits_off == (K3HUF_STRIPE_HDR_BYTES + 4u * nch + 15u) / 16u * 16u &&
-                  even_off % 16 == 0 && huff_bits <= uint64_t(K3HUF_MAXLEN) * n && huff_bits >= n &&
-                  uint64_t(even_off) >= bits_off + bits_need && uint64_t(even_off) + n <= T.stripe_bytes;
-        if (P.tables) ok = ok && s_hdr[1] == T.table;
-        s_hdr_ok = ok;
-        if (!ok) atomicOr(P.status, K3HUF_ST_HEADER);
-    }
-    __syncthreads();
-    if (!s_hdr_ok) return;
-
-    const uint8_t *codelen = P.tables ? P.tables + 256ull * T.table : P.inline_table;
-    if (!build_tables<kDouble>(codelen, lut1, lut2)) {
-        if (tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
-        return;
-    }
-
-    const uint32_t n = T.n_values;
-    const uint32_t nch = s_hdr[3];
-    const uint32_t huff_bits = s_hdr[4];          // < 2^32 for a valid stripe (<= 12 * 2^25)
-    const uint8_t *bits = T.stripe + s_hdr[6];
-    const uint8_t *even = T.stripe + s_hdr[7];
-    const uint4 *blocks = reinterpret_cast<const uint4 *>(bits);
-    const uint4 *last_block = reinterpret_cast<const uint4 *>(even) - 1;
-    const uint32_t *bitoff = reinterpret_cast<const uint32_t *>(T.stripe + K3HUF_STRIPE_HDR_BYTES);
-    uint8_t *out = T.out;
-
-    const uint32_t cta_chunk0 = (blockIdx.x - T.cta_begin) * kThreads;
-    const uint32_t warp_chunk0 = cta_chunk0 + uint32_t(warp) * 32u;
-    if (warp_chunk0 >= nch) return;               // whole warp idle (no CTA-wide sync below)
-
-    // this lane's chunk
-    const uint32_t my_chunk = warp_chunk0 + uint32_t(lane);
-    const bool active = my_chunk < nch;
-    const uint32_t my_v0 = my_chunk * chunk_syms;
-    const uint32_t my_len = active ? min(chunk_syms, n - my_v0) : 0u;
-    const uint32_t my_off = active ? bitoff[my_chunk] : 0u;
-    const uint32_t my_end = active ? (my_chunk + 1 < nch ? bitoff[my_chunk + 1] : huff_bits) : 0u;
-
-    uint8_t *ring = ring_base + size_t(warp) * 32 * kLaneStride;
-    uint32_t *my_ring = reinterpret_cast<uint32_t *>(ring + lane * kLaneStride);
-
-    BitReader rd;
-    rd.init(blocks, last_block, active ? min(my_off, huff_bits) : 0u);
-    uint64_t ob = 0;        // pending high bytes, first one lowest
-    uint32_t obn = 0;       // number pending
-    uint32_t wq = 0;        // words flushed to the ring
-    uint32_t op = 0;        // values decoded
-    uint32_t bad = 0;
-
-    // rounds: every lane of the warp runs the same number
-    const uint32_t warp_last_chunk = min(warp_chunk0 + 31u, nch - 1u);
-    const uint32_t warp_max_len = min(chunk_syms, n - warp_chunk0 * chunk_syms);
-    const uint32_t n_rounds = (warp_max_len + kRound - 1) / kRound;
-    (void)warp_last_chunk;
-
-    // merge-phase assignment (vector path): piece i of this lane is chunk
-    // (i * 4 + lane / 8) of the warp, values [round*64 + (lane % 8) * 8, +8)
-    const uint32_t sub = uint32_t(lane) & 7u;
-    uint2 ev[8];
-    uint32_t m_len[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t c = warp_chunk0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
-        m_len[i] = c < nch ? min(chunk_syms, n - c * chunk_syms) : 0u;
-        ev[i] = make_uint2(0, 0);
-    }
-    auto load_even = [&](uint32_t round) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t c = warp_chunk0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
-            const uint32_t v = round * kRound + sub * 8u;
-            if (kVec && v < m_len[i])
-                ev[i] = __ldg(reinterpret_cast<const uint2 *>(even + size_t(c) * chunk_syms + v));
-        }
-    };
-    load_even(0);
-
-    for (uint32_t r = 0; r < n_rounds; ++r) {
-        const uint32_t target = min(my_len, (r + 1) * uint32_t(kRound));
-        while (op < target) {
-            uint32_t v, nn;
-            if (op + 4 <= my_len) {
-                rd.refill();
-                const uint32_t e0 = lut2[uint32_t(rd.acc >> 52)];
-                const uint32_t t0 = (e0 >> 20) & 15u;
-                rd.acc <<= t0;
-                const uint32_t e1 = lut2[uint32_t(rd.acc >> 52)];
-                const uint32_t t1 = (e1 >> 20) & 15u;
-                rd.acc <<= t1;
-                rd.cnt -= int(t0 + t1);
-                bad |= e0 | e1;
-                const uint32_t n0 = (e0 >> 24) & 3u;
-                v = (e0 & 0xFFFFu) | ((e1 & 0xFFFFu) << (8u * n0));
-                nn = n0 + ((e1 >> 24) & 3u);
-            } else {
-                rd.refill();
-                const uint32_t a = lut1[uint32_t(rd.acc >> 52)];
-                uint32_t l = a & 15u;
-                if (l == 0) {
-                    bad |= kBad;
-                    l = 1;
-                }
-                rd.acc <<= l;
-                rd.cnt -= int(l);
-                v = a >> 4;
-                nn = 1;
-            }
-            ob |= uint64_t(v) << (8u * obn);
-            obn += nn;
-            op += nn;
-            if (obn >= 4) {
-                my_ring[wq & (kRingWords - 1)] = uint32_t(ob);
-                ++wq;
-                ob >>= 32;
-                obn -= 4;
-            }
-        }
-        if (active && op >= my_len && obn > 0) {      // chunk done: flush the partial word
-            my_ring[wq & (kRingWords - 1)] = uint32_t(ob);
-            ++wq;
-            ob = 0;
-            obn = 0;
-        }
-        __syncwarp();
-        if (kVec) {
-            uint2 cur[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) cur[i] = ev[i];
-            if (r + 1 < n_rounds) load_even(r + 1);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t v = r * kRound + sub * 8u;
-                if (v >= m_len[i]) continue;
-                const uint32_t cw = uint32_t(i) * 4u + uint32_t(lane >> 3);
-                const uint32_t c = warp_chunk0 + cw;
-                const uint2 h = *reinterpret_cast<const uint2 *>(ring + cw * kLaneStride + (r & 1u) * kRound + sub * 8u);
-                uint4 o;
-                o.x = interleave_lo(cur[i].x, h.x);
-                o.y = interleave_hi(cur[i].x, h.x);
-                o.z = interleave_lo(cur[i].y, h.y);
-                o.w = interleave_hi(cur[i].y, h.y);
-                uint8_t *dst = out + 2 * (size_t(c) * chunk_syms + v);
-                if (v + 8 <= m_len[i]) {
-                    *reinterpret_cast<uint4 *>(dst) = o;
-                } else {
-                    const uint32_t k = m_len[i] - v;   // 1..7 values left in the chunk
-                    uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
-#pragma unroll
-                    for (uint32_t j = 0; j < 8; ++j) {
-                        const uint32_t w = j < 2 ? o.x : j < 4 ? o.y : j < 6 ? o.z : o.w;
-                        if (j < k) d16[j] = uint16_t(w >> (16 * (j & 1)));
-                    }
-                }
-            }
-        } else if (active) {
-            // scalar path for chunk sizes that break 8-value alignment:
-            // each lane writes its own chunk's values
-            const uint32_t a = r * kRound, b = min(my_len, a + kRound);
-            const uint8_t *hb = reinterpret_cast<const uint8_t *>(my_ring);
-            for (uint32_t v = a; v < b; ++v) {
-                const uint32_t lo = even[size_t(my_v0) + v];
-                const uint32_t hi = hb[v & (2 * kRound - 1)];
-                out[2 * (size_t(my_v0) + v)] = uint8_t(lo);
-                out[2 * (size_t(my_v0) + v) + 1] = uint8_t(hi);
-            }
-        }
-        __syncwarp();
-    }
-
-    uint32_t st = 0;
-    if (active) {
-        if (bad & kBad) st |= K3HUF_ST_BADCODE;
-        const uint32_t pos = rd.position(min(my_off, huff_bits));
-        if (pos > huff_bits || my_off > huff_bits) st |= K3HUF_ST_OVERRUN;
-        if (pos != my_end) st |= K3HUF_ST_INDEX;
-    }
-    st = __reduce_or_sync(0xffffffffu, st);
-    if (lane == 0 && st) atomicOr(P.status, st);
+// Validate the device copy of a stripe header against the launch's view of it.
+__device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, uint32_t hdr[8]) {
+    const uint32_t *h = reinterpret_cast<const uint32_t *>(T.stripe);
+    for (int i = 0; i < 8; ++i) hdr[i] = h[i];
+    const uint32_t n = T.n_values, cs = P.chunk_syms, ss = P.sub_syms;
+    const uint32_t nch = (n + cs - 1) / cs;
+    const uint64_t huff_bits = uint64_t(hdr[4]) | (uint64_t(hdr[5]) << 32);
+    const uint32_t bits_off = hdr[6], even_off = hdr[7];
+    const uint64_t bits_need = ((huff_bits + 7) / 8 + 15) / 16 * 16 + kBitsSlack;
+    const uint64_t index = 4ull * nch + 2ull * nch * (cs / ss - 1);
+    bool ok = hdr[0] == kStripeMagic && hdr[2] == n && hdr[3] == nch &&
+              bits_off == (K3HUF_STRIPE_HDR_BYTES + index + 15) / 16 * 16 && even_off % 16 == 0 &&
+              huff_bits <= uint64_t(K3HUF_MAXLEN) * n && huff_bits >= n &&
+              uint64_t(even_off) >= bits_off + bits_need && uint64_t(even_off) + n <= T.stripe_bytes;
+    if (P.tables) ok = ok && hdr[1] == T.table;
+    return ok;
 }
 
-template <bool kDouble, bool kVec>
-int launch(const DecodeParams &P, uint32_t n_ctas, cudaStream_t stream) {
-    static bool attr_set[kMaxDevices] = {};   // per device; setting it twice is harmless
+template <int kSyms, bool kVec, bool kStaged>
+__global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
+decode_kernel(const __grid_constant__ DecodeParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
+    uint32_t *bitbuf = reinterpret_cast<uint32_t *>(smem + kSmemLut);
+    uint8_t *rows = smem + kSmemLut + kBitBuf + 16;
+    __shared__ uint8_t s_len[256];
+    __shared__ uint32_t s_hdr[8];
+    __shared__ uint32_t s_off[kThreads], s_end[kThreads];
+    __shared__ uint32_t s_pass_lo[kThreads + 1];
+    __shared__ int s_state, s_npass;
+    __shared__ __align__(8) uint64_t s_bar;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t cs = P.chunk_syms, ss = P.sub_syms, S = cs / ss;
+    const uint32_t per = (P.n_items + gridDim.x - 1) / gridDim.x;
+    const uint32_t it0 = blockIdx.x * per, it1 = min(P.n_items, it0 + per);
+    int table_built = -1;
+    int table_bad = 0;
+    uint32_t phase = 0;
+
+    if (tid == 0) {
+        mbar_init(&s_bar);
+        fence_proxy_async();
+    }
+    __syncthreads();
+
+    for (uint32_t item = it0; item < it1; ++item) {
+        const uint32_t ti = find_task(P, item);
+        const StripeTask &T = P.task[ti];
+        const int table = P.tables ? int(T.table) : 0;
+        __syncthreads();                           // previous item fully consumed
+        if (table != table_built) {
+            const uint8_t *codelen = P.tables ? P.tables + 256ull * T.table : P.inline_table;
+            table_bad = !build_tables<kSyms>(codelen, reinterpret_cast<uint16_t *>(bitbuf), lut, s_len);
+            table_built = table;
+            if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
+        }
+        if (tid == 0) {
+            uint32_t h[8];
+            const bool ok = stripe_header_ok(P, T, h);
+            for (int i = 0; i < 8; ++i) s_hdr[i] = h[i];
+            if (!ok && item == T.item_begin) atomicOr(P.status, K3HUF_ST_HEADER);
+            s_state = ok && !table_bad;
+        }
+        __syncthreads();
+        if (!s_state) continue;
+
+        const uint32_t n = T.n_values;
+        const uint32_t nch = s_hdr[3];
+        const uint32_t huff_bits = s_hdr[4];      // < 2^32 for a valid stripe (<= 12 * 2^25)
+        const uint8_t *stripe = T.stripe;
+        const uint8_t *bits = stripe + s_hdr[6];
+        const uint8_t *even = stripe + s_hdr[7];
+        const uint32_t *chunk_off = reinterpret_cast<const uint32_t *>(stripe + K3HUF_STRIPE_HDR_BYTES);
+        const uint16_t *sub_off = reinterpret_cast<const uint16_t *>(stripe + K3HUF_STRIPE_HDR_BYTES + 4ull * nch);
+        uint8_t *out = T.out;
+        const uint32_t n_streams = nch * S;
+        const uint32_t g0 = (item - T.item_begin) * kThreads;
+
+        // this thread's sub-stream g = g0 + tid: values [g*ss, g*ss + len)
+        const uint32_t g = g0 + uint32_t(tid);
+        const bool active = g < n_streams && uint64_t(g) * ss < n;
+        const uint32_t my_len = active ? min(ss, n - g * ss) : 0u;
+        uint32_t my_off = 0, my_end = 0;
+        if (active) {
+            const uint32_t c = g / S, k = g - c * S;
+            const uint32_t base = chunk_off[c];
+            my_off = base + (k ? uint32_t(sub_off[size_t(c) * (S - 1) + k - 1]) : 0u);
+            my_end = k + 1 < S ? base + sub_off[size_t(c) * (S - 1) + k]
+                               : (c + 1 < nch ? chunk_off[c + 1] : huff_bits);
+        }
+        // clamp so that a corrupt index cannot move a read outside the stream
+        const uint32_t c_off = min(my_off, huff_bits), c_end = min(max(my_end, c_off), huff_bits);
+        s_off[tid] = c_off;
+        s_end[tid] = c_end;
+        __syncthreads();
+        if (!kStaged) {
+            if (tid == 0) {
+                uint32_t nact = 0;
+                for (uint32_t t = 0; t < uint32_t(kThreads); ++t) {
+                    const uint32_t gg = g0 + t;
+                    if (gg < n_streams && uint64_t(gg) * ss < n) nact = t + 1;
+                }
+                s_pass_lo[0] = 0;
+                s_pass_lo[1] = nact;
+                s_npass = 1;
+            }
+        } else if (tid == 0) {
+            // active streams are a prefix; split them into passes whose bits fit the buffer
+            uint32_t nact = 0;
+            for (uint32_t t = 0; t < uint32_t(kThreads); ++t) {
+                const uint32_t gg = g0 + t;
+                if (gg < n_streams && uint64_t(gg) * ss < n) nact = t + 1;
+            }
+            int np = 0;
+            uint32_t a = 0;
+            while (a < nact) {
+                const uint32_t lo = (s_off[a] >> 7) << 4;
+                uint32_t b = a + 1;
+                while (b < nact && ((s_end[b] + 7) / 8 + 15) / 16 * 16 + 16 - lo <= kBitBuf) ++b;
+                s_pass_lo[np++] = a;
+                a = b;
+            }
+            s_pass_lo[np] = nact;
+            s_npass = np;
+        }
+        __syncthreads();
+        const int npass = s_npass;
+
+        for (int ps = 0; ps < npass; ++ps) {
+            const uint32_t pa = s_pass_lo[ps], pb = s_pass_lo[ps + 1];
+            uint32_t byte_lo = 0, nbytes = 32;
+            if (kStaged) {
+                byte_lo = (s_off[pa] >> 7) << 4;
+                const uint32_t byte_hi = ((s_end[pb - 1] + 7) / 8 + 15) / 16 * 16 + 16;
+                // a corrupt index may claim more bits than fit: reads are clamped below
+                nbytes = min(byte_hi - byte_lo, kBitBuf);
+                if (tid == 0) {
+                    fence_proxy_async();             // earlier generic reads of the buffer come first
+                    mbar_arrive_expect_tx(&s_bar, nbytes);
+                    bulk_g2s(bitbuf, bits + byte_lo, nbytes, &s_bar);
+                }
+                // bounded wait for the copy
+                uint32_t polls = 0;
+                bool landed = false;
+                while (!(landed = mbar_try_wait(&s_bar, phase)) && ++polls < kWaitLimit) {
+                }
+                phase ^= 1u;
+                const int ok_all = __syncthreads_and(landed ? 1 : 0);
+                if (!ok_all) {
+                    if (tid == 0) atomicOr(P.status, K3HUF_ST_TIMEOUT);
+                    // let the copy in flight land (again bounded) before giving up
+                    polls = 0;
+                    while (!landed && !(landed = mbar_try_wait(&s_bar, phase ^ 1u)) && ++polls < kWaitLimit) {
+                    }
+                    return;
+                }
+                // stream words MSB-first in each 32-bit word
+                for (uint32_t w = tid; w < nbytes / 4; w += kThreads) bitbuf[w] = bswap32(bitbuf[w]);
+                __syncthreads();
+            }
+
+            const bool in_pass = uint32_t(tid) >= pa && uint32_t(tid) < pb;
+            const uint32_t len = in_pass ? my_len : 0u;
+            uint32_t bp = in_pass ? c_off - byte_lo * 8u : 0u;
+            const uint32_t max_word = nbytes / 4 - 2;
+            GlobalBits gb;
+            if (!kStaged)
+                gb.init(reinterpret_cast<const uint4 *>(bits), reinterpret_cast<const uint4 *>(even) - 1, c_off);
+            uint32_t prod = 0, cons = 0, bad = 0;
+            uint32_t pre_pos = c_off, pre_prod = 0, e_last = 0;
+            uint8_t *row = rows + size_t(tid) * kRowBytes;
+            const uint8_t *wrows = rows + size_t(warp) * 32 * kRowBytes;
+
+            // rounds: the same number for every lane of the warp
+            const uint32_t wlen = __reduce_max_sync(0xffffffffu, len);
+            const uint32_t n_rounds = (wlen + kRound - 1) / kRound;
+            const uint32_t warp_g0 = g0 + uint32_t(warp) * 32u;
+
+            // merge-phase assignment (vector path): piece i of this lane is the
+            // warp's sub-stream (i * 4 + lane / 8), values [r*64 + (lane % 8) * 8, +8)
+            const uint32_t sub = uint32_t(lane) & 7u;
+            uint2 ev[8];
+            uint32_t m_len[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t t = uint32_t(warp) * 32u + uint32_t(i) * 4u + uint32_t(lane >> 3);
+                const uint32_t gi = g0 + t;
+                m_len[i] = (t >= pa && t < pb) ? min(ss, n - gi * ss) : 0u;
+                ev[i] = make_uint2(0, 0);
+            }
+            auto load_even = [&](uint32_t round) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t gi = warp_g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
+                    const uint32_t v = round * kRound + sub * 8u;
+                    if (kVec && v < m_len[i])
+                        ev[i] = __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v));
+                }
+            };
+            load_even(0);
+
+            for (uint32_t r = 0; r < n_rounds; ++r) {
+                const uint32_t target = min(len, (r + 1) * uint32_t(kRound));
+                // decode until every lane of the warp holds this round's values
+                while (__any_sync(0xffffffffu, prod < target)) {
+                    const bool go = prod < len && prod - cons <= uint32_t(kRowLimit - 3) + 1u;
+                    uint32_t win;
+                    if (kStaged) {
+                        const uint32_t i = min(bp >> 5, max_word);
+                        const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1];
+                        win = __funnelshift_l(w1, w0, bp);
+                    } else {
+                        win = gb.window();
+                    }
+                    const uint32_t e = lut[win >> 20];
+                    if (go) {
+                        uint8_t *dst = row + (prod - cons);
+                        dst[0] = uint8_t(e);
+                        if (kSyms > 1) dst[1] = uint8_t(e >> 8);
+                        if (kSyms > 2) dst[2] = uint8_t(e >> 16);
+                        const uint32_t t = (e >> 26) & 15u;
+                        pre_prod = prod;
+                        e_last = e;
+                        if (kStaged) {
+                            pre_pos = bp;
+                            bp += t;
+                        } else {
+                            pre_pos = gb.position();
+                            gb.advance(t);
+                        }
+                        prod += (e >> 24) & 3u;
+                        bad |= e;
+                    }
+                }
+                __syncwarp();
+                if (kVec) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t v = r * kRound + sub * 8u;
+                        if (v >= m_len[i]) continue;
+                        const uint32_t gw = uint32_t(i) * 4u + uint32_t(lane >> 3);
+                        const uint32_t gi = warp_g0 + gw;
+                        const uint8_t *hrow = wrows + gw * kRowBytes + sub * 8u;
+                        const uint32_t hx = *reinterpret_cast<const uint32_t *>(hrow);
+                        const uint32_t hy = *reinterpret_cast<const uint32_t *>(hrow + 4);
+                        uint4 o;
+                        o.x = interleave_lo(ev[i].x, hx);
+                        o.y = interleave_hi(ev[i].x, hx);
+                        o.z = interleave_lo(ev[i].y, hy);
+                        o.w = interleave_hi(ev[i].y, hy);
+                        uint8_t *dst = out + 2 * (size_t(gi) * ss + v);
+                        if (v + 8 <= m_len[i]) {
+                            *reinterpret_cast<uint4 *>(dst) = o;
+                        } else {
+                            const uint32_t kk = m_len[i] - v;   // 1..7 values left in the sub-stream
+                            uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
+#pragma unroll
+                            for (uint32_t j = 0; j < 8; ++j) {
+                                const uint32_t w = j < 2 ? o.x : j < 4 ? o.y : j < 6 ? o.z : o.w;
+                                if (j < kk) d16[j] = uint16_t(w >> (16 * (j & 1)));
+                            }
+                        }
+                    }
+                    if (r + 1 < n_rounds) load_even(r + 1);   // in flight while the next round decodes
+                } else if (len) {
+                    // scalar path for sub-stream sizes that break 8-value alignment
+                    const uint32_t a = r * kRound, b = min(len, a + kRound);
+                    const size_t v0 = size_t(g) * ss;
+                    for (uint32_t v = a; v < b; ++v) {
+                        out[2 * (v0 + v)] = even[v0 + v];
+                        out[2 * (v0 + v) + 1] = row[v - a];
+                    }
+                }
+                __syncwarp();
+                // drop the merged round from this lane's row
+                {
+                    uint32_t *rw = reinterpret_cast<uint32_t *>(row);
+#pragma unroll
+                    for (int k = 0; k < (kRowBytes - 4 * (kRound / 4)) / 4; ++k) rw[k] = rw[k + kRound / 4];
+                }
+                cons += kRound;
+            }
+
+            uint32_t st = 0;
+            if (len) {
+                if (bad & kBad) st |= K3HUF_ST_BADCODE;
+                // exact end: the last lookup may have emitted codes past the
+                // sub-stream's end; re-walk the ones inside by their lengths
+                uint32_t pos = kStaged ? bp : gb.position();
+                if (prod > len) {
+                    pos = pre_pos;
+                    for (uint32_t k = 0; k < len - pre_prod; ++k) pos += s_len[(e_last >> (8 * k)) & 0xFFu];
+                }
+                if (kStaged) pos += byte_lo * 8u;
+                if (my_off > huff_bits || my_end > huff_bits) st |= K3HUF_ST_OVERRUN;
+                if (pos != my_end) st |= K3HUF_ST_INDEX;
+            }
+            st = __reduce_or_sync(0xffffffffu, st);
+            if (lane == 0 && st) atomicOr(P.status, st);
+            __syncthreads();                         // buffer free for the next pass / item
+        }
+    }
+}
+
+template <int kSyms, bool kVec, bool kStaged>
+int launch(DecodeParams &P, cudaStream_t stream) {
+    static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
+    static int grid_max[kMaxDevices] = {};
     int dev = 0;
-    cudaError_t e0 = cudaGetDevice(&dev);
-    if (e0 != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        set_cuda_error(int(e0));
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        set_cuda_error(int(e));
         return K3HUF_E_CUDA;
     }
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<kDouble, kVec>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+        e = cudaFuncSetAttribute(decode_kernel<kSyms, kVec, kStaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kSmemBytes));
+        int sms = 0, per_sm = 0;
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kSyms, kVec, kStaged>, kThreads,
+                                                              kSmemBytes);
         if (e != cudaSuccess) {
             set_cuda_error(int(e));
             return K3HUF_E_CUDA;
         }
+        grid_max[dev] = std::max(1, sms * std::max(1, per_sm));
         attr_set[dev] = true;
     }
-    decode_kernel<kDouble, kVec><<<n_ctas, kThreads, kSmemBytes, stream>>>(P);
-    cudaError_t e = cudaGetLastError();
+    const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(grid_max[dev]));
+    decode_kernel<kSyms, kVec, kStaged><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_cuda_error(int(e));
         return K3HUF_E_CUDA;
@@ -480,16 +654,33 @@ int launch(const DecodeParams &P, uint32_t n_ctas, cudaStream_t stream) {
     return K3HUF_OK;
 }
 
-int launch_tasks(DecodeParams &P, uint32_t n_ctas, cudaStream_t stream, int mode) {
-    const bool vec = P.chunk_syms % 8 == 0;
-    if (mode == 1) return vec ? launch<false, true>(P, n_ctas, stream) : launch<false, false>(P, n_ctas, stream);
-    return vec ? launch<true, true>(P, n_ctas, stream) : launch<true, false>(P, n_ctas, stream);
+// Decoder variant: the most codes one lookup emits (1, 2 or 3).
+int g_syms = 3;
+
+template <int kSyms>
+int launch_syms(DecodeParams &P, cudaStream_t stream) {
+    const bool vec = P.sub_syms % 8 == 0;
+    // a sub-stream's bits (at most 12 per value) must fit the shared buffer
+    const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= kBitBuf;
+    if (staged) return vec ? launch<kSyms, true, true>(P, stream) : launch<kSyms, false, true>(P, stream);
+    return vec ? launch<kSyms, true, false>(P, stream) : launch<kSyms, false, false>(P, stream);
+}
+
+int launch_tasks(DecodeParams &P, cudaStream_t stream) {
+    switch (g_syms) {
+        case 1: return launch_syms<1>(P, stream);
+        case 2: return launch_syms<2>(P, stream);
+        default: return launch_syms<3>(P, stream);
+    }
+}
+
+uint32_t items_of(uint32_t n_values, uint32_t cs, uint32_t ss) {
+    const uint64_t nch = (uint64_t(n_values) + cs - 1) / cs;
+    const uint64_t streams = nch * (cs / ss);
+    return uint32_t((streams + kThreads - 1) / kThreads);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Decoder variant: 0 = double-symbol table (default), 1 = single-symbol.
-int g_mode = 0;
 
 }  // namespace
 }  // namespace k3huf
@@ -499,8 +690,8 @@ using namespace k3huf;
 extern "C" int k3huf_last_cuda_error(void) { return g_last_cuda_error; }
 
 extern "C" int k3huf_set_decoder_variant(int variant) {
-    if (variant != 0 && variant != 1) return K3HUF_E_ARG;
-    g_mode = variant;
+    if (variant < 0 || variant > 3) return K3HUF_E_ARG;
+    g_syms = variant == 0 ? 3 : variant;
     return K3HUF_OK;
 }
 
@@ -514,14 +705,14 @@ extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, con
     if (layer_bytes < L.info.blob_bytes || out_bytes < L.info.out_bytes) return K3HUF_E_ARG;
     const uint8_t *blob = static_cast<const uint8_t *>(d_layer);
     uint8_t *out = static_cast<uint8_t *>(d_out);
-    const uint32_t cs = L.info.chunk_syms;
     DecodeParams P;
     P.tables = blob + K3HUF_LAYER_HDR_BYTES;
     P.status = d_status;
-    P.chunk_syms = cs;
+    P.chunk_syms = L.info.chunk_syms;
+    P.sub_syms = L.info.sub_syms;
     for (size_t s0 = 0; s0 < L.stripes.size(); s0 += kMaxTasks) {
         const size_t s1 = std::min(L.stripes.size(), s0 + kMaxTasks);
-        uint32_t ctas = 0;
+        uint32_t items = 0;
         P.n_tasks = uint32_t(s1 - s0);
         for (size_t s = s0; s < s1; ++s) {
             const StripeEntry &e = L.stripes[s];
@@ -531,32 +722,35 @@ extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, con
             t.stripe_bytes = e.stripe_bytes;
             t.n_values = e.n_values;
             t.table = e.table;
-            t.cta_begin = ctas;
+            t.item_begin = items;
             t.reserved = 0;
-            const uint32_t nch = (e.n_values + cs - 1) / cs;
-            ctas += (nch + kThreads - 1) / kThreads;
+            items += items_of(e.n_values, P.chunk_syms, P.sub_syms);
         }
-        rc = launch_tasks(P, ctas, static_cast<cudaStream_t>(stream), g_mode);
+        P.n_items = items;
+        rc = launch_tasks(P, static_cast<cudaStream_t>(stream));
         if (rc) return rc;
     }
     return K3HUF_OK;
 }
 
-extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms, const void *d_stripe,
-                                   size_t stripe_bytes, uint32_t n_values, void *d_out, uint32_t *d_status,
-                                   void *stream) {
+extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms, uint32_t sub_syms,
+                                   const void *d_stripe, size_t stripe_bytes, uint32_t n_values, void *d_out,
+                                   uint32_t *d_status, void *stream) {
     if (!codelen || !d_stripe || !d_out || !d_status || chunk_syms == 0 || n_values == 0 ||
-        n_values > K3HUF_STRIPE_VALUES)
+        n_values > K3HUF_STRIPE_VALUES || sub_syms == 0 || effective_sub_syms(chunk_syms, sub_syms) != sub_syms)
         return K3HUF_E_ARG;
     if (!aligned16(d_stripe) || !aligned16(d_out) || (reinterpret_cast<uintptr_t>(d_status) & 3u)) return K3HUF_E_ARG;
     int rc = k3huf_build(codelen, nullptr);
     if (rc) return rc;
     const uint32_t nch = (n_values + chunk_syms - 1) / chunk_syms;
-    if (stripe_bytes < align_up(K3HUF_STRIPE_HDR_BYTES + 4ull * nch, 16) + kBitsSlack + n_values) return K3HUF_E_ARG;
+    if (stripe_bytes < align_up(K3HUF_STRIPE_HDR_BYTES + index_bytes(nch, chunk_syms, sub_syms), 16) + kBitsSlack +
+                           n_values)
+        return K3HUF_E_ARG;
     DecodeParams P;
     P.tables = nullptr;
     P.status = d_status;
     P.chunk_syms = chunk_syms;
+    P.sub_syms = sub_syms;
     P.n_tasks = 1;
     for (int i = 0; i < 256; ++i) P.inline_table[i] = codelen[i];
     StripeTask &t = P.task[0];
@@ -565,7 +759,8 @@ extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_sy
     t.stripe_bytes = stripe_bytes;
     t.n_values = n_values;
     t.table = 0;
-    t.cta_begin = 0;
+    t.item_begin = 0;
     t.reserved = 0;
-    return launch_tasks(P, (nch + kThreads - 1) / kThreads, static_cast<cudaStream_t>(stream), g_mode);
+    P.n_items = items_of(n_values, chunk_syms, sub_syms);
+    return launch_tasks(P, static_cast<cudaStream_t>(stream));
 }

@@ -153,8 +153,10 @@ int parse_layer(const void *h_layer, size_t bytes, Layer *L) {
     in.stripe_values = rd32(p + 40);
     in.hdr_bytes = rd32(p + 44);
     in.out_bytes = rd64(p + 48);
+    in.sub_syms = rd32(p + 56);
     if (in.chunk_syms == 0 || in.n_tables == 0 || in.n_tensors == 0 || in.n_stripes == 0 ||
-        in.stripe_values != K3HUF_STRIPE_VALUES || in.hdr_bytes % 256 != 0)
+        in.stripe_values != K3HUF_STRIPE_VALUES || in.hdr_bytes % 256 != 0 || in.sub_syms == 0 ||
+        effective_sub_syms(in.chunk_syms, in.sub_syms) != in.sub_syms)
         return K3HUF_E_FORMAT;
     const uint64_t need = K3HUF_LAYER_HDR_BYTES + 256ull * in.n_tables + 32ull * in.n_tensors + 32ull * in.n_stripes;
     if (need > in.hdr_bytes || in.hdr_bytes > in.blob_bytes) return K3HUF_E_FORMAT;
@@ -187,7 +189,8 @@ int parse_layer(const void *h_layer, size_t bytes, Layer *L) {
             const uint64_t v0 = uint64_t(k) * K3HUF_STRIPE_VALUES;
             const uint64_t nv = std::min<uint64_t>(K3HUF_STRIPE_VALUES, te.n_values - v0);
             const uint64_t nch = (nv + in.chunk_syms - 1) / in.chunk_syms;
-            const uint64_t min_bytes = align_up(K3HUF_STRIPE_HDR_BYTES + 4 * nch, 16) + kBitsSlack + nv;
+            const uint64_t min_bytes =
+                align_up(K3HUF_STRIPE_HDR_BYTES + index_bytes(nch, in.chunk_syms, in.sub_syms), 16) + kBitsSlack + nv;
             if (se.n_values != nv || se.table != te.table || se.out_offset != te.out_offset + 2 * v0 ||
                 se.blob_offset % 256 != 0 || se.blob_offset < blob_end || se.stripe_bytes % 16 != 0 ||
                 se.stripe_bytes < min_bytes || se.stripe_bytes > in.blob_bytes - se.blob_offset ||
@@ -315,9 +318,11 @@ struct BitWriter {
 }  // namespace
 
 extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tensors, const uint64_t *n_values,
-                                  uint32_t chunk_syms, int shared_table, int n_threads, void *h_blob,
-                                  size_t blob_cap, size_t *blob_bytes) {
+                                  uint32_t chunk_syms, uint32_t sub_syms_req, int shared_table, int n_threads,
+                                  void *h_blob, size_t blob_cap, size_t *blob_bytes) {
     if (n_tensors == 0 || !h_tensors || !n_values || chunk_syms == 0 || !blob_bytes) return K3HUF_E_ARG;
+    const uint32_t sub_syms = effective_sub_syms(chunk_syms, sub_syms_req);
+    const uint32_t S = chunk_syms / sub_syms;
     for (uint32_t t = 0; t < n_tensors; ++t)
         if (!h_tensors[t] || n_values[t] == 0) return K3HUF_E_ARG;
     const int threads = n_threads > 0 ? n_threads : int(std::max(1u, std::thread::hardware_concurrency()));
@@ -389,7 +394,7 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
             uint64_t bits = 0;
             for (int s = 0; s < 256; ++s) bits += p.hist[s] * cl[s];
             p.huff_bits = bits;
-            p.bits_offset = uint32_t(align_up(K3HUF_STRIPE_HDR_BYTES + 4ull * p.n_chunks, 16));
+            p.bits_offset = uint32_t(align_up(K3HUF_STRIPE_HDR_BYTES + index_bytes(p.n_chunks, chunk_syms, sub_syms), 16));
             p.even_offset = uint32_t(p.bits_offset + align_up((bits + 7) / 8, 16) + kBitsSlack);
             p.stripe_bytes = p.even_offset + align_up(p.n, 16);
             pos = align_up(pos, 256);
@@ -415,6 +420,7 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
         wr32(blob + 40, K3HUF_STRIPE_VALUES);
         wr32(blob + 44, uint32_t(hdr));
         wr64(blob + 48, out);
+        wr32(blob + 56, sub_syms);
         std::memcpy(blob + K3HUF_LAYER_HDR_BYTES, codelen.data(), codelen.size());
         uint8_t *td = blob + K3HUF_LAYER_HDR_BYTES + 256ull * n_tables;
         uint8_t *sd = td + 32ull * n_tensors;
@@ -465,7 +471,7 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
             uint32_t first[kMaxLen + 1], count[kMaxLen + 1];
             canonical_codes(&codelen[256ull * tb], &code[256ull * tb], first, count);
         }
-        // per-chunk bit counts, in parallel over segments
+        // per-chunk bit counts and sub-stream starts, in parallel over segments
         std::vector<std::vector<uint32_t>> chunk_bits(sp.size());
         for (size_t i = 0; i < sp.size(); ++i) chunk_bits[i].assign(sp[i].n_chunks, 0);
         parallel_for(segs.size(), threads, [&](size_t i) {
@@ -473,12 +479,18 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
             const StripePlan &p = sp[g.stripe];
             const uint8_t *cl = &codelen[256ull * p.table];
             const uint8_t *x = static_cast<const uint8_t *>(h_tensors[p.tensor]) + 2 * p.v0;
+            uint8_t *sub = blob + p.blob_offset + K3HUF_STRIPE_HDR_BYTES + 4ull * p.n_chunks;
             // chunks that start inside this segment are summed whole here
             uint64_t c0 = (g.a + chunk_syms - 1) / chunk_syms;
             for (uint64_t c = c0; c * chunk_syms < g.b; ++c) {
                 const uint64_t a = c * chunk_syms, b = std::min<uint64_t>(p.n, a + chunk_syms);
                 uint32_t bits = 0;
-                for (uint64_t k = a; k < b; ++k) bits += cl[x[2 * k + 1]];
+                for (uint32_t k = 0; k < S; ++k) {
+                    const uint64_t ka = std::min(b, a + uint64_t(k) * sub_syms);
+                    const uint64_t kb = std::min(b, ka + sub_syms);
+                    if (k > 0) wr16(sub + 2 * (c * (S - 1) + (k - 1)), bits);
+                    for (uint64_t j = ka; j < kb; ++j) bits += cl[x[2 * j + 1]];
+                }
                 chunk_bits[g.stripe][c] = bits;
             }
         });

@@ -49,6 +49,18 @@ constexpr uint32_t kBitsSlack = 32;             // zero bytes after each padded 
 
 inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
+// Sub-streams per chunk actually used for a requested size (see k3huf.h).
+inline uint32_t effective_sub_syms(uint32_t chunk_syms, uint32_t sub_syms) {
+    if (sub_syms == 0 || chunk_syms % sub_syms != 0 || uint64_t(chunk_syms) * K3HUF_MAXLEN > 65535u)
+        return chunk_syms;
+    return sub_syms;
+}
+
+// Bytes of a stripe's chunk index plus sub-stream index.
+inline uint64_t index_bytes(uint64_t n_chunks, uint32_t chunk_syms, uint32_t sub_syms) {
+    return 4 * n_chunks + 2 * n_chunks * (chunk_syms / sub_syms - 1);
+}
+
 // Record a CUDA error code for k3huf_last_cuda_error (thread-local).
 void set_cuda_error(int code);
 

@@ -60,7 +60,8 @@ def lib():
             L.orc_canonical.argtypes = [_intp, ctypes.c_int, _u32p, _u32p, _u32p]
             L.orc_decode_window.argtypes = [_u8p, ctypes.c_int, ctypes.c_uint32, _intp]
             L.orc_encode_layer.argtypes = [ctypes.c_int, ctypes.POINTER(_u8p), _u64p, ctypes.c_uint32,
-                                           ctypes.c_int, ctypes.c_int, _u8p, ctypes.c_uint64, _u64p]
+                                           ctypes.c_uint32, ctypes.c_int, ctypes.c_int, _u8p, ctypes.c_uint64,
+                                           _u64p]
             L.orc_layer_info.argtypes = [_u8p, ctypes.c_uint64, _u64p]
             L.orc_decode_stripe_range.argtypes = [_u8p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                                   ctypes.c_uint32, _u8p]
@@ -145,19 +146,21 @@ def decode_window(codelen, window: int, maxlen: int = MAXLEN):
     return int(s), int(used.value)
 
 
-def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, maxlen: int = MAXLEN) -> np.ndarray:
-    """Container bytes (uint8) of a layer made of the given bf16 tensors (uint16 arrays)."""
+def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, maxlen: int = MAXLEN,
+                 sub_syms: int = 512) -> np.ndarray:
+    """Container bytes (uint8) of a layer made of the given bf16 tensors
+    (uint16 arrays); sub_syms = values per sub-stream (0: no sub index)."""
     ts = [np.ascontiguousarray(t, dtype=np.uint16).reshape(-1) for t in tensors]
     n = len(ts)
     ptrs = (_u8p * n)(*[_ptr(t.view(np.uint8)) for t in ts])
     nv = np.array([t.size for t in ts], dtype=np.uint64)
     size = ctypes.c_uint64(0)
-    rc = lib().orc_encode_layer(n, ptrs, _ptr(nv, _u64p), chunk_syms, int(shared_table), maxlen,
+    rc = lib().orc_encode_layer(n, ptrs, _ptr(nv, _u64p), chunk_syms, sub_syms, int(shared_table), maxlen,
                                 None, 0, ctypes.byref(size))
     if rc:
         raise ValueError(f"oracle encode failed: {rc}")
     out = np.zeros(size.value, dtype=np.uint8)
-    rc = lib().orc_encode_layer(n, ptrs, _ptr(nv, _u64p), chunk_syms, int(shared_table), maxlen,
+    rc = lib().orc_encode_layer(n, ptrs, _ptr(nv, _u64p), chunk_syms, sub_syms, int(shared_table), maxlen,
                                 _ptr(out), out.size, ctypes.byref(size))
     if rc:
         raise ValueError(f"oracle encode failed: {rc}")
@@ -165,12 +168,12 @@ def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, ma
 
 
 def layer_info(blob: np.ndarray) -> dict:
-    info = np.zeros(9, dtype=np.uint64)
+    info = np.zeros(10, dtype=np.uint64)
     rc = lib().orc_layer_info(_ptr(blob), blob.size, _ptr(info, _u64p))
     if rc:
         raise ValueError(f"not a k3huf layer: {rc}")
     keys = ["chunk_syms", "n_tables", "n_tensors", "n_stripes", "raw_bytes", "blob_bytes",
-            "hdr_bytes", "out_bytes", "maxlen"]
+            "hdr_bytes", "out_bytes", "maxlen", "sub_syms"]
     return {k: int(v) for k, v in zip(keys, info)}
 
 

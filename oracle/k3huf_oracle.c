@@ -42,8 +42,9 @@
  *      conflict-free on incomplete ones.
  *   R5 bit order: bit j of a stream is bit 7-(j%8) of byte j/8; the last
  *      byte is zero padded.
- *   R6 container, chunk index and padding: this project's own layout,
- *      version 1 (the article names only codelen[256] and the stripe order).
+ *   R6 container, chunk index, sub-stream index and padding: this
+ *      project's own layout, version 1 (the article names only
+ *      codelen[256] and the stripe order).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -314,7 +315,7 @@ static void put_bits(uint8_t *bytes, uint64_t *pos, uint32_t code, int len)
  *   0 u32 magic 'K3HF' | 4 u16 version | 6 u16 maxlen | 8 u32 chunk_syms
  *  12 u32 n_tables | 16 u32 n_tensors | 20 u32 n_stripes | 24 u64 raw_bytes
  *  32 u64 blob_bytes | 40 u32 stripe_values | 44 u32 hdr_bytes
- *  48 u64 out_bytes | 56 zero
+ *  48 u64 out_bytes | 56 u32 sub_syms | 60 zero
  * then codelen[256] per table, the tensor directory (32 B each:
  *   u32 table_id, u32 first_stripe, u32 n_stripes, u32 0, u64 n_values,
  *   u64 out_offset), the stripe directory (32 B each: u64 blob_offset,
@@ -324,7 +325,10 @@ static void put_bits(uint8_t *bytes, uint64_t *pos, uint32_t code, int len)
  *   0 u32 magic 'K3HS' | 4 u32 table_id | 8 u32 n_values | 12 u32 n_chunks
  *  16 u64 huff_bits | 24 u32 bits_offset | 28 u32 even_offset
  *  32 u32 chunk_bitoff[n_chunks]
- *  bits_offset = align16(32 + 4 n_chunks): the bit stream, padded with zero
+ *  then u16 sub_bitoff[n_chunks][S-1], S = chunk_syms / sub_syms: entry
+ *     k-1 of chunk c is the bit offset, relative to chunk c's first bit,
+ *     of the code of value min(k sub_syms, len_c) of the chunk
+ *  bits_offset = align16(32 + 4 n_chunks + 2 n_chunks (S-1)): the bit stream, padded with zero
  *     bytes to align16(ceil(huff_bits/8)) + 32 bytes
  *  even_offset = end of the padded bit stream: the n low bytes, then zero
  *     padding to a multiple of 16 (stripe_bytes = even_offset + align16(n))
@@ -339,15 +343,33 @@ typedef struct {
 
 static uint32_t n_chunks_of(uint64_t n, uint32_t chunk_syms) { return (uint32_t)((n + chunk_syms - 1) / chunk_syms); }
 
+/* Sub-streams per chunk.  A requested sub_syms that is 0, does not divide
+ * chunk_syms, or would let a relative offset exceed 16 bits (chunks longer
+ * than 65535 / 12 values) means no sub-stream index (one sub-stream). */
+static uint32_t effective_sub_syms(uint32_t chunk_syms, uint32_t sub_syms)
+{
+    if (sub_syms == 0 || chunk_syms % sub_syms != 0 || (uint64_t)chunk_syms * ORC_FMT_MAXLEN > 65535u)
+        return chunk_syms;
+    return sub_syms;
+}
+
+static uint64_t index_bytes(uint32_t nch, uint32_t chunk_syms, uint32_t sub_syms)
+{
+    uint64_t S = chunk_syms / sub_syms;
+    return 4ull * nch + 2ull * nch * (S - 1);
+}
+
 /* Encode a layer.  tensors[t] points at n_values[t] little-endian bf16
  * values.  shared_table != 0 gives one code table for the whole layer
  * (histogram summed over all tensors), else one table per tensor.  With
  * out == NULL only *blob_bytes is computed. */
 int orc_encode_layer(int n_tensors, const uint8_t *const *tensors, const uint64_t *n_values,
-                     uint32_t chunk_syms, int shared_table, int maxlen,
+                     uint32_t chunk_syms, uint32_t sub_syms_req, int shared_table, int maxlen,
                      uint8_t *out, uint64_t cap, uint64_t *blob_bytes)
 {
     if (n_tensors <= 0 || chunk_syms == 0 || maxlen < 1 || maxlen > 16) return ORC_E_ARG;
+    uint32_t sub_syms = effective_sub_syms(chunk_syms, sub_syms_req);
+    uint32_t S = chunk_syms / sub_syms;
     for (int t = 0; t < n_tensors; t++) if (n_values[t] == 0) return ORC_E_ARG;
     int n_tables = shared_table ? 1 : n_tensors;
     int (*lens)[256] = calloc((size_t)n_tables, sizeof *lens);
@@ -386,8 +408,8 @@ int orc_encode_layer(int n_tensors, const uint8_t *const *tensors, const uint64_
             uint64_t nv = n_values[t] - v0 < ORC_STRIPE_VALUES ? n_values[t] - v0 : ORC_STRIPE_VALUES;
             uint64_t bits = 0;
             for (uint64_t i = 0; i < nv; i++) bits += (uint64_t)lens[tp[t].table][tensors[t][2 * (v0 + i) + 1]];
-            uint64_t nch = n_chunks_of(nv, chunk_syms);
-            uint64_t bits_off = align_up(ORC_STRIPE_HDR + 4 * nch, 16);
+            uint32_t nch = n_chunks_of(nv, chunk_syms);
+            uint64_t bits_off = align_up(ORC_STRIPE_HDR + index_bytes(nch, chunk_syms, sub_syms), 16);
             uint64_t even_off = bits_off + align_up((bits + 7) / 8, 16) + ORC_BITS_SLACK;
             uint64_t sbytes = even_off + align_up(nv, 16);
             pos = align_up(pos, 256) + sbytes;
@@ -411,6 +433,7 @@ int orc_encode_layer(int n_tensors, const uint8_t *const *tensors, const uint64_
     put32(out + 40, ORC_STRIPE_VALUES);
     put32(out + 44, (uint32_t)hdr);
     put64(out + 48, outp);
+    put32(out + 56, sub_syms);
     for (int tb = 0; tb < n_tables; tb++)
         for (int s = 0; s < 256; s++) out[ORC_LAYER_HDR + 256 * tb + s] = (uint8_t)lens[tb][s];
     uint8_t *tdir = out + ORC_LAYER_HDR + 256 * n_tables;
@@ -437,13 +460,30 @@ int orc_encode_layer(int n_tensors, const uint8_t *const *tensors, const uint64_
             uint64_t v0 = (uint64_t)k * ORC_STRIPE_VALUES;
             uint64_t nv = n_values[t] - v0 < ORC_STRIPE_VALUES ? n_values[t] - v0 : ORC_STRIPE_VALUES;
             uint32_t nch = n_chunks_of(nv, chunk_syms);
-            uint64_t bits_off = align_up(ORC_STRIPE_HDR + 4ull * nch, 16);
+            uint64_t bits_off = align_up(ORC_STRIPE_HDR + index_bytes(nch, chunk_syms, sub_syms), 16);
             pos = align_up(pos, 256);
             uint8_t *st = out + pos;
             uint8_t *bytes = st + bits_off;
-            uint64_t bp = 0;
-            for (uint64_t i = 0; i < nv; i++) {
-                if (i % chunk_syms == 0) put32(st + ORC_STRIPE_HDR + 4 * (i / chunk_syms), (uint32_t)bp);
+            uint8_t *sub = st + ORC_STRIPE_HDR + 4ull * nch;
+            uint64_t bp = 0, chunk_start = 0;
+            for (uint64_t i = 0; i <= nv; i++) {
+                uint64_t c = i / chunk_syms, k = (i % chunk_syms) / sub_syms;
+                if (i < nv && i % chunk_syms == 0) {
+                    put32(st + ORC_STRIPE_HDR + 4 * c, (uint32_t)bp);
+                    chunk_start = bp;
+                }
+                /* sub-stream k (k >= 1) of chunk c starts at value c*chunk_syms + k*sub_syms */
+                if (i % sub_syms == 0 && k > 0 && i <= nv)
+                    put16(sub + 2 * (c * (S - 1) + (k - 1)), (uint32_t)(bp - chunk_start));
+                if (i == nv) {
+                    /* a short last chunk: its missing sub-stream starts sit at its end */
+                    uint64_t clast = (nv - 1) / chunk_syms;
+                    uint64_t used = nv - clast * chunk_syms;             /* values in the last chunk */
+                    for (uint64_t kk = 1; kk < S; kk++)
+                        if (kk * sub_syms >= used)
+                            put16(sub + 2 * (clast * (S - 1) + (kk - 1)), (uint32_t)(bp - chunk_start));
+                    break;
+                }
                 uint8_t s = tensors[t][2 * (v0 + i) + 1];
                 put_bits(bytes, &bp, code[s], ln[s]);
             }
@@ -473,10 +513,10 @@ int orc_encode_layer(int n_tensors, const uint8_t *const *tensors, const uint64_
 
 /* ---- container reading and bit-serial decoding ------------------------- */
 
-/* Header fields the Python side wants: fills info[0..8] =
+/* Header fields the Python side wants: fills info[0..9] =
  * chunk_syms, n_tables, n_tensors, n_stripes, raw_bytes, blob_bytes,
- * hdr_bytes, out_bytes, maxlen. */
-int orc_layer_info(const uint8_t *blob, uint64_t bytes, uint64_t info[9])
+ * hdr_bytes, out_bytes, maxlen, sub_syms. */
+int orc_layer_info(const uint8_t *blob, uint64_t bytes, uint64_t info[10])
 {
     if (bytes < ORC_LAYER_HDR) return ORC_E_FORMAT;
     if (get32(blob) != ORC_MAGIC_LAYER || get16(blob + 4) != ORC_VERSION) return ORC_E_FORMAT;
@@ -489,6 +529,8 @@ int orc_layer_info(const uint8_t *blob, uint64_t bytes, uint64_t info[9])
     info[6] = get32(blob + 44);
     info[7] = get64(blob + 48);
     info[8] = get16(blob + 6);
+    info[9] = get32(blob + 56);
+    if (info[0] == 0 || info[9] == 0 || info[0] % info[9] != 0) return ORC_E_FORMAT;
     return ORC_OK;
 }
 
@@ -501,10 +543,11 @@ int orc_layer_info(const uint8_t *blob, uint64_t bytes, uint64_t info[9])
 int orc_decode_stripe_range(const uint8_t *blob, uint64_t bytes, uint32_t s,
                             uint32_t first_chunk, uint32_t n_chunks_sel, uint8_t *out)
 {
-    uint64_t info[9];
+    uint64_t info[10];
     int rc = orc_layer_info(blob, bytes, info);
     if (rc) return rc;
     uint32_t chunk_syms = (uint32_t)info[0], n_tables = (uint32_t)info[1];
+    uint32_t sub_syms = (uint32_t)info[9], S = chunk_syms / sub_syms;
     uint32_t n_tensors = (uint32_t)info[2], n_stripes = (uint32_t)info[3];
     int maxlen = (int)info[8];
     if (s >= n_stripes || chunk_syms == 0) return ORC_E_ARG;
@@ -519,6 +562,8 @@ int orc_decode_stripe_range(const uint8_t *blob, uint64_t bytes, uint32_t s,
     uint64_t huff_bits = get64(st + 16);
     uint32_t bits_off = get32(st + 24), even_off = get32(st + 28);
     if (nch != n_chunks_of(nv, chunk_syms) || (uint64_t)even_off + nv > sbytes) return ORC_E_FORMAT;
+    if (bits_off < ORC_STRIPE_HDR + index_bytes(nch, chunk_syms, sub_syms)) return ORC_E_FORMAT;
+    const uint8_t *sub = st + ORC_STRIPE_HDR + 4ull * nch;
     orc_code code;
     rc = orc_code_init(&code, blob + ORC_LAYER_HDR + 256ull * table, maxlen);
     if (rc) return rc;
@@ -530,8 +575,12 @@ int orc_decode_stripe_range(const uint8_t *blob, uint64_t bytes, uint32_t s,
         uint64_t end = (c + 1 < nch) ? get32(st + ORC_STRIPE_HDR + 4ull * (c + 1)) : huff_bits;
         uint64_t i0 = (uint64_t)c * chunk_syms;
         uint64_t i1 = i0 + chunk_syms < nv ? i0 + chunk_syms : nv;
+        uint64_t cstart = bp;
         for (uint64_t i = i0; i < i1; i++) {
             int used;
+            uint64_t k = (i - i0) / sub_syms;
+            if ((i - i0) % sub_syms == 0 && k > 0 && get16(sub + 2 * ((uint64_t)c * (S - 1) + (k - 1))) != bp - cstart)
+                return ORC_E_FORMAT;
             if (bp >= huff_bits) return ORC_E_FORMAT;
             int sym = orc_decode_symbol(&code, stream_bit, &stream, bp, &used);
             if (sym < 0) return ORC_E_FORMAT;
@@ -540,6 +589,9 @@ int orc_decode_stripe_range(const uint8_t *blob, uint64_t bytes, uint32_t s,
             out[out_off + 2 * i + 1] = (uint8_t)sym;
         }
         if (bp != end) return ORC_E_FORMAT;
+        for (uint64_t k = 1; k < S; k++)           /* sub-streams starting at or past the chunk end */
+            if (k * sub_syms >= i1 - i0 && get16(sub + 2 * ((uint64_t)c * (S - 1) + (k - 1))) != bp - cstart)
+                return ORC_E_FORMAT;
     }
     return ORC_OK;
 }
@@ -548,7 +600,7 @@ int orc_decode_stripe_range(const uint8_t *blob, uint64_t bytes, uint32_t s,
  * left as they are). */
 int orc_decode_layer(const uint8_t *blob, uint64_t bytes, uint8_t *out)
 {
-    uint64_t info[9];
+    uint64_t info[10];
     int rc = orc_layer_info(blob, bytes, info);
     if (rc) return rc;
     for (uint32_t s = 0; s < (uint32_t)info[3]; s++) {

@@ -67,24 +67,26 @@ def check_parity(tensors, variant=0, **enc):
     return blob
 
 
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1, 2])
 def test_tiny(variant):
     check_parity([workloads.tiny()], variant)
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 7, 8, 9, 15, 16, 17, 63, 64, 65, 4095, 4096, 4097, 8191, 12289,
                                128 * 4096 - 1, 128 * 4096 + 1, 100_003])
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1, 2])
 def test_ragged_sizes(n, variant):
     check_parity([workloads.normal_tensor((n,), 0.02, seed=n)], variant)
 
 
-@pytest.mark.parametrize("chunk_syms", [1, 7, 8, 64, 256, 1000, 4096, 65536])
-def test_chunk_sizes(chunk_syms):
-    check_parity([workloads.normal_tensor((70_001,), 0.05, seed=9)], chunk_syms=chunk_syms)
+@pytest.mark.parametrize("chunk_syms,sub_syms", [(1, 0), (7, 0), (8, 0), (64, 0), (256, 0), (1000, 0), (4096, 0),
+                                                (65536, 0), (4096, 512), (4096, 256), (4096, 1024), (4096, 8),
+                                                (1000, 200), (1000, 8), (4096, 64), (2048, 512), (64, 16)])
+def test_chunk_sizes(chunk_syms, sub_syms):
+    check_parity([workloads.normal_tensor((70_001,), 0.05, seed=9)], chunk_syms=chunk_syms, sub_syms=sub_syms)
 
 
-@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("variant", [0, 1, 2])
 def test_degenerate_planes(variant):
     check_parity([workloads.single_symbol(50_001)], variant)
     check_parity([workloads.two_symbol(50_001)], variant)
@@ -132,7 +134,7 @@ def test_decode_stripe_entry():
         nv = int.from_bytes(blob[e + 24:e + 28].tobytes(), "little")
         out = torch.zeros(2 * nv, dtype=torch.uint8, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
-        k3.decode_stripe(blob[64:64 + 256], info["chunk_syms"], d_blob[off:], sb, nv, out, st)
+        k3.decode_stripe(blob[64:64 + 256], info["chunk_syms"], info["sub_syms"], d_blob[off:], sb, nv, out, st)
         torch.cuda.synchronize()
         assert st.item() == 0
         assert np.array_equal(out.cpu().numpy().view(np.uint16), x[s * (1 << 25): s * (1 << 25) + nv])
@@ -190,6 +192,8 @@ def test_fault_undecodable_window():
     blob[64 + 1] = 2
     blob[o + 16:o + 24] = np.frombuffer((15).to_bytes(8, "little"), np.uint8)
     blob[o + bits_off:o + bits_off + 2] = [0b10011100, 0b11100110]
+    so = o + 32 + 4 * 1                                # sub-stream starts past the end: all at bit 15
+    blob[so:so + 14] = np.frombuffer(np.full(7, 15, "<u2").tobytes(), np.uint8)
     assert oracle.decode_layer(blob)[0] == 0
     out, st, _ = gpu_decode(blob)
     assert st == 0 and np.array_equal(out[:24].view(np.uint16), x)

@@ -112,11 +112,12 @@ def test_encoder_matches_oracle_container(name):
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("chunk_syms", [1, 7, 1000, 65536, 1 << 21])
-def test_encoder_chunk_sizes_match_oracle(chunk_syms):
+@pytest.mark.parametrize("chunk_syms,sub_syms", [(1, 512), (7, 512), (1000, 512), (65536, 512), (1 << 21, 512),
+                                                (4096, 0), (4096, 256), (4096, 8), (1000, 200), (5000, 1000)])
+def test_encoder_chunk_sizes_match_oracle(chunk_syms, sub_syms):
     x = workloads.normal_tensor((300_001,), 0.05, 9)
-    assert np.array_equal(k3.encode_layer([x], chunk_syms=chunk_syms, threads=3),
-                          oracle.encode_layer([x], chunk_syms=chunk_syms))
+    assert np.array_equal(k3.encode_layer([x], chunk_syms=chunk_syms, sub_syms=sub_syms, threads=3),
+                          oracle.encode_layer([x], chunk_syms=chunk_syms, sub_syms=sub_syms))
 
 
 def test_encoder_shared_table_matches_oracle():
@@ -219,6 +220,7 @@ def test_decode_argument_checks_need_no_device():
     st = L.k3huf_decode_layer(b.ctypes.data, b.size, 4096, b.size - 1, 4096, 1 << 20, 4096, None)
     assert st == k3.E_ARG                              # device blob shorter than the container
     cl = np.zeros(256, np.uint8)
-    st = L.k3huf_decode_stripe(cl.ctypes.data, 4096, 4096, 1 << 20, 100, 4096, 4096, None)
+    st = L.k3huf_decode_stripe(cl.ctypes.data, 4096, 512, 4096, 1 << 20, 100, 4096, 4096, None)
     assert st == k3.E_EMPTY
     assert L.k3huf_set_decoder_variant(7) == k3.E_ARG
+    assert L.k3huf_set_decoder_variant(-1) == k3.E_ARG

@@ -29,7 +29,7 @@ def parse(blob):
         "maxlen": int.from_bytes(blob[6:8].tobytes(), "little"), "chunk_syms": _u32(blob, 8),
         "n_tables": _u32(blob, 12), "n_tensors": _u32(blob, 16), "n_stripes": _u32(blob, 20),
         "raw_bytes": _u64(blob, 24), "blob_bytes": _u64(blob, 32), "stripe_values": _u32(blob, 40),
-        "hdr_bytes": _u32(blob, 44), "out_bytes": _u64(blob, 48),
+        "hdr_bytes": _u32(blob, 44), "out_bytes": _u64(blob, 48), "sub_syms": _u32(blob, 56),
     }
     t0 = 64 + 256 * h["n_tables"]
     h["tables"] = [blob[64 + 256 * i: 64 + 256 * (i + 1)].copy() for i in range(h["n_tables"])]
@@ -49,6 +49,10 @@ def parse(blob):
                   n_chunks=_u32(blob, o + 12), huff_bits=_u64(blob, o + 16), bits_offset=_u32(blob, o + 24),
                   even_offset=_u32(blob, o + 28))
         st["chunk_bitoff"] = np.frombuffer(blob[o + 32: o + 32 + 4 * st["n_chunks"]].tobytes(), dtype="<u4")
+        S = h["chunk_syms"] // h["sub_syms"]
+        so = o + 32 + 4 * st["n_chunks"]
+        st["sub_bitoff"] = np.frombuffer(blob[so: so + 2 * st["n_chunks"] * (S - 1)].tobytes(),
+                                         dtype="<u2").reshape(st["n_chunks"], S - 1)
         h["stripes"].append(st)
     return h
 
@@ -77,8 +81,17 @@ def roundtrip(tensors, **kw):
     return blob, h
 
 
-def check_layout(blob, tensors, chunk_syms=4096, shared=False):
+def _expected_sub_syms(chunk_syms, sub_syms):
+    if sub_syms == 0 or chunk_syms % sub_syms or chunk_syms * 12 > 65535:
+        return chunk_syms
+    return sub_syms
+
+
+def check_layout(blob, tensors, chunk_syms=4096, shared=False, sub_syms=512):
     h = parse(blob)
+    ss = _expected_sub_syms(chunk_syms, sub_syms)
+    assert h["sub_syms"] == ss
+    S = chunk_syms // ss
     assert h["magic"] == b"K3HF" and h["version"] == 1 and h["maxlen"] == 12
     assert h["chunk_syms"] == chunk_syms and h["stripe_values"] == STRIPE_VALUES
     assert h["blob_bytes"] == blob.size and h["hdr_bytes"] % 256 == 0
@@ -111,7 +124,14 @@ def check_layout(blob, tensors, chunk_syms=4096, shared=False):
             per_chunk = np.add.reduceat(lens[hi], np.arange(0, xs.size, chunk_syms))
             assert np.array_equal(st["chunk_bitoff"].astype(np.int64), np.concatenate([[0], np.cumsum(per_chunk)[:-1]]))
             assert st["bits_offset"] % 16 == 0 and st["even_offset"] % 16 == 0
-            assert st["bits_offset"] >= 32 + 4 * st["n_chunks"]
+            assert st["bits_offset"] == -(-(32 + 4 * st["n_chunks"] + 2 * st["n_chunks"] * (S - 1)) // 16) * 16
+            # sub-stream index: relative bit offset of value min(k*ss, len) of each chunk
+            cum = np.concatenate([[0], np.cumsum(lens[hi])])
+            for c in range(st["n_chunks"]):
+                a = c * chunk_syms
+                ln_c = min(chunk_syms, xs.size - a)
+                for k in range(1, S):
+                    assert st["sub_bitoff"][c, k - 1] == cum[a + min(k * ss, ln_c)] - cum[a], (c, k)
             o = st["blob_offset"]
             nbytes = (st["huff_bits"] + 7) // 8
             assert st["even_offset"] == st["bits_offset"] + (-(-nbytes // 16)) * 16 + 32
@@ -213,6 +233,27 @@ def test_multi_stripe_tensor():
     assert h["stripes"][1]["n_values"] == 5003
 
 
+@pytest.mark.parametrize("chunk_syms,sub_syms", [(4096, 512), (4096, 256), (4096, 4096), (4096, 0), (4096, 1000),
+                                                (1024, 8), (8192, 512), (64, 16), (8, 1)])
+@pytest.mark.parametrize("n", [1, 4095, 4097, 30_001])
+def test_sub_stream_index(chunk_syms, sub_syms, n):
+    x = workloads.normal_tensor((n,), 0.03, seed=n + chunk_syms)
+    blob, _ = roundtrip([x], chunk_syms=chunk_syms, sub_syms=sub_syms)
+    check_layout(blob, [x], chunk_syms=chunk_syms, sub_syms=sub_syms)
+
+
+def test_corrupt_sub_index_is_rejected():
+    x = workloads.normal_tensor((20_000,), 0.02, seed=66)
+    blob = oracle.encode_layer([x])
+    h = parse(blob)
+    st = h["stripes"][0]
+    so = st["blob_offset"] + 32 + 4 * st["n_chunks"]
+    for entry in (0, 6, 7 * 4 + 6):                   # first, last of chunk 0, last of the short chunk 4
+        bad = blob.copy()
+        bad[so + 2 * entry] ^= 1
+        assert oracle.decode_layer(bad)[0] == oracle.E_FORMAT, entry
+
+
 def test_decode_chunks_matches_full_decode():
     x = workloads.normal_tensor((40_000,), 0.02, seed=4)
     blob = oracle.encode_layer([x])
@@ -266,6 +307,8 @@ def test_incomplete_code_invalid_window_is_rejected():
     blob[64 + 1] = 2                                   # table {0:1, 1:2}
     blob[o + 16: o + 24] = np.frombuffer((5).to_bytes(8, "little"), np.uint8)
     blob[o + st["bits_offset"]] = 0b10011000           # 1 00 1 1
+    so = o + 32 + 4 * st["n_chunks"]                   # sub-stream starts past the end: all at bit 5
+    blob[so: so + 14] = np.frombuffer(np.full(7, 5, "<u2").tobytes(), np.uint8)
     rc, out = oracle.decode_layer(blob)
     assert rc == 0 and np.array_equal(out[:8].view(np.uint16), x)
     bad = blob.copy()
