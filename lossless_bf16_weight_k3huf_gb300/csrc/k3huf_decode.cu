@@ -50,22 +50,23 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;         // sub-streams per work item
 constexpr int kRound = 64;                    // values per lane between merges
-constexpr int kRowBytes = 132;                // per-lane high-byte row: 2 rounds + 2 spill + pad (33 words)
-constexpr int kRowLimit = 2 * kRound - 1;     // a lane decodes only while its row has room for 3 more bytes
-constexpr uint32_t kBitBuf = 32768;           // bytes of staged bit stream per pass
+constexpr int kRowBytes = 132;                // per-lane high-byte row: 2 rounds + spill + pad (33 words)
+constexpr uint32_t kBitBuf = 30720;           // bytes of staged bit stream per pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
 constexpr int kMinBlocksPerSm = 3;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
+constexpr int kCols = 16;                     // copies of the first-level table (one per lane mod 16)
 
-// Multi-symbol table entry:
-//   [23:0] up to three symbols, first in the low byte
-//   [25:24] number of symbols (1..3)  [29:26] bits consumed  [30] no code here
-constexpr uint32_t kBad = 1u << 30;
-
-constexpr size_t kSmemLut = 4096 * sizeof(uint32_t);
+// First-level table, indexed by the next 8 bits, kCols interleaved copies so
+// that lanes of a half-warp never share a bank:
+//   [23:0] up to three symbols (first in the low byte)  [25:24] number of
+//   symbols, 0 when the first code is longer than 8 bits  [31:28] bits used.
+// Second level: the 4096-entry single-symbol table (sym << 4) | length.
+constexpr size_t kSmemL8 = 256 * kCols * sizeof(uint32_t);
+constexpr size_t kSmemL12 = 4096 * sizeof(uint16_t);
 constexpr size_t kSmemRows = size_t(kThreads) * kRowBytes;
-constexpr size_t kSmemBytes = kSmemLut + kBitBuf + 16 + kSmemRows;
+constexpr size_t kSmemBytes = kSmemL8 + kSmemL12 + kBitBuf + 16 + kSmemRows;
 
 struct StripeTask {
     const uint8_t *stripe;      // device: stripe header
@@ -196,13 +197,11 @@ struct GlobalBits {
     }
 };
 
-// Build the multi-symbol table in shared memory from codelen[256]; the
-// single-symbol table (sym << 4) | len is built first in `scratch` (8 KB).
-// s_len keeps the code lengths for the end-of-stream fix-up.  Returns
+// Build both table levels in shared memory from codelen[256].  Returns
 // false, uniformly across the CTA, when the table fails the Kraft check.
 // All threads of the CTA must call it.
 template <int kSyms>
-__device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *lut1, uint32_t *lut, uint8_t *s_len) {
+__device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *lut1, uint32_t *l8, uint8_t *s_len) {
     __shared__ uint8_t s_rank[256];
     __shared__ uint8_t s_sorted[256];
     __shared__ uint32_t s_first[K3HUF_MAXLEN + 1], s_count[K3HUF_MAXLEN + 1], s_off[K3HUF_MAXLEN + 2];
@@ -254,8 +253,8 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
         if (l) s_sorted[s_off[l] + s_rank[s]] = uint8_t(s);
     }
     __syncthreads();
-    // single-symbol table: each thread fills 32 consecutive windows, one
-    // search per run of equal entries
+    // single-symbol 12-bit table: each thread fills 32 consecutive windows,
+    // one search per run of equal entries
     {
         const uint32_t e0 = uint32_t(tid) * 32u, e1 = e0 + 32u;
         uint32_t e = e0;
@@ -275,28 +274,27 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
         }
     }
     __syncthreads();
-    // multi-symbol table: follow up to kSyms codes inside the 12-bit window
-    for (uint32_t e = tid; e < 4096u; e += kThreads) {
-        uint32_t a = lut1[e];
-        uint32_t used = a & 15u;
-        uint32_t ent;
-        if (used == 0) {
-            ent = kBad | (1u << 24) | (1u << 26);          // emit symbol 0, consume one bit
-        } else {
+    // first level: up to kSyms whole codes inside the next 8 bits
+    for (uint32_t x = tid; x < 256u; x += kThreads) {
+        const uint32_t w = x << 4;                   // the 8 bits at the top of a 12-bit window
+        const uint32_t a = lut1[w];
+        uint32_t used = a & 15u, ent = 0;
+        if (used != 0 && used <= 8) {
             uint32_t syms = a >> 4, n = 1;
 #pragma unroll
             for (int k = 1; k < kSyms; ++k) {
-                const uint32_t b = lut1[(e << used) & 4095u];
+                const uint32_t b = lut1[(w << used) & 4095u];
                 const uint32_t l = b & 15u;
-                if (n == uint32_t(k) && l != 0 && used + l <= K3HUF_MAXLEN) {
+                if (n == uint32_t(k) && l != 0 && used + l <= 8) {
                     syms |= (b >> 4) << (8 * k);
                     used += l;
                     n += 1;
                 }
             }
-            ent = syms | (n << 24) | (used << 26);
+            ent = syms | (n << 24) | (used << 28);
         }
-        lut[e] = ent;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) l8[x * kCols + c] = ent;
     }
     __syncthreads();
     return true;
@@ -332,17 +330,29 @@ __device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, uin
     return ok;
 }
 
+// The 12-bit second level as a first-level style entry (one symbol); an
+// undecodable window consumes one bit and raises `bad`.
+__device__ __forceinline__ uint32_t second_level(const uint16_t *lut1, uint32_t win, uint32_t &bad) {
+    const uint32_t a = lut1[win >> 20];
+    uint32_t l = a & 15u;
+    bad |= l == 0;
+    l += l == 0;
+    return (a >> 4) | (1u << 24) | (l << 28);
+}
+
 template <int kSyms, bool kVec, bool kStaged>
 __global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
 decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
-    uint32_t *bitbuf = reinterpret_cast<uint32_t *>(smem + kSmemLut);
-    uint8_t *rows = smem + kSmemLut + kBitBuf + 16;
+    uint32_t *l8 = reinterpret_cast<uint32_t *>(smem);
+    uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemL8);
+    uint32_t *bitbuf = reinterpret_cast<uint32_t *>(smem + kSmemL8 + kSmemL12);
+    uint8_t *rows = smem + kSmemL8 + kSmemL12 + kBitBuf + 16;
     __shared__ uint8_t s_len[256];
     __shared__ uint32_t s_hdr[8];
     __shared__ uint32_t s_off[kThreads], s_end[kThreads];
     __shared__ uint32_t s_pass_lo[kThreads + 1];
+    __shared__ uint32_t s_cut;
     __shared__ int s_state, s_npass;
     __shared__ __align__(8) uint64_t s_bar;
 
@@ -350,6 +360,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     const uint32_t cs = P.chunk_syms, ss = P.sub_syms, S = cs / ss;
     const uint32_t per = (P.n_items + gridDim.x - 1) / gridDim.x;
     const uint32_t it0 = blockIdx.x * per, it1 = min(P.n_items, it0 + per);
+    const uint32_t *l8col = l8 + (lane & (kCols - 1));
     int table_built = -1;
     int table_bad = 0;
     uint32_t phase = 0;
@@ -367,7 +378,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         __syncthreads();                           // previous item fully consumed
         if (table != table_built) {
             const uint8_t *codelen = P.tables ? P.tables + 256ull * T.table : P.inline_table;
-            table_bad = !build_tables<kSyms>(codelen, reinterpret_cast<uint16_t *>(bitbuf), lut, s_len);
+            table_bad = !build_tables<kSyms>(codelen, lut1, l8, s_len);
             table_built = table;
             if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
         }
@@ -409,36 +420,35 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         const uint32_t c_off = min(my_off, huff_bits), c_end = min(max(my_end, c_off), huff_bits);
         s_off[tid] = c_off;
         s_end[tid] = c_end;
-        __syncthreads();
+        // active sub-streams are a prefix of the item
+        const uint32_t nact = uint32_t(__syncthreads_count(active));
         if (!kStaged) {
             if (tid == 0) {
-                uint32_t nact = 0;
-                for (uint32_t t = 0; t < uint32_t(kThreads); ++t) {
-                    const uint32_t gg = g0 + t;
-                    if (gg < n_streams && uint64_t(gg) * ss < n) nact = t + 1;
-                }
                 s_pass_lo[0] = 0;
                 s_pass_lo[1] = nact;
                 s_npass = 1;
             }
-        } else if (tid == 0) {
-            // active streams are a prefix; split them into passes whose bits fit the buffer
-            uint32_t nact = 0;
-            for (uint32_t t = 0; t < uint32_t(kThreads); ++t) {
-                const uint32_t gg = g0 + t;
-                if (gg < n_streams && uint64_t(gg) * ss < n) nact = t + 1;
-            }
-            int np = 0;
+        } else {
+            // passes: longest runs of sub-streams whose bits fit the buffer
             uint32_t a = 0;
-            while (a < nact) {
+            int np = 0;
+            while (a < nact) {                      // CTA-uniform
+                if (tid == 0) s_cut = nact;
+                __syncthreads();
                 const uint32_t lo = (s_off[a] >> 7) << 4;
-                uint32_t b = a + 1;
-                while (b < nact && ((s_end[b] + 7) / 8 + 15) / 16 * 16 + 16 - lo <= kBitBuf) ++b;
-                s_pass_lo[np++] = a;
-                a = b;
+                const uint32_t t = uint32_t(tid);
+                if (t > a && t < nact && ((s_end[t] + 7) / 8 + 15) / 16 * 16 + 16 - lo > kBitBuf)
+                    atomicMin(&s_cut, t);
+                __syncthreads();
+                if (tid == 0) s_pass_lo[np] = a;
+                a = s_cut;
+                ++np;
+                __syncthreads();
             }
-            s_pass_lo[np] = nact;
-            s_npass = np;
+            if (tid == 0) {
+                s_pass_lo[np] = nact;
+                s_npass = np;
+            }
         }
         __syncthreads();
         const int npass = s_npass;
@@ -472,19 +482,20 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     return;
                 }
                 // stream words MSB-first in each 32-bit word
-                for (uint32_t w = tid; w < nbytes / 4; w += kThreads) bitbuf[w] = bswap32(bitbuf[w]);
+                const uint32_t nw = nbytes / 4;
+#pragma unroll 4
+                for (uint32_t w = tid; w < nw; w += kThreads) bitbuf[w] = bswap32(bitbuf[w]);
                 __syncthreads();
             }
 
             const bool in_pass = uint32_t(tid) >= pa && uint32_t(tid) < pb;
             const uint32_t len = in_pass ? my_len : 0u;
             uint32_t bp = in_pass ? c_off - byte_lo * 8u : 0u;
-            const uint32_t max_word = nbytes / 4 - 2;
+            const uint32_t max_word = nbytes / 4 - 3;
             GlobalBits gb;
             if (!kStaged)
                 gb.init(reinterpret_cast<const uint4 *>(bits), reinterpret_cast<const uint4 *>(even) - 1, c_off);
             uint32_t prod = 0, cons = 0, bad = 0;
-            uint32_t pre_pos = c_off, pre_prod = 0, e_last = 0;
             uint8_t *row = rows + size_t(tid) * kRowBytes;
             const uint8_t *wrows = rows + size_t(warp) * 32 * kRowBytes;
 
@@ -516,56 +527,83 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             };
             load_even(0);
 
+            // three first-level lookups per 64-bit window write at most
+            // 3 * kSyms bytes from row position prod - cons (up to 3 bytes
+            // per lookup, the unused ones overwritten later)
+            constexpr uint32_t kBurst = 3 * kSyms;
+            constexpr uint32_t kRoom = kRowBytes - 2 - kBurst;
+            const uint32_t *hrow[8];
+            size_t vbase[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t gw = uint32_t(i) * 4u + uint32_t(lane >> 3);
+                hrow[i] = reinterpret_cast<const uint32_t *>(wrows + gw * kRowBytes + sub * 8u);
+                vbase[i] = size_t(warp_g0 + gw) * ss + sub * 8u;
+            }
+
             for (uint32_t r = 0; r < n_rounds; ++r) {
                 const uint32_t target = min(len, (r + 1) * uint32_t(kRound));
+                // a burst is allowed while it can neither pass the sub-stream's
+                // end nor overrun the row
+                const uint32_t burst_lim = min(len >= kBurst ? len - kBurst : 0u, cons + kRoom);
+                const bool burst_ok = len >= kBurst;
+                uint8_t *const rbase = row - cons;      // row position of value v is rbase + v
                 // decode until every lane of the warp holds this round's values
                 while (__any_sync(0xffffffffu, prod < target)) {
-                    const bool go = prod < len && prod - cons <= uint32_t(kRowLimit - 3) + 1u;
-                    uint32_t win;
-                    if (kStaged) {
+                    if (kStaged && burst_ok && prod <= burst_lim) {
                         const uint32_t i = min(bp >> 5, max_word);
-                        const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1];
-                        win = __funnelshift_l(w1, w0, bp);
-                    } else {
-                        win = gb.window();
-                    }
-                    const uint32_t e = lut[win >> 20];
-                    if (go) {
-                        uint8_t *dst = row + (prod - cons);
-                        dst[0] = uint8_t(e);
-                        if (kSyms > 1) dst[1] = uint8_t(e >> 8);
-                        if (kSyms > 2) dst[2] = uint8_t(e >> 16);
-                        const uint32_t t = (e >> 26) & 15u;
-                        pre_prod = prod;
-                        e_last = e;
-                        if (kStaged) {
-                            pre_pos = bp;
+                        const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1], w2 = bitbuf[i + 2];
+                        uint32_t hi = __funnelshift_l(w1, w0, bp), lo = __funnelshift_l(w2, w1, bp);
+                        uint8_t *dst = rbase + prod;
+                        uint32_t e = 0;
+#pragma unroll
+                        for (int k = 0; k < 3; ++k) {
+                            e = l8col[(hi >> 24) * kCols];
+                            const uint32_t t = e >> 28;
+                            dst[0] = uint8_t(e);
+                            if (kSyms > 1) dst[1] = uint8_t(e >> 8);
+                            if (kSyms > 2) dst[2] = uint8_t(e >> 16);
+                            dst += (e >> 24) & 3u;
                             bp += t;
-                        } else {
-                            pre_pos = gb.position();
-                            gb.advance(t);
+                            hi = __funnelshift_l(lo, hi, t);
+                            lo <<= t;
                         }
-                        prod += (e >> 24) & 3u;
-                        bad |= e;
+                        if (((e >> 24) & 3u) == 0) {
+                            // a code longer than 8 bits stopped the window: one exact code
+                            e = second_level(lut1, hi, bad);
+                            dst[0] = uint8_t(e);
+                            dst += 1;
+                            bp += e >> 28;
+                        }
+                        prod = uint32_t(dst - rbase);
+                    } else if (prod < len && prod - cons <= kRoom) {
+                        // exact tail: one code at a time
+                        uint32_t win;
+                        if (kStaged) {
+                            const uint32_t i = min(bp >> 5, max_word);
+                            win = __funnelshift_l(bitbuf[i + 1], bitbuf[i], bp);
+                        } else {
+                            win = gb.window();
+                        }
+                        const uint32_t e = second_level(lut1, win, bad);
+                        rbase[prod] = uint8_t(e);
+                        prod += 1;
+                        if (kStaged) bp += e >> 28; else gb.advance(e >> 28);
                     }
                 }
                 __syncwarp();
                 if (kVec) {
+                    const uint32_t v = r * kRound + sub * 8u;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const uint32_t v = r * kRound + sub * 8u;
                         if (v >= m_len[i]) continue;
-                        const uint32_t gw = uint32_t(i) * 4u + uint32_t(lane >> 3);
-                        const uint32_t gi = warp_g0 + gw;
-                        const uint8_t *hrow = wrows + gw * kRowBytes + sub * 8u;
-                        const uint32_t hx = *reinterpret_cast<const uint32_t *>(hrow);
-                        const uint32_t hy = *reinterpret_cast<const uint32_t *>(hrow + 4);
+                        const uint32_t hx = hrow[i][0], hy = hrow[i][1];
                         uint4 o;
                         o.x = interleave_lo(ev[i].x, hx);
                         o.y = interleave_hi(ev[i].x, hx);
                         o.z = interleave_lo(ev[i].y, hy);
                         o.w = interleave_hi(ev[i].y, hy);
-                        uint8_t *dst = out + 2 * (size_t(gi) * ss + v);
+                        uint8_t *dst = out + 2 * (vbase[i] + r * kRound);
                         if (v + 8 <= m_len[i]) {
                             *reinterpret_cast<uint4 *>(dst) = o;
                         } else {
@@ -593,22 +631,15 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 {
                     uint32_t *rw = reinterpret_cast<uint32_t *>(row);
 #pragma unroll
-                    for (int k = 0; k < (kRowBytes - 4 * (kRound / 4)) / 4; ++k) rw[k] = rw[k + kRound / 4];
+                    for (int k = 0; k < (kRowBytes - kRound) / 4; ++k) rw[k] = rw[k + kRound / 4];
                 }
                 cons += kRound;
             }
 
             uint32_t st = 0;
             if (len) {
-                if (bad & kBad) st |= K3HUF_ST_BADCODE;
-                // exact end: the last lookup may have emitted codes past the
-                // sub-stream's end; re-walk the ones inside by their lengths
-                uint32_t pos = kStaged ? bp : gb.position();
-                if (prod > len) {
-                    pos = pre_pos;
-                    for (uint32_t k = 0; k < len - pre_prod; ++k) pos += s_len[(e_last >> (8 * k)) & 0xFFu];
-                }
-                if (kStaged) pos += byte_lo * 8u;
+                if (bad) st |= K3HUF_ST_BADCODE;
+                uint32_t pos = kStaged ? bp + byte_lo * 8u : gb.position();
                 if (my_off > huff_bits || my_end > huff_bits) st |= K3HUF_ST_OVERRUN;
                 if (pos != my_end) st |= K3HUF_ST_INDEX;
             }
