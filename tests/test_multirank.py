@@ -1,0 +1,43 @@
+"""The benchmark's replica scaling logic with two gloo ranks on CPU: the
+path has no exchange step, so ranks only agree on the slowest rank's time
+and the job's value counts every rank's decoded bytes."""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, times, result):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms = bench.max_over_ranks(times[rank], torch.device("cpu"), world)
+    result[rank] = ms
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_value():
+    world = 2
+    times = [12.5, 20.0]
+    mgr = mp.get_context("spawn").Manager()
+    result = mgr.dict()
+    mp.start_processes(_worker, args=(world, _free_port(), times, result), nprocs=world, join=True,
+                       start_method="spawn")
+    assert result[0] == result[1] == 20.0
+    import bench
+    # two ranks, 256 MiB each, 10 steps in 20 ms
+    assert bench.whole_job_gbs(1 << 28, 2, 10, 20.0) == pytest.approx(2 * 10 * (1 << 28) / 0.020 / 1e9)
+    assert bench.max_over_ranks(3.0, torch.device("cpu"), 1) == 3.0
