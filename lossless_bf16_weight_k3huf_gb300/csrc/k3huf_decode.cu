@@ -47,14 +47,14 @@ void set_cuda_error(int code) { g_last_cuda_error = code; }
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;         // sub-streams per work item
+constexpr int kWarps = 16;                    // one CTA per SM
+constexpr int kThreads = 32 * kWarps;
+constexpr int kItem = 32;                     // sub-streams per work item (one warp)
 constexpr int kRound = 64;                    // values per lane between merges
-constexpr int kRowBytes = 132;                // per-lane high-byte row: 2 rounds + spill + pad (33 words)
-constexpr uint32_t kBitBuf = 30720;           // bytes of staged bit stream per pass
+constexpr int kRowBytes = 76;                 // per-lane high-byte row: a round + burst spill + pad (19 words)
+constexpr uint32_t kBitBuf = 9968;            // bytes of staged bit stream per warp and pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
-constexpr int kMinBlocksPerSm = 3;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
 constexpr int kCols = 16;                     // copies of the first-level table (one per lane mod 16)
 
@@ -65,8 +65,8 @@ constexpr int kCols = 16;                     // copies of the first-level table
 // Second level: the 4096-entry single-symbol table (sym << 4) | length.
 constexpr size_t kSmemL8 = 256 * kCols * sizeof(uint32_t);
 constexpr size_t kSmemL12 = 4096 * sizeof(uint16_t);
-constexpr size_t kSmemRows = size_t(kThreads) * kRowBytes;
-constexpr size_t kSmemBytes = kSmemL8 + kSmemL12 + kBitBuf + 16 + kSmemRows;
+constexpr size_t kWarpSlot = kBitBuf + 16 + size_t(32) * kRowBytes;   // bits + rows of one warp
+constexpr size_t kSmemBytes = kSmemL8 + kSmemL12 + size_t(kWarps) * kWarpSlot;
 
 struct StripeTask {
     const uint8_t *stripe;      // device: stripe header
@@ -253,10 +253,11 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
         if (l) s_sorted[s_off[l] + s_rank[s]] = uint8_t(s);
     }
     __syncthreads();
-    // single-symbol 12-bit table: each thread fills 32 consecutive windows,
+    // single-symbol 12-bit table: each thread fills consecutive windows,
     // one search per run of equal entries
     {
-        const uint32_t e0 = uint32_t(tid) * 32u, e1 = e0 + 32u;
+        constexpr uint32_t kPer = 4096u / kThreads;
+        const uint32_t e0 = uint32_t(tid) * kPer, e1 = e0 + kPer;
         uint32_t e = e0;
         while (e < e1) {
             uint32_t val = 0, end = e + 1;
@@ -341,312 +342,287 @@ __device__ __forceinline__ uint32_t second_level(const uint16_t *lut1, uint32_t 
 }
 
 template <int kSyms, bool kVec, bool kStaged>
-__global__ void __launch_bounds__(kThreads, kMinBlocksPerSm)
+__global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *l8 = reinterpret_cast<uint32_t *>(smem);
     uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemL8);
-    uint32_t *bitbuf = reinterpret_cast<uint32_t *>(smem + kSmemL8 + kSmemL12);
-    uint8_t *rows = smem + kSmemL8 + kSmemL12 + kBitBuf + 16;
     __shared__ uint8_t s_len[256];
-    __shared__ uint32_t s_hdr[8];
-    __shared__ uint32_t s_off[kThreads], s_end[kThreads];
-    __shared__ uint32_t s_pass_lo[kThreads + 1];
-    __shared__ uint32_t s_cut;
-    __shared__ int s_state, s_npass;
-    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ __align__(8) uint64_t s_bar[kWarps];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint8_t *wslot = smem + kSmemL8 + kSmemL12 + size_t(warp) * kWarpSlot;
+    uint32_t *bitbuf = reinterpret_cast<uint32_t *>(wslot);
+    uint8_t *wrows = wslot + kBitBuf + 16;
+    uint8_t *row = wrows + size_t(lane) * kRowBytes;
+
     const uint32_t cs = P.chunk_syms, ss = P.sub_syms, S = cs / ss;
     const uint32_t per = (P.n_items + gridDim.x - 1) / gridDim.x;
     const uint32_t it0 = blockIdx.x * per, it1 = min(P.n_items, it0 + per);
     const uint32_t *l8col = l8 + (lane & (kCols - 1));
     int table_built = -1;
-    int table_bad = 0;
+    bool table_bad = false, dead = false;
     uint32_t phase = 0;
 
-    if (tid == 0) {
-        mbar_init(&s_bar);
+    if (lane == 0) {
+        mbar_init(&s_bar[warp]);
         fence_proxy_async();
     }
     __syncthreads();
 
-    for (uint32_t item = it0; item < it1; ++item) {
-        const uint32_t ti = find_task(P, item);
-        const StripeTask &T = P.task[ti];
-        const int table = P.tables ? int(T.table) : 0;
-        __syncthreads();                           // previous item fully consumed
+    // the CTA's items in phases of one code table each
+    uint32_t item = it0;
+    while (item < it1) {                              // CTA-uniform
+        const uint32_t ti0 = find_task(P, item);
+        const int table = P.tables ? int(P.task[ti0].table) : 0;
+        uint32_t pend = it1;
+        for (uint32_t u = ti0 + 1; u < P.n_tasks && P.task[u].item_begin < it1; ++u)
+            if (P.tables && int(P.task[u].table) != table) {
+                pend = P.task[u].item_begin;
+                break;
+            }
+        __syncthreads();                              // every warp done with the previous table
         if (table != table_built) {
-            const uint8_t *codelen = P.tables ? P.tables + 256ull * T.table : P.inline_table;
+            const uint8_t *codelen = P.tables ? P.tables + 256ull * table : P.inline_table;
             table_bad = !build_tables<kSyms>(codelen, lut1, l8, s_len);
             table_built = table;
             if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
         }
-        if (tid == 0) {
-            uint32_t h[8];
-            const bool ok = stripe_header_ok(P, T, h);
-            for (int i = 0; i < 8; ++i) s_hdr[i] = h[i];
-            if (!ok && item == T.item_begin) atomicOr(P.status, K3HUF_ST_HEADER);
-            s_state = ok && !table_bad;
-        }
         __syncthreads();
-        if (!s_state) continue;
 
-        const uint32_t n = T.n_values;
-        const uint32_t nch = s_hdr[3];
-        const uint32_t huff_bits = s_hdr[4];      // < 2^32 for a valid stripe (<= 12 * 2^25)
-        const uint8_t *stripe = T.stripe;
-        const uint8_t *bits = stripe + s_hdr[6];
-        const uint8_t *even = stripe + s_hdr[7];
-        const uint32_t *chunk_off = reinterpret_cast<const uint32_t *>(stripe + K3HUF_STRIPE_HDR_BYTES);
-        const uint16_t *sub_off = reinterpret_cast<const uint16_t *>(stripe + K3HUF_STRIPE_HDR_BYTES + 4ull * nch);
-        uint8_t *out = T.out;
-        const uint32_t n_streams = nch * S;
-        const uint32_t g0 = (item - T.item_begin) * kThreads;
+        for (uint32_t wi = item + uint32_t(warp); wi < pend && !table_bad && !dead; wi += kWarps) {
+            const uint32_t ti = find_task(P, wi);
+            const StripeTask &T = P.task[ti];
+            uint32_t hdr[8];
+            const bool ok = stripe_header_ok(P, T, hdr);      // every lane reads the same 32 bytes
+            if (!ok) {
+                if (lane == 0 && wi == T.item_begin) atomicOr(P.status, K3HUF_ST_HEADER);
+                continue;
+            }
+            const uint32_t n = T.n_values;
+            const uint32_t nch = hdr[3];
+            const uint32_t huff_bits = hdr[4];       // < 2^32 for a valid stripe (<= 12 * 2^25)
+            const uint8_t *stripe = T.stripe;
+            const uint8_t *bits = stripe + hdr[6];
+            const uint8_t *even = stripe + hdr[7];
+            const uint32_t *chunk_off = reinterpret_cast<const uint32_t *>(stripe + K3HUF_STRIPE_HDR_BYTES);
+            const uint16_t *sub_off = reinterpret_cast<const uint16_t *>(stripe + K3HUF_STRIPE_HDR_BYTES + 4ull * nch);
+            uint8_t *out = T.out;
+            const uint32_t n_streams = nch * S;
+            const uint32_t g0 = (wi - T.item_begin) * kItem;
 
-        // this thread's sub-stream g = g0 + tid: values [g*ss, g*ss + len)
-        const uint32_t g = g0 + uint32_t(tid);
-        const bool active = g < n_streams && uint64_t(g) * ss < n;
-        const uint32_t my_len = active ? min(ss, n - g * ss) : 0u;
-        uint32_t my_off = 0, my_end = 0;
-        if (active) {
-            const uint32_t c = g / S, k = g - c * S;
-            const uint32_t base = chunk_off[c];
-            my_off = base + (k ? uint32_t(sub_off[size_t(c) * (S - 1) + k - 1]) : 0u);
-            my_end = k + 1 < S ? base + sub_off[size_t(c) * (S - 1) + k]
-                               : (c + 1 < nch ? chunk_off[c + 1] : huff_bits);
-        }
-        // clamp so that a corrupt index cannot move a read outside the stream
-        const uint32_t c_off = min(my_off, huff_bits), c_end = min(max(my_end, c_off), huff_bits);
-        s_off[tid] = c_off;
-        s_end[tid] = c_end;
-        // active sub-streams are a prefix of the item
-        const uint32_t nact = uint32_t(__syncthreads_count(active));
-        if (!kStaged) {
-            if (tid == 0) {
-                s_pass_lo[0] = 0;
-                s_pass_lo[1] = nact;
-                s_npass = 1;
+            // this lane's sub-stream g: values [g*ss, g*ss + len)
+            const uint32_t g = g0 + uint32_t(lane);
+            const bool active = g < n_streams && uint64_t(g) * ss < n;
+            const uint32_t my_len = active ? min(ss, n - g * ss) : 0u;
+            uint32_t my_off = 0, my_end = 0;
+            if (active) {
+                const uint32_t c = g / S, k = g - c * S;
+                const uint32_t base = chunk_off[c];
+                my_off = base + (k ? uint32_t(sub_off[size_t(c) * (S - 1) + k - 1]) : 0u);
+                my_end = k + 1 < S ? base + sub_off[size_t(c) * (S - 1) + k]
+                                   : (c + 1 < nch ? chunk_off[c + 1] : huff_bits);
             }
-        } else {
-            // passes: longest runs of sub-streams whose bits fit the buffer
-            uint32_t a = 0;
-            int np = 0;
-            while (a < nact) {                      // CTA-uniform
-                if (tid == 0) s_cut = nact;
-                __syncthreads();
-                const uint32_t lo = (s_off[a] >> 7) << 4;
-                const uint32_t t = uint32_t(tid);
-                if (t > a && t < nact && ((s_end[t] + 7) / 8 + 15) / 16 * 16 + 16 - lo > kBitBuf)
-                    atomicMin(&s_cut, t);
-                __syncthreads();
-                if (tid == 0) s_pass_lo[np] = a;
-                a = s_cut;
-                ++np;
-                __syncthreads();
-            }
-            if (tid == 0) {
-                s_pass_lo[np] = nact;
-                s_npass = np;
-            }
-        }
-        __syncthreads();
-        const int npass = s_npass;
+            // clamp so that a corrupt index cannot move a read outside the stream
+            const uint32_t c_off = min(my_off, huff_bits), c_end = min(max(my_end, c_off), huff_bits);
+            // active sub-streams are a prefix of the item
+            const uint32_t nact = uint32_t(__popc(__ballot_sync(0xffffffffu, active)));
 
-        for (int ps = 0; ps < npass; ++ps) {
-            const uint32_t pa = s_pass_lo[ps], pb = s_pass_lo[ps + 1];
-            uint32_t byte_lo = 0, nbytes = 32;
-            if (kStaged) {
-                byte_lo = (s_off[pa] >> 7) << 4;
-                const uint32_t byte_hi = ((s_end[pb - 1] + 7) / 8 + 15) / 16 * 16 + 16;
-                // a corrupt index may claim more bits than fit: reads are clamped below
-                nbytes = min(byte_hi - byte_lo, kBitBuf);
-                if (tid == 0) {
-                    fence_proxy_async();             // earlier generic reads of the buffer come first
-                    mbar_arrive_expect_tx(&s_bar, nbytes);
-                    bulk_g2s(bitbuf, bits + byte_lo, nbytes, &s_bar);
-                }
-                // bounded wait for the copy
-                uint32_t polls = 0;
-                bool landed = false;
-                while (!(landed = mbar_try_wait(&s_bar, phase)) && ++polls < kWaitLimit) {
-                }
-                phase ^= 1u;
-                const int ok_all = __syncthreads_and(landed ? 1 : 0);
-                if (!ok_all) {
-                    if (tid == 0) atomicOr(P.status, K3HUF_ST_TIMEOUT);
-                    // let the copy in flight land (again bounded) before giving up
-                    polls = 0;
-                    while (!landed && !(landed = mbar_try_wait(&s_bar, phase ^ 1u)) && ++polls < kWaitLimit) {
+            uint32_t pa = 0;
+            while (pa < nact) {                              // warp-uniform passes
+                uint32_t pb = nact, byte_lo = 0, nbytes = 32;
+                if (kStaged) {
+                    byte_lo = (__shfl_sync(0xffffffffu, c_off, int(pa)) >> 7) << 4;
+                    const uint32_t need = ((c_end + 7) / 8 + 15) / 16 * 16 + 16;
+                    const unsigned nofit = __ballot_sync(0xffffffffu, uint32_t(lane) > pa &&
+                                                         uint32_t(lane) < nact && need - byte_lo > kBitBuf);
+                    if (nofit) pb = uint32_t(__ffs(nofit)) - 1;
+                    const uint32_t byte_hi = __shfl_sync(0xffffffffu, need, int(pb - 1));
+                    // a corrupt index may claim a range that is reversed or too long:
+                    // the copy stays inside the buffer and inside the stripe's
+                    // stream (which holds at least 32 bytes past byte_lo), and
+                    // reads are clamped below
+                    const uint32_t region = hdr[7] - hdr[6];
+                    const uint32_t span = byte_hi > byte_lo ? byte_hi - byte_lo : 32u;
+                    nbytes = max(32u, min(min(span, kBitBuf), region - byte_lo));
+                    if (lane == 0) {
+                        fence_proxy_async();                 // earlier generic reads of the slot come first
+                        mbar_arrive_expect_tx(&s_bar[warp], nbytes);
+                        bulk_g2s(bitbuf, bits + byte_lo, nbytes, &s_bar[warp]);
                     }
-                    return;
-                }
-                // stream words MSB-first in each 32-bit word
-                const uint32_t nw = nbytes / 4;
+                    // bounded wait for the copy
+                    uint32_t polls = 0;
+                    bool landed = false;
+                    while (!(landed = mbar_try_wait(&s_bar[warp], phase)) && ++polls < kWaitLimit) {
+                    }
+                    phase ^= 1u;
+                    if (!__all_sync(0xffffffffu, landed)) {
+                        if (lane == 0) atomicOr(P.status, K3HUF_ST_TIMEOUT);
+                        // let the copy in flight land (again bounded), then stop this warp's work
+                        polls = 0;
+                        while (!landed && !(landed = mbar_try_wait(&s_bar[warp], phase ^ 1u)) && ++polls < kWaitLimit) {
+                        }
+                        dead = true;
+                        break;
+                    }
+                    // stream words MSB-first in each 32-bit word
+                    const uint32_t nw = nbytes / 4;
 #pragma unroll 4
-                for (uint32_t w = tid; w < nw; w += kThreads) bitbuf[w] = bswap32(bitbuf[w]);
-                __syncthreads();
-            }
+                    for (uint32_t w = uint32_t(lane); w < nw; w += 32) bitbuf[w] = bswap32(bitbuf[w]);
+                    __syncwarp();
+                }
 
-            const bool in_pass = uint32_t(tid) >= pa && uint32_t(tid) < pb;
-            const uint32_t len = in_pass ? my_len : 0u;
-            uint32_t bp = in_pass ? c_off - byte_lo * 8u : 0u;
-            const uint32_t max_word = nbytes / 4 - 3;
-            GlobalBits gb;
-            if (!kStaged)
-                gb.init(reinterpret_cast<const uint4 *>(bits), reinterpret_cast<const uint4 *>(even) - 1, c_off);
-            uint32_t prod = 0, cons = 0, bad = 0;
-            uint8_t *row = rows + size_t(tid) * kRowBytes;
-            const uint8_t *wrows = rows + size_t(warp) * 32 * kRowBytes;
+                const bool in_pass = uint32_t(lane) >= pa && uint32_t(lane) < pb;
+                const uint32_t len = in_pass ? my_len : 0u;
+                uint32_t bp = in_pass ? c_off - byte_lo * 8u : 0u;
+                const uint32_t max_word = nbytes / 4 - 3;
+                GlobalBits gb;
+                if (!kStaged)
+                    gb.init(reinterpret_cast<const uint4 *>(bits), reinterpret_cast<const uint4 *>(even) - 1, c_off);
+                uint32_t prod = 0, cons = 0, bad = 0;
 
-            // rounds: the same number for every lane of the warp
-            const uint32_t wlen = __reduce_max_sync(0xffffffffu, len);
-            const uint32_t n_rounds = (wlen + kRound - 1) / kRound;
-            const uint32_t warp_g0 = g0 + uint32_t(warp) * 32u;
+                // rounds: the same number for every lane of the warp
+                const uint32_t wlen = __reduce_max_sync(0xffffffffu, len);
+                const uint32_t n_rounds = (wlen + kRound - 1) / kRound;
 
-            // merge-phase assignment (vector path): piece i of this lane is the
-            // warp's sub-stream (i * 4 + lane / 8), values [r*64 + (lane % 8) * 8, +8)
-            const uint32_t sub = uint32_t(lane) & 7u;
-            uint2 ev[8];
-            uint32_t m_len[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t t = uint32_t(warp) * 32u + uint32_t(i) * 4u + uint32_t(lane >> 3);
-                const uint32_t gi = g0 + t;
-                m_len[i] = (t >= pa && t < pb) ? min(ss, n - gi * ss) : 0u;
-                ev[i] = make_uint2(0, 0);
-            }
-            auto load_even = [&](uint32_t round) {
+                // merge-phase assignment (vector path): piece i of this lane is the
+                // item's sub-stream (i * 4 + lane / 8), values [r*64 + (lane % 8) * 8, +8)
+                const uint32_t sub = uint32_t(lane) & 7u;
+                uint2 ev[8];
+                uint32_t m_len[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const uint32_t gi = warp_g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
-                    const uint32_t v = round * kRound + sub * 8u;
-                    if (kVec && v < m_len[i])
-                        ev[i] = __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v));
+                    const uint32_t t = uint32_t(i) * 4u + uint32_t(lane >> 3);
+                    m_len[i] = (t >= pa && t < pb) ? min(ss, n - (g0 + t) * ss) : 0u;
+                    ev[i] = make_uint2(0, 0);
                 }
-            };
-            load_even(0);
-
-            // three first-level lookups per 64-bit window write at most
-            // 3 * kSyms bytes from row position prod - cons (up to 3 bytes
-            // per lookup, the unused ones overwritten later)
-            constexpr uint32_t kBurst = 3 * kSyms;
-            constexpr uint32_t kRoom = kRowBytes - 2 - kBurst;
-            const uint32_t *hrow[8];
-            size_t vbase[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t gw = uint32_t(i) * 4u + uint32_t(lane >> 3);
-                hrow[i] = reinterpret_cast<const uint32_t *>(wrows + gw * kRowBytes + sub * 8u);
-                vbase[i] = size_t(warp_g0 + gw) * ss + sub * 8u;
-            }
-
-            for (uint32_t r = 0; r < n_rounds; ++r) {
-                const uint32_t target = min(len, (r + 1) * uint32_t(kRound));
-                // a burst is allowed while it can neither pass the sub-stream's
-                // end nor overrun the row
-                const uint32_t burst_lim = min(len >= kBurst ? len - kBurst : 0u, cons + kRoom);
-                const bool burst_ok = len >= kBurst;
-                uint8_t *const rbase = row - cons;      // row position of value v is rbase + v
-                // decode until every lane of the warp holds this round's values
-                while (__any_sync(0xffffffffu, prod < target)) {
-                    if (kStaged && burst_ok && prod <= burst_lim) {
-                        const uint32_t i = min(bp >> 5, max_word);
-                        const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1], w2 = bitbuf[i + 2];
-                        uint32_t hi = __funnelshift_l(w1, w0, bp), lo = __funnelshift_l(w2, w1, bp);
-                        uint8_t *dst = rbase + prod;
-                        uint32_t e = 0;
-#pragma unroll
-                        for (int k = 0; k < 3; ++k) {
-                            e = l8col[(hi >> 24) * kCols];
-                            const uint32_t t = e >> 28;
-                            dst[0] = uint8_t(e);
-                            if (kSyms > 1) dst[1] = uint8_t(e >> 8);
-                            if (kSyms > 2) dst[2] = uint8_t(e >> 16);
-                            dst += (e >> 24) & 3u;
-                            bp += t;
-                            hi = __funnelshift_l(lo, hi, t);
-                            lo <<= t;
-                        }
-                        if (((e >> 24) & 3u) == 0) {
-                            // a code longer than 8 bits stopped the window: one exact code
-                            e = second_level(lut1, hi, bad);
-                            dst[0] = uint8_t(e);
-                            dst += 1;
-                            bp += e >> 28;
-                        }
-                        prod = uint32_t(dst - rbase);
-                    } else if (prod < len && prod - cons <= kRoom) {
-                        // exact tail: one code at a time
-                        uint32_t win;
-                        if (kStaged) {
-                            const uint32_t i = min(bp >> 5, max_word);
-                            win = __funnelshift_l(bitbuf[i + 1], bitbuf[i], bp);
-                        } else {
-                            win = gb.window();
-                        }
-                        const uint32_t e = second_level(lut1, win, bad);
-                        rbase[prod] = uint8_t(e);
-                        prod += 1;
-                        if (kStaged) bp += e >> 28; else gb.advance(e >> 28);
-                    }
-                }
-                __syncwarp();
-                if (kVec) {
-                    const uint32_t v = r * kRound + sub * 8u;
+                auto load_even = [&](uint32_t round) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        if (v >= m_len[i]) continue;
-                        const uint32_t hx = hrow[i][0], hy = hrow[i][1];
-                        uint4 o;
-                        o.x = interleave_lo(ev[i].x, hx);
-                        o.y = interleave_hi(ev[i].x, hx);
-                        o.z = interleave_lo(ev[i].y, hy);
-                        o.w = interleave_hi(ev[i].y, hy);
-                        uint8_t *dst = out + 2 * (vbase[i] + r * kRound);
-                        if (v + 8 <= m_len[i]) {
-                            *reinterpret_cast<uint4 *>(dst) = o;
-                        } else {
-                            const uint32_t kk = m_len[i] - v;   // 1..7 values left in the sub-stream
-                            uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
+                        const uint32_t gi = g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
+                        const uint32_t v = round * kRound + sub * 8u;
+                        if (kVec && v < m_len[i])
+                            ev[i] = __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v));
+                    }
+                };
+                load_even(0);
+
+                // three first-level lookups per 64-bit window write at most
+                // 3 * kSyms bytes from row position prod - cons; a lane stops
+                // at its round target, so a row never holds more than one
+                // round plus one burst's spill
+                constexpr uint32_t kBurst = 3 * kSyms;
+                static_assert(kRound + kBurst <= kRowBytes, "row too short for a burst past the round");
+
+                for (uint32_t r = 0; r < n_rounds; ++r) {
+                    const uint32_t target = min(len, (r + 1) * uint32_t(kRound));
+                    const uint32_t burst_lim = min(len >= kBurst ? len - kBurst : 0u, target - 1u);
+                    const bool burst_ok = len >= kBurst && target > 0;
+                    uint8_t *const rbase = row - cons;      // row position of value v is rbase + v
+                    // decode until every lane of the warp holds this round's values
+                    while (__any_sync(0xffffffffu, prod < target)) {
+                        if (kStaged && burst_ok && prod <= burst_lim) {
+                            const uint32_t i = min(bp >> 5, max_word);
+                            const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1], w2 = bitbuf[i + 2];
+                            uint32_t hi = __funnelshift_l(w1, w0, bp), lo = __funnelshift_l(w2, w1, bp);
+                            uint8_t *dst = rbase + prod;
+                            uint32_t e = 0;
 #pragma unroll
-                            for (uint32_t j = 0; j < 8; ++j) {
-                                const uint32_t w = j < 2 ? o.x : j < 4 ? o.y : j < 6 ? o.z : o.w;
-                                if (j < kk) d16[j] = uint16_t(w >> (16 * (j & 1)));
+                            for (int k = 0; k < 3; ++k) {
+                                e = l8col[(hi >> 24) * kCols];
+                                const uint32_t t = e >> 28;
+                                dst[0] = uint8_t(e);
+                                if (kSyms > 1) dst[1] = uint8_t(e >> 8);
+                                if (kSyms > 2) dst[2] = uint8_t(e >> 16);
+                                dst += (e >> 24) & 3u;
+                                bp += t;
+                                hi = __funnelshift_l(lo, hi, t);
+                                lo <<= t;
                             }
+                            if (((e >> 24) & 3u) == 0) {
+                                // a code longer than 8 bits stopped the window: one exact code
+                                e = second_level(lut1, hi, bad);
+                                dst[0] = uint8_t(e);
+                                dst += 1;
+                                bp += e >> 28;
+                            }
+                            prod = uint32_t(dst - rbase);
+                        } else if (prod < target) {
+                            // exact tail: one code at a time
+                            uint32_t win;
+                            if (kStaged) {
+                                const uint32_t i = min(bp >> 5, max_word);
+                                win = __funnelshift_l(bitbuf[i + 1], bitbuf[i], bp);
+                            } else {
+                                win = gb.window();
+                            }
+                            const uint32_t e = second_level(lut1, win, bad);
+                            rbase[prod] = uint8_t(e);
+                            prod += 1;
+                            if (kStaged) bp += e >> 28; else gb.advance(e >> 28);
                         }
                     }
-                    if (r + 1 < n_rounds) load_even(r + 1);   // in flight while the next round decodes
-                } else if (len) {
-                    // scalar path for sub-stream sizes that break 8-value alignment
-                    const uint32_t a = r * kRound, b = min(len, a + kRound);
-                    const size_t v0 = size_t(g) * ss;
-                    for (uint32_t v = a; v < b; ++v) {
-                        out[2 * (v0 + v)] = even[v0 + v];
-                        out[2 * (v0 + v) + 1] = row[v - a];
-                    }
-                }
-                __syncwarp();
-                // drop the merged round from this lane's row
-                {
-                    uint32_t *rw = reinterpret_cast<uint32_t *>(row);
+                    __syncwarp();
+                    if (kVec) {
+                        const uint32_t v = r * kRound + sub * 8u;
 #pragma unroll
-                    for (int k = 0; k < (kRowBytes - kRound) / 4; ++k) rw[k] = rw[k + kRound / 4];
+                        for (int i = 0; i < 8; ++i) {
+                            if (v >= m_len[i]) continue;
+                            const uint32_t gw = uint32_t(i) * 4u + uint32_t(lane >> 3);
+                            const uint32_t *hrow = reinterpret_cast<const uint32_t *>(wrows + gw * kRowBytes + sub * 8u);
+                            const uint32_t hx = hrow[0], hy = hrow[1];
+                            uint4 o;
+                            o.x = interleave_lo(ev[i].x, hx);
+                            o.y = interleave_hi(ev[i].x, hx);
+                            o.z = interleave_lo(ev[i].y, hy);
+                            o.w = interleave_hi(ev[i].y, hy);
+                            uint8_t *dst = out + 2 * (size_t(g0 + gw) * ss + v);
+                            if (v + 8 <= m_len[i]) {
+                                *reinterpret_cast<uint4 *>(dst) = o;
+                            } else {
+                                const uint32_t kk = m_len[i] - v;   // 1..7 values left in the sub-stream
+                                uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
+#pragma unroll
+                                for (uint32_t j = 0; j < 8; ++j) {
+                                    const uint32_t w = j < 2 ? o.x : j < 4 ? o.y : j < 6 ? o.z : o.w;
+                                    if (j < kk) d16[j] = uint16_t(w >> (16 * (j & 1)));
+                                }
+                            }
+                        }
+                        if (r + 1 < n_rounds) load_even(r + 1);   // in flight while the next round decodes
+                    } else if (len) {
+                        // scalar path for sub-stream sizes that break 8-value alignment
+                        const uint32_t a0 = r * kRound, b0 = min(len, a0 + kRound);
+                        const size_t v0 = size_t(g) * ss;
+                        for (uint32_t vv = a0; vv < b0; ++vv) {
+                            out[2 * (v0 + vv)] = even[v0 + vv];
+                            out[2 * (v0 + vv) + 1] = row[vv - a0];
+                        }
+                    }
+                    __syncwarp();
+                    // drop the merged round from this lane's row (the spill moves down)
+                    {
+                        uint32_t *rw = reinterpret_cast<uint32_t *>(row);
+#pragma unroll
+                        for (int k = 0; k < (kRowBytes - kRound) / 4; ++k) rw[k] = rw[k + kRound / 4];
+                    }
+                    cons += kRound;
                 }
-                cons += kRound;
-            }
 
-            uint32_t st = 0;
-            if (len) {
-                if (bad) st |= K3HUF_ST_BADCODE;
-                uint32_t pos = kStaged ? bp + byte_lo * 8u : gb.position();
-                if (my_off > huff_bits || my_end > huff_bits) st |= K3HUF_ST_OVERRUN;
-                if (pos != my_end) st |= K3HUF_ST_INDEX;
+                uint32_t st = 0;
+                if (len) {
+                    if (bad) st |= K3HUF_ST_BADCODE;
+                    const uint32_t pos = kStaged ? bp + byte_lo * 8u : gb.position();
+                    if (my_off > huff_bits || my_end > huff_bits) st |= K3HUF_ST_OVERRUN;
+                    if (pos != my_end) st |= K3HUF_ST_INDEX;
+                }
+                st = __reduce_or_sync(0xffffffffu, st);
+                if (lane == 0 && st) atomicOr(P.status, st);
+                __syncwarp();                            // slot free for the next pass / item
+                pa = pb;
             }
-            st = __reduce_or_sync(0xffffffffu, st);
-            if (lane == 0 && st) atomicOr(P.status, st);
-            __syncthreads();                         // buffer free for the next pass / item
         }
+        item = pend;
     }
 }
 
@@ -708,7 +684,7 @@ int launch_tasks(DecodeParams &P, cudaStream_t stream) {
 uint32_t items_of(uint32_t n_values, uint32_t cs, uint32_t ss) {
     const uint64_t nch = (uint64_t(n_values) + cs - 1) / cs;
     const uint64_t streams = nch * (cs / ss);
-    return uint32_t((streams + kThreads - 1) / kThreads);
+    return uint32_t((streams + kItem - 1) / kItem);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
