@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--variant", type=int, default=0, help="most codes per lookup: 0 default (3), 1, 2, 3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ring-layers", type=int, default=14)
+    ap.add_argument("--sub-syms", type=int, default=None, help="values per sub-stream in the container")
     return ap.parse_args()
 
 
@@ -66,11 +67,12 @@ def describe(name):
     return d
 
 
-def make_layer(name):
+def make_layer(name, sub_syms=None):
     """(tensors, container) of a named single-layer workload."""
     import lossless_bf16_weight_k3huf_gb300 as k3
     tensors = workloads.workload(name)
-    blob = k3.encode_layer(tensors)
+    kw = {} if sub_syms is None else {"sub_syms": sub_syms}
+    blob = k3.encode_layer(tensors, **kw)
     return tensors, blob
 
 
@@ -270,7 +272,7 @@ def main():
     if args.workload == "ring":
         return bench_ring(args, rank, world, local, dev)
 
-    tensors, blob = make_layer(args.workload)
+    tensors, blob = make_layer(args.workload, args.sub_syms)
     info = k3.layer_info(blob)
     hdr = blob[: info["hdr_bytes"]].copy()
     raw = info["raw_bytes"]
@@ -348,7 +350,7 @@ def main():
         "config": {**describe(args.workload), "values": raw // 2, "raw_bytes": raw,
                    "blob_bytes": info["blob_bytes"], "compression_ratio": round(raw / info["blob_bytes"], 4),
                    "compression_rate": round(info["blob_bytes"] / raw, 4), "stripes": info["n_stripes"],
-                   "chunk_syms": info["chunk_syms"], "decoder": ["3 codes/lookup", "1 code/lookup", "2 codes/lookup", "3 codes/lookup"][args.variant],
+                   "chunk_syms": info["chunk_syms"], "sub_syms": info["sub_syms"], "decoder": ["3 codes/lookup", "1 code/lookup", "2 codes/lookup", "3 codes/lookup"][args.variant],
                    "l2": l2_note, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",

@@ -47,12 +47,12 @@ void set_cuda_error(int code) { g_last_cuda_error = code; }
 
 namespace {
 
-constexpr int kWarps = 16;                    // one CTA per SM
+constexpr int kWarps = 20;                    // one CTA per SM
 constexpr int kThreads = 32 * kWarps;
 constexpr int kItem = 32;                     // sub-streams per work item (one warp)
 constexpr int kRound = 64;                    // values per lane between merges
 constexpr int kRowBytes = 76;                 // per-lane high-byte row: a round + burst spill + pad (19 words)
-constexpr uint32_t kBitBuf = 9968;            // bytes of staged bit stream per warp and pass
+constexpr uint32_t kBitBuf = 7872;            // bytes of staged bit stream per warp and pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
@@ -256,8 +256,8 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
     // single-symbol 12-bit table: each thread fills consecutive windows,
     // one search per run of equal entries
     {
-        constexpr uint32_t kPer = 4096u / kThreads;
-        const uint32_t e0 = uint32_t(tid) * kPer, e1 = e0 + kPer;
+        constexpr uint32_t kPer = (4096u + kThreads - 1) / kThreads;
+        const uint32_t e0 = min(uint32_t(tid) * kPer, 4096u), e1 = min(e0 + kPer, 4096u);
         uint32_t e = e0;
         while (e < e1) {
             uint32_t val = 0, end = e + 1;
@@ -488,24 +488,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 // merge-phase assignment (vector path): piece i of this lane is the
                 // item's sub-stream (i * 4 + lane / 8), values [r*64 + (lane % 8) * 8, +8)
                 const uint32_t sub = uint32_t(lane) & 7u;
-                uint2 ev[8];
-                uint32_t m_len[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                auto piece_len = [&](int i) -> uint32_t {
                     const uint32_t t = uint32_t(i) * 4u + uint32_t(lane >> 3);
-                    m_len[i] = (t >= pa && t < pb) ? min(ss, n - (g0 + t) * ss) : 0u;
-                    ev[i] = make_uint2(0, 0);
-                }
-                auto load_even = [&](uint32_t round) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t gi = g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
-                        const uint32_t v = round * kRound + sub * 8u;
-                        if (kVec && v < m_len[i])
-                            ev[i] = __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v));
-                    }
+                    return (t >= pa && t < pb) ? min(ss, n - (g0 + t) * ss) : 0u;
                 };
-                load_even(0);
 
                 // three first-level lookups per 64-bit window write at most
                 // 3 * kSyms bytes from row position prod - cons; a lane stops
@@ -565,9 +551,17 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     __syncwarp();
                     if (kVec) {
                         const uint32_t v = r * kRound + sub * 8u;
+                        uint2 ev[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {       // all low-byte loads in flight at once
+                            const uint32_t gi = g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
+                            ev[i] = v < piece_len(i) ? __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v))
+                                                     : make_uint2(0, 0);
+                        }
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            if (v >= m_len[i]) continue;
+                            const uint32_t m_len = piece_len(i);
+                            if (v >= m_len) continue;
                             const uint32_t gw = uint32_t(i) * 4u + uint32_t(lane >> 3);
                             const uint32_t *hrow = reinterpret_cast<const uint32_t *>(wrows + gw * kRowBytes + sub * 8u);
                             const uint32_t hx = hrow[0], hy = hrow[1];
@@ -577,10 +571,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             o.z = interleave_lo(ev[i].y, hy);
                             o.w = interleave_hi(ev[i].y, hy);
                             uint8_t *dst = out + 2 * (size_t(g0 + gw) * ss + v);
-                            if (v + 8 <= m_len[i]) {
+                            if (v + 8 <= m_len) {
                                 *reinterpret_cast<uint4 *>(dst) = o;
                             } else {
-                                const uint32_t kk = m_len[i] - v;   // 1..7 values left in the sub-stream
+                                const uint32_t kk = m_len - v;   // 1..7 values left in the sub-stream
                                 uint16_t *d16 = reinterpret_cast<uint16_t *>(dst);
 #pragma unroll
                                 for (uint32_t j = 0; j < 8; ++j) {
@@ -589,7 +583,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                                 }
                             }
                         }
-                        if (r + 1 < n_rounds) load_even(r + 1);   // in flight while the next round decodes
                     } else if (len) {
                         // scalar path for sub-stream sizes that break 8-value alignment
                         const uint32_t a0 = r * kRound, b0 = min(len, a0 + kRound);
