@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--workload", default="projection",
                     choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
-    ap.add_argument("--variant", type=int, default=0, help="most codes per lookup: 0 default (3), 1, 2, 3")
+    ap.add_argument("--variant", type=int, default=0, help="codes per lookup: 0 default (2), 1, 2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ring-layers", type=int, default=14)
     ap.add_argument("--sub-syms", type=int, default=None, help="values per sub-stream in the container")
@@ -350,7 +350,7 @@ def main():
         "config": {**describe(args.workload), "values": raw // 2, "raw_bytes": raw,
                    "blob_bytes": info["blob_bytes"], "compression_ratio": round(raw / info["blob_bytes"], 4),
                    "compression_rate": round(info["blob_bytes"] / raw, 4), "stripes": info["n_stripes"],
-                   "chunk_syms": info["chunk_syms"], "sub_syms": info["sub_syms"], "decoder": ["3 codes/lookup", "1 code/lookup", "2 codes/lookup", "3 codes/lookup"][args.variant],
+                   "chunk_syms": info["chunk_syms"], "sub_syms": info["sub_syms"], "decoder": ["2 codes/lookup", "1 code/lookup", "2 codes/lookup"][args.variant],
                    "l2": l2_note, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",

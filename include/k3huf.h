@@ -154,11 +154,12 @@ int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms, uint32_
                         uint32_t *d_status, void *stream);
 
 /* Select the decode kernel variant for later decode calls in this process:
- * the most codes one table lookup may emit.  0 = default (3), 1 = one code
- * per lookup (the article's shelved decoder's scheme), 2 = the article's
- * double-symbol table (section 如果将来重启), 3 = up to three codes when
- * they fit in the 12-bit window.  All give identical output.  Returns
- * K3HUF_E_ARG for any other value. */
+ * the number of codes every table lookup of the lockstep decoder emits.
+ * 0 = default (2), 1 = one code per lookup (the article's shelved
+ * decoder's scheme), 2 = the article's double-symbol table (section
+ * 如果将来重启): two codes per lookup when both fit in the 12-bit window,
+ * otherwise the two codes are read one at a time.  All give identical
+ * output.  Returns K3HUF_E_ARG for any other value. */
 int k3huf_set_decoder_variant(int variant);
 
 /* Pack-time encoder (host, multi-threaded), producing the container above

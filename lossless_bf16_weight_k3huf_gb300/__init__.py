@@ -210,7 +210,7 @@ def decode_stripe(codelen, chunk_syms: int, sub_syms: int, d_stripe, stripe_byte
 
 
 def set_decoder_variant(variant: int) -> None:
-    """Most codes per table lookup: 0 = default (3), 1, 2 or 3."""
+    """Codes per lockstep table lookup: 0 = default (2), 1 or 2."""
     _check(_lib().k3huf_set_decoder_variant(variant), "k3huf_set_decoder_variant")
 
 

@@ -51,22 +51,21 @@ constexpr int kWarps = 20;                    // one CTA per SM
 constexpr int kThreads = 32 * kWarps;
 constexpr int kItem = 32;                     // sub-streams per work item (one warp)
 constexpr int kRound = 64;                    // values per lane between merges
-constexpr int kRowBytes = 76;                 // per-lane high-byte row: a round + burst spill + pad (19 words)
-constexpr uint32_t kBitBuf = 7872;            // bytes of staged bit stream per warp and pass
+constexpr int kRowBytes = 80;                 // per-lane row: one round of high bytes + pad (20 words)
+constexpr uint32_t kBitBuf = 7744;            // bytes of staged bit stream per warp and pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
-constexpr int kCols = 16;                     // copies of the first-level table (one per lane mod 16)
 
-// First-level table, indexed by the next 8 bits, kCols interleaved copies so
-// that lanes of a half-warp never share a bank:
-//   [23:0] up to three symbols (first in the low byte)  [25:24] number of
-//   symbols, 0 when the first code is longer than 8 bits  [31:28] bits used.
-// Second level: the 4096-entry single-symbol table (sym << 4) | length.
-constexpr size_t kSmemL8 = 256 * kCols * sizeof(uint32_t);
+// Lockstep table, indexed by the next 12 bits: exactly kPer whole codes.
+//   [7:0] first symbol [15:8] second symbol [31:28] bits used by the kPer
+//   codes; 0 there when the window does not start with kPer codes of at
+//   most 12 bits in total (then the codes are read one at a time).
+// Single-code table: the 4096-entry (sym << 4) | length table.
+constexpr size_t kSmemLut = 4096 * sizeof(uint32_t);
 constexpr size_t kSmemL12 = 4096 * sizeof(uint16_t);
 constexpr size_t kWarpSlot = kBitBuf + 16 + size_t(32) * kRowBytes;   // bits + rows of one warp
-constexpr size_t kSmemBytes = kSmemL8 + kSmemL12 + size_t(kWarps) * kWarpSlot;
+constexpr size_t kSmemBytes = kSmemLut + kSmemL12 + size_t(kWarps) * kWarpSlot;
 
 struct StripeTask {
     const uint8_t *stripe;      // device: stripe header
@@ -197,11 +196,12 @@ struct GlobalBits {
     }
 };
 
-// Build both table levels in shared memory from codelen[256].  Returns
+// Build the single-code and lockstep tables in shared memory from
+// codelen[256].  Returns
 // false, uniformly across the CTA, when the table fails the Kraft check.
 // All threads of the CTA must call it.
-template <int kSyms>
-__device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *lut1, uint32_t *l8, uint8_t *s_len) {
+template <int kPer>
+__device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *lut1, uint32_t *lut, uint8_t *s_len) {
     __shared__ uint8_t s_rank[256];
     __shared__ uint8_t s_sorted[256];
     __shared__ uint32_t s_first[K3HUF_MAXLEN + 1], s_count[K3HUF_MAXLEN + 1], s_off[K3HUF_MAXLEN + 2];
@@ -256,8 +256,8 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
     // single-symbol 12-bit table: each thread fills consecutive windows,
     // one search per run of equal entries
     {
-        constexpr uint32_t kPer = (4096u + kThreads - 1) / kThreads;
-        const uint32_t e0 = min(uint32_t(tid) * kPer, 4096u), e1 = min(e0 + kPer, 4096u);
+        constexpr uint32_t kFill = (4096u + kThreads - 1) / kThreads;
+        const uint32_t e0 = min(uint32_t(tid) * kFill, 4096u), e1 = min(e0 + kFill, 4096u);
         uint32_t e = e0;
         while (e < e1) {
             uint32_t val = 0, end = e + 1;
@@ -275,27 +275,21 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
         }
     }
     __syncthreads();
-    // first level: up to kSyms whole codes inside the next 8 bits
-    for (uint32_t x = tid; x < 256u; x += kThreads) {
-        const uint32_t w = x << 4;                   // the 8 bits at the top of a 12-bit window
-        const uint32_t a = lut1[w];
-        uint32_t used = a & 15u, ent = 0;
-        if (used != 0 && used <= 8) {
-            uint32_t syms = a >> 4, n = 1;
-#pragma unroll
-            for (int k = 1; k < kSyms; ++k) {
-                const uint32_t b = lut1[(w << used) & 4095u];
-                const uint32_t l = b & 15u;
-                if (n == uint32_t(k) && l != 0 && used + l <= 8) {
-                    syms |= (b >> 4) << (8 * k);
-                    used += l;
-                    n += 1;
-                }
+    // lockstep table: exactly kPer codes inside the 12-bit window
+    for (uint32_t e = tid; e < 4096u; e += kThreads) {
+        const uint32_t a = lut1[e];
+        const uint32_t l1 = a & 15u;
+        uint32_t ent = 0;
+        if (l1 != 0) {
+            if (kPer == 1) {
+                ent = (a >> 4) | (l1 << 28);
+            } else {
+                const uint32_t b = lut1[(e << l1) & 4095u];
+                const uint32_t l2 = b & 15u;
+                if (l2 != 0 && l1 + l2 <= K3HUF_MAXLEN) ent = (a >> 4) | ((b >> 4) << 8) | ((l1 + l2) << 28);
             }
-            ent = syms | (n << 24) | (used << 28);
         }
-#pragma unroll
-        for (int c = 0; c < kCols; ++c) l8[x * kCols + c] = ent;
+        lut[e] = ent;
     }
     __syncthreads();
     return true;
@@ -331,35 +325,23 @@ __device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, uin
     return ok;
 }
 
-// The 12-bit second level as a first-level style entry (one symbol); an
-// undecodable window consumes one bit and raises `bad`.
-__device__ __forceinline__ uint32_t second_level(const uint16_t *lut1, uint32_t win, uint32_t &bad) {
-    const uint32_t a = lut1[win >> 20];
-    uint32_t l = a & 15u;
-    bad |= l == 0;
-    l += l == 0;
-    return (a >> 4) | (1u << 24) | (l << 28);
-}
-
-template <int kSyms, bool kVec, bool kStaged>
+template <int kPer, bool kVec, bool kStaged>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint32_t *l8 = reinterpret_cast<uint32_t *>(smem);
-    uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemL8);
+    uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
+    uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemLut);
     __shared__ uint8_t s_len[256];
     __shared__ __align__(8) uint64_t s_bar[kWarps];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    uint8_t *wslot = smem + kSmemL8 + kSmemL12 + size_t(warp) * kWarpSlot;
+    uint8_t *wslot = smem + kSmemLut + kSmemL12 + size_t(warp) * kWarpSlot;
     uint32_t *bitbuf = reinterpret_cast<uint32_t *>(wslot);
     uint8_t *wrows = wslot + kBitBuf + 16;
-    uint8_t *row = wrows + size_t(lane) * kRowBytes;
 
     const uint32_t cs = P.chunk_syms, ss = P.sub_syms, S = cs / ss;
     const uint32_t per = (P.n_items + gridDim.x - 1) / gridDim.x;
     const uint32_t it0 = blockIdx.x * per, it1 = min(P.n_items, it0 + per);
-    const uint32_t *l8col = l8 + (lane & (kCols - 1));
     int table_built = -1;
     bool table_bad = false, dead = false;
     uint32_t phase = 0;
@@ -384,7 +366,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         __syncthreads();                              // every warp done with the previous table
         if (table != table_built) {
             const uint8_t *codelen = P.tables ? P.tables + 256ull * table : P.inline_table;
-            table_bad = !build_tables<kSyms>(codelen, lut1, l8, s_len);
+            table_bad = !build_tables<kPer>(codelen, lut1, lut, s_len);
             table_built = table;
             if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
         }
@@ -479,7 +461,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 GlobalBits gb;
                 if (!kStaged)
                     gb.init(reinterpret_cast<const uint4 *>(bits), reinterpret_cast<const uint4 *>(even) - 1, c_off);
-                uint32_t prod = 0, cons = 0, bad = 0;
+                uint32_t bad = 0;
 
                 // rounds: the same number for every lane of the warp
                 const uint32_t wlen = __reduce_max_sync(0xffffffffu, len);
@@ -493,48 +475,79 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     return (t >= pa && t < pb) ? min(ss, n - (g0 + t) * ss) : 0u;
                 };
 
-                // three first-level lookups per 64-bit window write at most
-                // 3 * kSyms bytes from row position prod - cons; a lane stops
-                // at its round target, so a row never holds more than one
-                // round plus one burst's spill
-                constexpr uint32_t kBurst = 3 * kSyms;
-                static_assert(kRound + kBurst <= kRowBytes, "row too short for a burst past the round");
+                // 64-bit window at bit position `cur` of the staged stream
+                auto window = [&](uint32_t cur, uint32_t &hi, uint32_t &lo) {
+                    const uint32_t i = min(cur >> 5, max_word);
+                    const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1], w2 = bitbuf[i + 2];
+                    hi = __funnelshift_l(w1, w0, cur);
+                    lo = __funnelshift_l(w2, w1, cur);
+                };
+                // one code from the 12-bit single-code table; an undecodable
+                // window gives symbol 0 and one bit, and raises `bad`
+                auto single = [&](uint32_t win, uint32_t &len_out) -> uint32_t {
+                    const uint32_t a = lut1[win >> 20];
+                    const uint32_t l = a & 15u;
+                    bad |= l == 0;
+                    len_out = l + (l == 0);
+                    return a >> 4;
+                };
 
                 for (uint32_t r = 0; r < n_rounds; ++r) {
-                    const uint32_t target = min(len, (r + 1) * uint32_t(kRound));
-                    const uint32_t burst_lim = min(len >= kBurst ? len - kBurst : 0u, target - 1u);
-                    const bool burst_ok = len >= kBurst && target > 0;
-                    uint8_t *const rbase = row - cons;      // row position of value v is rbase + v
-                    // decode until every lane of the warp holds this round's values
-                    while (__any_sync(0xffffffffu, prod < target)) {
-                        if (kStaged && burst_ok && prod <= burst_lim) {
-                            const uint32_t i = min(bp >> 5, max_word);
-                            const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1], w2 = bitbuf[i + 2];
-                            uint32_t hi = __funnelshift_l(w1, w0, bp), lo = __funnelshift_l(w2, w1, bp);
-                            uint8_t *dst = rbase + prod;
-                            uint32_t e = 0;
+                    const uint32_t rem = len > r * kRound ? len - r * kRound : 0u;
+                    uint8_t *row = wrows + size_t(lane) * kRowBytes;
+                    if (kStaged && __all_sync(0xffffffffu, rem >= uint32_t(kRound))) {
+                        // lockstep round: every lookup yields exactly kPer codes, so
+                        // the round's 64 high bytes land in registers at fixed places
+                        uint32_t R[kRound / 4];
 #pragma unroll
-                            for (int k = 0; k < 3; ++k) {
-                                e = l8col[(hi >> 24) * kCols];
-                                const uint32_t t = e >> 28;
-                                dst[0] = uint8_t(e);
-                                if (kSyms > 1) dst[1] = uint8_t(e >> 8);
-                                if (kSyms > 2) dst[2] = uint8_t(e >> 16);
-                                dst += (e >> 24) & 3u;
-                                bp += t;
-                                hi = __funnelshift_l(lo, hi, t);
-                                lo <<= t;
+                        for (int grp = 0; grp < kRound / (4 * kPer); ++grp) {
+                            uint32_t cur = bp, hi, lo;
+                            window(cur, hi, lo);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int j = grp * 4 + k;              // lookup index in the round
+                                uint32_t e = lut[hi >> 20];
+                                uint32_t t = e >> 28;
+                                if (t == 0) {
+                                    // fewer than kPer codes fit the window: read them one at a time
+                                    window(cur, hi, lo);
+                                    uint32_t l, syms = single(hi, l);
+                                    t = l;
+                                    hi = __funnelshift_l(lo, hi, l);
+                                    lo <<= l;
+                                    if (kPer == 2) {
+                                        syms |= single(hi, l) << 8;
+                                        t += l;
+                                        hi = __funnelshift_l(lo, hi, l);
+                                        lo <<= l;
+                                    }
+                                    cur += t;
+                                    e = syms;
+                                    // the shifted window stays valid for the group's other lookups
+                                    t = 0;
+                                } else {
+                                    cur += t;
+                                    hi = __funnelshift_l(lo, hi, t);
+                                    lo <<= t;
+                                }
+                                if (kPer == 2) {
+                                    if (j & 1) R[j >> 1] |= e << 16;
+                                    else R[j >> 1] = e & 0xFFFFu;
+                                } else {
+                                    if (j & 3) R[j >> 2] |= (e & 0xFFu) << (8 * (j & 3));
+                                    else R[j >> 2] = e & 0xFFu;
+                                }
                             }
-                            if (((e >> 24) & 3u) == 0) {
-                                // a code longer than 8 bits stopped the window: one exact code
-                                e = second_level(lut1, hi, bad);
-                                dst[0] = uint8_t(e);
-                                dst += 1;
-                                bp += e >> 28;
-                            }
-                            prod = uint32_t(dst - rbase);
-                        } else if (prod < target) {
-                            // exact tail: one code at a time
+                            bp = cur;
+                        }
+                        uint4 *row4 = reinterpret_cast<uint4 *>(row);
+#pragma unroll
+                        for (int k = 0; k < kRound / 16; ++k)
+                            row4[k] = make_uint4(R[4 * k], R[4 * k + 1], R[4 * k + 2], R[4 * k + 3]);
+                    } else {
+                        // partial round (a stream's end or a split pass): exact single codes
+                        const uint32_t cnt = min(rem, uint32_t(kRound));
+                        for (uint32_t j = 0; j < cnt; ++j) {
                             uint32_t win;
                             if (kStaged) {
                                 const uint32_t i = min(bp >> 5, max_word);
@@ -542,10 +555,9 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             } else {
                                 win = gb.window();
                             }
-                            const uint32_t e = second_level(lut1, win, bad);
-                            rbase[prod] = uint8_t(e);
-                            prod += 1;
-                            if (kStaged) bp += e >> 28; else gb.advance(e >> 28);
+                            uint32_t l;
+                            row[j] = uint8_t(single(win, l));
+                            if (kStaged) bp += l; else gb.advance(l);
                         }
                     }
                     __syncwarp();
@@ -593,13 +605,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         }
                     }
                     __syncwarp();
-                    // drop the merged round from this lane's row (the spill moves down)
-                    {
-                        uint32_t *rw = reinterpret_cast<uint32_t *>(row);
-#pragma unroll
-                        for (int k = 0; k < (kRowBytes - kRound) / 4; ++k) rw[k] = rw[k + kRound / 4];
-                    }
-                    cons += kRound;
                 }
 
                 uint32_t st = 0;
@@ -619,7 +624,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     }
 }
 
-template <int kSyms, bool kVec, bool kStaged>
+template <int kPer, bool kVec, bool kStaged>
 int launch(DecodeParams &P, cudaStream_t stream) {
     static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
     static int grid_max[kMaxDevices] = {};
@@ -630,12 +635,12 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         return K3HUF_E_CUDA;
     }
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_kernel<kSyms, kVec, kStaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(kSmemBytes));
         int sms = 0, per_sm = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kSyms, kVec, kStaged>, kThreads,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged>, kThreads,
                                                               kSmemBytes);
         if (e != cudaSuccess) {
             set_cuda_error(int(e));
@@ -645,7 +650,7 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         attr_set[dev] = true;
     }
     const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(grid_max[dev]));
-    decode_kernel<kSyms, kVec, kStaged><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    decode_kernel<kPer, kVec, kStaged><<<grid, kThreads, kSmemBytes, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_cuda_error(int(e));
@@ -654,23 +659,22 @@ int launch(DecodeParams &P, cudaStream_t stream) {
     return K3HUF_OK;
 }
 
-// Decoder variant: the most codes one lookup emits (1, 2 or 3).
-int g_syms = 3;
+// Decoder variant: codes per lockstep lookup (1 or 2).
+int g_per = 2;
 
-template <int kSyms>
+template <int kPer>
 int launch_syms(DecodeParams &P, cudaStream_t stream) {
     const bool vec = P.sub_syms % 8 == 0;
     // a sub-stream's bits (at most 12 per value) must fit the shared buffer
     const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= kBitBuf;
-    if (staged) return vec ? launch<kSyms, true, true>(P, stream) : launch<kSyms, false, true>(P, stream);
-    return vec ? launch<kSyms, true, false>(P, stream) : launch<kSyms, false, false>(P, stream);
+    if (staged) return vec ? launch<kPer, true, true>(P, stream) : launch<kPer, false, true>(P, stream);
+    return vec ? launch<kPer, true, false>(P, stream) : launch<kPer, false, false>(P, stream);
 }
 
 int launch_tasks(DecodeParams &P, cudaStream_t stream) {
-    switch (g_syms) {
+    switch (g_per) {
         case 1: return launch_syms<1>(P, stream);
-        case 2: return launch_syms<2>(P, stream);
-        default: return launch_syms<3>(P, stream);
+        default: return launch_syms<2>(P, stream);
     }
 }
 
@@ -690,8 +694,8 @@ using namespace k3huf;
 extern "C" int k3huf_last_cuda_error(void) { return g_last_cuda_error; }
 
 extern "C" int k3huf_set_decoder_variant(int variant) {
-    if (variant < 0 || variant > 3) return K3HUF_E_ARG;
-    g_syms = variant == 0 ? 3 : variant;
+    if (variant < 0 || variant > 2) return K3HUF_E_ARG;
+    g_per = variant == 0 ? 2 : variant;
     return K3HUF_OK;
 }
 
