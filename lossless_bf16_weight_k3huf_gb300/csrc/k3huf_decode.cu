@@ -59,8 +59,9 @@ constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
 
 // Lockstep table, indexed by the next 12 bits: exactly kPer whole codes.
 //   [7:0] first symbol [15:8] second symbol [31:28] bits used by the kPer
-//   codes; 0 there when the window does not start with kPer codes of at
-//   most 12 bits in total (then the codes are read one at a time).
+//   codes.  0 in [31:28] when the window does not hold kPer whole codes:
+//   then [11:8] is the first code's length (0: no code starts here) and the
+//   second code is read from the single-code table.
 // Single-code table: the 4096-entry (sym << 4) | length table.
 constexpr size_t kSmemLut = 4096 * sizeof(uint32_t);
 constexpr size_t kSmemL12 = 4096 * sizeof(uint16_t);
@@ -286,7 +287,10 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
             } else {
                 const uint32_t b = lut1[(e << l1) & 4095u];
                 const uint32_t l2 = b & 15u;
-                if (l2 != 0 && l1 + l2 <= K3HUF_MAXLEN) ent = (a >> 4) | ((b >> 4) << 8) | ((l1 + l2) << 28);
+                if (l2 != 0 && l1 + l2 <= K3HUF_MAXLEN)
+                    ent = (a >> 4) | ((b >> 4) << 8) | ((l1 + l2) << 28);
+                else
+                    ent = (a >> 4) | (l1 << 8);        // second code read separately
             }
         }
         lut[e] = ent;
@@ -492,29 +496,52 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     return a >> 4;
                 };
 
+                // low bytes of a round, loaded one round ahead
+                uint2 ev[8];
+                auto load_even = [&](uint32_t round) {
+                    const uint32_t v = round * kRound + sub * 8u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t gi = g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
+                        ev[i] = kVec && v < piece_len(i)
+                                    ? __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v))
+                                    : make_uint2(0, 0);
+                    }
+                };
+                load_even(0);
+
                 for (uint32_t r = 0; r < n_rounds; ++r) {
                     const uint32_t rem = len > r * kRound ? len - r * kRound : 0u;
                     uint8_t *row = wrows + size_t(lane) * kRowBytes;
                     if (kStaged && __all_sync(0xffffffffu, rem >= uint32_t(kRound))) {
                         // lockstep round: every lookup yields exactly kPer codes, so
-                        // the round's 64 high bytes land in registers at fixed places
-                        uint32_t R[kRound / 4];
-#pragma unroll
+                        // each group of 4 lookups fills 4 * kPer bytes at a fixed place
+#pragma unroll 4
                         for (int grp = 0; grp < kRound / (4 * kPer); ++grp) {
-                            uint32_t cur = bp, hi, lo;
+                            uint32_t cur = bp, cur0 = bp, hi, lo;
                             window(cur, hi, lo);
+                            uint32_t R0 = 0, R1 = 0;
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                const int j = grp * 4 + k;              // lookup index in the round
                                 uint32_t e = lut[hi >> 20];
                                 uint32_t t = e >> 28;
                                 if (t == 0) {
-                                    // fewer than kPer codes fit the window: read them one at a time
-                                    window(cur, hi, lo);
-                                    uint32_t l, syms = single(hi, l);
-                                    t = l;
+                                    // the window does not hold kPer whole codes: take the
+                                    // first code from the entry, read the second one alone.
+                                    // The 64-bit window must still cover this lookup (up to
+                                    // 24 bits) and the group's remaining normal lookups (up
+                                    // to 12 bits each): reload it when it might not
+                                    if (cur - cur0 > 4u + 12u * uint32_t(k)) {
+                                        window(cur, hi, lo);
+                                        cur0 = cur;
+                                    }
+                                    uint32_t l = (e >> 8) & 15u;
+                                    bad |= l == 0;
+                                    l += l == 0;
+                                    uint32_t syms = e & 0xFFu;
                                     hi = __funnelshift_l(lo, hi, l);
                                     lo <<= l;
+                                    t = l;
                                     if (kPer == 2) {
                                         syms |= single(hi, l) << 8;
                                         t += l;
@@ -523,27 +550,27 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                                     }
                                     cur += t;
                                     e = syms;
-                                    // the shifted window stays valid for the group's other lookups
-                                    t = 0;
                                 } else {
                                     cur += t;
                                     hi = __funnelshift_l(lo, hi, t);
                                     lo <<= t;
                                 }
                                 if (kPer == 2) {
-                                    if (j & 1) R[j >> 1] |= e << 16;
-                                    else R[j >> 1] = e & 0xFFFFu;
+                                    if (k == 0) R0 = e & 0xFFFFu;
+                                    if (k == 1) R0 |= e << 16;
+                                    if (k == 2) R1 = e & 0xFFFFu;
+                                    if (k == 3) R1 |= e << 16;
                                 } else {
-                                    if (j & 3) R[j >> 2] |= (e & 0xFFu) << (8 * (j & 3));
-                                    else R[j >> 2] = e & 0xFFu;
+                                    if (k == 0) R0 = e & 0xFFu;
+                                    else R0 |= (e & 0xFFu) << (8 * k);
                                 }
                             }
                             bp = cur;
+                            if (kPer == 2)
+                                reinterpret_cast<uint2 *>(row)[grp] = make_uint2(R0, R1);
+                            else
+                                reinterpret_cast<uint32_t *>(row)[grp] = R0;
                         }
-                        uint4 *row4 = reinterpret_cast<uint4 *>(row);
-#pragma unroll
-                        for (int k = 0; k < kRound / 16; ++k)
-                            row4[k] = make_uint4(R[4 * k], R[4 * k + 1], R[4 * k + 2], R[4 * k + 3]);
                     } else {
                         // partial round (a stream's end or a split pass): exact single codes
                         const uint32_t cnt = min(rem, uint32_t(kRound));
@@ -563,13 +590,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     __syncwarp();
                     if (kVec) {
                         const uint32_t v = r * kRound + sub * 8u;
-                        uint2 ev[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {       // all low-byte loads in flight at once
-                            const uint32_t gi = g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
-                            ev[i] = v < piece_len(i) ? __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v))
-                                                     : make_uint2(0, 0);
-                        }
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const uint32_t m_len = piece_len(i);
@@ -595,6 +615,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                                 }
                             }
                         }
+                        if (r + 1 < n_rounds) load_even(r + 1);   // in flight while the next round decodes
                     } else if (len) {
                         // scalar path for sub-stream sizes that break 8-value alignment
                         const uint32_t a0 = r * kRound, b0 = min(len, a0 + kRound);
