@@ -56,6 +56,7 @@ constexpr uint32_t kBitBuf = 7744;            // bytes of staged bit stream per 
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
+constexpr int kMaxHeavy = 64;                 // items listed for the first sweep of a table phase
 
 // Lockstep table, indexed by the next 12 bits: exactly kPer whole codes.
 //   [7:0] first symbol [15:8] second symbol [31:28] bits used by the kPer
@@ -308,6 +309,24 @@ __device__ __forceinline__ uint32_t find_task(const DecodeParams &P, uint32_t it
     return lo;
 }
 
+// Whether a work item's bits (estimated at chunk granularity from the
+// chunk offsets) overflow one staging pass.  Such items take two or more
+// passes and are started first.  Deterministic in the container bytes, so
+// every warp classifies an item the same way; reads stay inside the stripe.
+__device__ bool item_heavy(const DecodeParams &P, uint32_t wi) {
+    const StripeTask &T = P.task[find_task(P, wi)];
+    const uint32_t cs = P.chunk_syms, S = cs / P.sub_syms;
+    const uint32_t nch = (T.n_values + cs - 1) / cs;
+    if (uint64_t(K3HUF_STRIPE_HDR_BYTES) + 4ull * nch > T.stripe_bytes) return false;
+    const uint32_t *h = reinterpret_cast<const uint32_t *>(T.stripe);
+    const uint32_t *chunk_off = h + K3HUF_STRIPE_HDR_BYTES / 4;
+    const uint32_t g0 = (wi - T.item_begin) * kItem;
+    const uint32_t c0 = g0 / S, c1 = min(nch, (g0 + kItem - 1) / S + 1);
+    if (c0 >= nch) return false;
+    const uint32_t lo = chunk_off[c0], hi = c1 < nch ? chunk_off[c1] : h[4];
+    return hi > lo && (hi - lo) / 8 + 64 > kBitBuf;
+}
+
 __device__ __forceinline__ uint32_t interleave_lo(uint32_t even4, uint32_t hi4) { return __byte_perm(even4, hi4, 0x5140); }
 __device__ __forceinline__ uint32_t interleave_hi(uint32_t even4, uint32_t hi4) { return __byte_perm(even4, hi4, 0x7362); }
 
@@ -337,6 +356,8 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemLut);
     __shared__ uint8_t s_len[256];
     __shared__ __align__(8) uint64_t s_bar[kWarps];
+    __shared__ uint32_t s_heavy[kMaxHeavy];
+    __shared__ uint32_t s_nheavy, s_next;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *wslot = smem + kSmemLut + kSmemL12 + size_t(warp) * kWarpSlot;
@@ -344,8 +365,9 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     uint8_t *wrows = wslot + kBitBuf + 16;
 
     const uint32_t cs = P.chunk_syms, ss = P.sub_syms, S = cs / ss;
-    const uint32_t per = (P.n_items + gridDim.x - 1) / gridDim.x;
-    const uint32_t it0 = blockIdx.x * per, it1 = min(P.n_items, it0 + per);
+    // contiguous item ranges whose sizes differ by at most one
+    const uint32_t it0 = uint32_t(uint64_t(blockIdx.x) * P.n_items / gridDim.x);
+    const uint32_t it1 = uint32_t(uint64_t(blockIdx.x + 1) * P.n_items / gridDim.x);
     int table_built = -1;
     bool table_bad = false, dead = false;
     uint32_t phase = 0;
@@ -374,9 +396,35 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             table_built = table;
             if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
         }
+        if (tid == 0) {
+            s_nheavy = 0;
+            s_next = 0;
+        }
         __syncthreads();
+        // list the phase's multi-pass items; warps then take items from a
+        // shared counter, listed items first, the rest in index order
+        for (uint32_t i = item + uint32_t(tid); i < pend && !table_bad; i += kThreads)
+            if (item_heavy(P, i)) {
+                const uint32_t k = atomicAdd(&s_nheavy, 1u);
+                if (k < kMaxHeavy) s_heavy[k] = i;
+            }
+        __syncthreads();
+        const uint32_t nheavy = s_nheavy <= uint32_t(kMaxHeavy) ? s_nheavy : 0u;   // overflow: index order only
 
-        for (uint32_t wi = item + uint32_t(warp); wi < pend && !table_bad && !dead; wi += kWarps) {
+        while (!table_bad && !dead) {
+            uint32_t v = 0;
+            if (lane == 0) v = atomicAdd(&s_next, 1u);
+            v = __shfl_sync(0xffffffffu, v, 0);
+            uint32_t wi;
+            if (v < nheavy) {
+                wi = s_heavy[v];
+            } else {
+                if (v - nheavy >= pend - item) break;
+                wi = item + (v - nheavy);
+                bool listed = false;
+                for (uint32_t k = uint32_t(lane); k < nheavy; k += 32) listed |= s_heavy[k] == wi;
+                if (__any_sync(0xffffffffu, listed)) continue;       // taken in the first sweep
+            }
             const uint32_t ti = find_task(P, wi);
             const StripeTask &T = P.task[ti];
             uint32_t hdr[8];
