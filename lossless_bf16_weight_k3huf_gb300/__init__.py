@@ -166,7 +166,7 @@ def tensor_info(hdr, t: int) -> dict:
 
 
 def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, threads: int = 0,
-                 out: np.ndarray | None = None, sub_syms: int = 512) -> np.ndarray:
+                 out: np.ndarray | None = None, sub_syms: int = 256) -> np.ndarray:
     """Container bytes of a layer of bf16 tensors (numpy uint16 / torch bf16
     CPU); chunk_syms values per indexed chunk, sub_syms per sub-stream."""
     arrs = []

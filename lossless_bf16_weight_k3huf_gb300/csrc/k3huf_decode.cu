@@ -15,19 +15,24 @@
 //
 // GPU mapping (no tensor cores: a bit-serial scan bound by HBM bandwidth):
 //  - the sub-stream index splits every chunk into independently decodable
-//    sub-streams; lane = sub-stream.  A work item is 128 consecutive
-//    sub-streams (a CTA of 4 warps); their bits are one contiguous range of
-//    the stripe's stream, staged into shared memory by one TMA bulk copy
-//    (cp.async.bulk + mbarrier, bounded wait).  A persistent grid walks
-//    contiguous item ranges and rebuilds the code table only when it changes;
-//  - each lookup reads the 12-bit window at its bit position with a funnel
-//    shift of two shared words (no per-lane refill branch) and emits up to
-//    three codes from a multi-symbol table; the warp loops on a warp-uniform
-//    condition, so lanes never diverge;
-//  - decoded high bytes go to a per-lane row in shared memory; every 64
-//    values the warp merges its 32 sub-streams' high bytes with their raw
-//    low bytes (8-byte loads issued one round early) into coalesced 16-byte
-//    bf16 stores;
+//    sub-streams; lane = sub-stream.  A work item is 32 consecutive
+//    sub-streams (one warp); their bits are one contiguous range of the
+//    stripe's stream, staged into the warp's shared-memory slot by one bulk
+//    copy (cp.async.bulk + the warp's mbarrier, bounded wait).  An item too
+//    long for the slot is decoded in passes over prefixes of its lanes;
+//  - one persistent CTA of 20 warps per SM takes a contiguous item range and
+//    rebuilds the code table only when it changes; inside a table phase the
+//    warps take items from a shared counter, multi-pass items first;
+//  - every lockstep lookup emits exactly two codes from a 12-bit
+//    double-symbol table (a window that does not hold two whole codes gives
+//    the first code and the second is read from the single-code table), so
+//    all lanes of the warp advance by the same number of values per step and
+//    never diverge; the window is a funnel shift of three shared words,
+//    reloaded every four lookups;
+//  - a round's 64 high bytes per lane are built in registers and stored to a
+//    per-lane row in shared memory; every 64 values the warp merges its 32
+//    sub-streams' high bytes with their raw low bytes (loads issued one round
+//    early) into coalesced 16-byte bf16 stores;
 //  - a sub-stream that ends away from the next recorded bit offset, or an
 //    undecodable window, sets a status bit; every loop is bounded by value
 //    counts, every shared/global read index is clamped, and the only wait

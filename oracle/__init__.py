@@ -147,7 +147,7 @@ def decode_window(codelen, window: int, maxlen: int = MAXLEN):
 
 
 def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, maxlen: int = MAXLEN,
-                 sub_syms: int = 512) -> np.ndarray:
+                 sub_syms: int = 256) -> np.ndarray:
     """Container bytes (uint8) of a layer made of the given bf16 tensors
     (uint16 arrays); sub_syms = values per sub-stream (0: no sub index)."""
     ts = [np.ascontiguousarray(t, dtype=np.uint16).reshape(-1) for t in tensors]

@@ -87,7 +87,7 @@ def _expected_sub_syms(chunk_syms, sub_syms):
     return sub_syms
 
 
-def check_layout(blob, tensors, chunk_syms=4096, shared=False, sub_syms=512):
+def check_layout(blob, tensors, chunk_syms=4096, shared=False, sub_syms=256):
     h = parse(blob)
     ss = _expected_sub_syms(chunk_syms, sub_syms)
     assert h["sub_syms"] == ss
@@ -308,7 +308,8 @@ def test_incomplete_code_invalid_window_is_rejected():
     blob[o + 16: o + 24] = np.frombuffer((5).to_bytes(8, "little"), np.uint8)
     blob[o + st["bits_offset"]] = 0b10011000           # 1 00 1 1
     so = o + 32 + 4 * st["n_chunks"]                   # sub-stream starts past the end: all at bit 5
-    blob[so: so + 14] = np.frombuffer(np.full(7, 5, "<u2").tobytes(), np.uint8)
+    k = h["chunk_syms"] // h["sub_syms"] - 1
+    blob[so: so + 2 * k] = np.frombuffer(np.full(k, 5, "<u2").tobytes(), np.uint8)
     rc, out = oracle.decode_layer(blob)
     assert rc == 0 and np.array_equal(out[:8].view(np.uint16), x)
     bad = blob.copy()
