@@ -20,7 +20,7 @@
 //    stripe's stream, staged into the warp's shared-memory slot by one bulk
 //    copy (cp.async.bulk + the warp's mbarrier, bounded wait).  An item too
 //    long for the slot is decoded in passes over prefixes of its lanes;
-//  - one persistent CTA of 20 warps per SM takes a contiguous item range and
+//  - one persistent CTA of 16 warps per SM takes a contiguous item range and
 //    rebuilds the code table only when it changes; inside a table phase the
 //    warps take items from a shared counter, multi-pass items first;
 //  - every lockstep lookup emits exactly two codes from a 12-bit
@@ -52,11 +52,11 @@ void set_cuda_error(int code) { g_last_cuda_error = code; }
 
 namespace {
 
-constexpr int kWarps = 20;                    // one CTA per SM
+constexpr int kWarps = 16;                    // one CTA per SM
 constexpr int kThreads = 32 * kWarps;
 constexpr int kItem = 32;                     // sub-streams per work item (one warp)
 constexpr int kRound = 64;                    // values per lane between merges
-constexpr int kRowBytes = 80;                 // per-lane row: one round of high bytes + pad (20 words)
+constexpr int kRowBytes = 64;                 // per-lane row: one round of high bytes (8-byte units, swizzled)
 constexpr uint32_t kBitBuf = 7744;            // bytes of staged bit stream per warp and pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
@@ -64,9 +64,10 @@ constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
 constexpr int kMaxHeavy = 64;                 // items listed for the first sweep of a table phase
 
 // Lockstep table, indexed by the next 12 bits: exactly kPer whole codes.
-//   [7:0] first symbol [15:8] second symbol [31:28] bits used by the kPer
-//   codes.  0 in [31:28] when the window does not hold kPer whole codes:
-//   then [11:8] is the first code's length (0: no code starts here) and the
+//   [4:0] bits used by the kPer codes (the shift, taken straight from the
+//   entry by a wrapping funnel shift) [23:16] first symbol [31:24] second
+//   symbol.  0 in [4:0] when the window does not hold kPer whole codes: then
+//   [11:8] is the first code's length (0: no code starts here) and the
 //   second code is read from the single-code table.
 // Single-code table: the 4096-entry (sym << 4) | length table.
 constexpr size_t kSmemLut = 4096 * sizeof(uint32_t);
@@ -96,6 +97,12 @@ struct DecodeParams {
 };
 
 __device__ __forceinline__ uint32_t bswap32(uint32_t x) { return __byte_perm(x, 0, 0x0123); }
+
+// Row swizzle: 8-byte unit u of lane l's row sits at unit u ^ row_swz(l).
+// The 32 lanes' 8-byte stores of one unit, and the merge's 8-byte reads of
+// unit (lane % 8) of rows 4i .. 4i+3, then each touch every bank exactly twice.
+__device__ __forceinline__ uint32_t row_swz(uint32_t l) { return (l >> 1) & 7u; }
+__device__ __forceinline__ uint32_t row_byte(uint32_t j, uint32_t swz) { return (((j >> 3) ^ swz) << 3) | (j & 7u); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -289,14 +296,14 @@ __device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *
         uint32_t ent = 0;
         if (l1 != 0) {
             if (kPer == 1) {
-                ent = (a >> 4) | (l1 << 28);
+                ent = ((a >> 4) << 16) | l1;
             } else {
                 const uint32_t b = lut1[(e << l1) & 4095u];
                 const uint32_t l2 = b & 15u;
                 if (l2 != 0 && l1 + l2 <= K3HUF_MAXLEN)
-                    ent = (a >> 4) | ((b >> 4) << 8) | ((l1 + l2) << 28);
+                    ent = ((a >> 4) << 16) | ((b >> 4) << 24) | (l1 + l2);
                 else
-                    ent = (a >> 4) | (l1 << 8);        // second code read separately
+                    ent = ((a >> 4) << 16) | (l1 << 8);        // second code read separately
             }
         }
         lut[e] = ent;
@@ -566,6 +573,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 for (uint32_t r = 0; r < n_rounds; ++r) {
                     const uint32_t rem = len > r * kRound ? len - r * kRound : 0u;
                     uint8_t *row = wrows + size_t(lane) * kRowBytes;
+                    const uint32_t swz = row_swz(uint32_t(lane));
                     if (kStaged && __all_sync(0xffffffffu, rem >= uint32_t(kRound))) {
                         // lockstep round: every lookup yields exactly kPer codes, so
                         // each group of 4 lookups fills 4 * kPer bytes at a fixed place
@@ -573,56 +581,57 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         for (int grp = 0; grp < kRound / (4 * kPer); ++grp) {
                             uint32_t cur = bp, cur0 = bp, hi, lo;
                             window(cur, hi, lo);
-                            uint32_t R0 = 0, R1 = 0;
+                            uint32_t ek[4];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
                                 uint32_t e = lut[hi >> 20];
-                                uint32_t t = e >> 28;
-                                if (t == 0) {
-                                    // the window does not hold kPer whole codes: take the
-                                    // first code from the entry, read the second one alone.
-                                    // The 64-bit window must still cover this lookup (up to
-                                    // 24 bits) and the group's remaining normal lookups (up
-                                    // to 12 bits each): reload it when it might not
-                                    if (cur - cur0 > 4u + 12u * uint32_t(k)) {
-                                        window(cur, hi, lo);
-                                        cur0 = cur;
+                                uint32_t t = e & 31u;
+                                // a whole-pair entry shifts the window by its low five bits
+                                uint32_t nhi = __funnelshift_l(lo, hi, e), nlo = __funnelshift_l(0u, lo, e);
+                                {
+                                    if (t == 0u) {
+                                        // the window does not hold kPer whole codes: take the
+                                        // first code from the entry, read the second one alone.
+                                        // The 64-bit window must still cover this lookup (up to
+                                        // 24 bits) and the group's remaining normal lookups (up
+                                        // to 12 bits each): reload it when it might not
+                                        if (cur - cur0 > 4u + 12u * uint32_t(k)) {
+                                            window(cur, hi, lo);
+                                            cur0 = cur;
+                                        }
+                                        uint32_t l = (e >> 8) & 15u;
+                                        bad |= l == 0;
+                                        l += l == 0;
+                                        uint32_t syms = e & 0x00FF0000u;
+                                        nhi = __funnelshift_l(lo, hi, l);
+                                        nlo = lo << l;
+                                        t = l;
+                                        if (kPer == 2) {
+                                            syms |= single(nhi, l) << 24;
+                                            t += l;
+                                            nhi = __funnelshift_l(nlo, nhi, l);
+                                            nlo <<= l;
+                                        }
+                                        e = syms;
                                     }
-                                    uint32_t l = (e >> 8) & 15u;
-                                    bad |= l == 0;
-                                    l += l == 0;
-                                    uint32_t syms = e & 0xFFu;
-                                    hi = __funnelshift_l(lo, hi, l);
-                                    lo <<= l;
-                                    t = l;
-                                    if (kPer == 2) {
-                                        syms |= single(hi, l) << 8;
-                                        t += l;
-                                        hi = __funnelshift_l(lo, hi, l);
-                                        lo <<= l;
-                                    }
-                                    cur += t;
-                                    e = syms;
-                                } else {
-                                    cur += t;
-                                    hi = __funnelshift_l(lo, hi, t);
-                                    lo <<= t;
                                 }
-                                if (kPer == 2) {
-                                    if (k == 0) R0 = e & 0xFFFFu;
-                                    if (k == 1) R0 |= e << 16;
-                                    if (k == 2) R1 = e & 0xFFFFu;
-                                    if (k == 3) R1 |= e << 16;
-                                } else {
-                                    if (k == 0) R0 = e & 0xFFu;
-                                    else R0 |= (e & 0xFFu) << (8 * k);
-                                }
+                                hi = nhi;
+                                lo = nlo;
+                                cur += t;
+                                ek[k] = e;
+                            }
+                            uint32_t R0, R1 = 0;
+                            if (kPer == 2) {
+                                R0 = __byte_perm(ek[0], ek[1], 0x7632);
+                                R1 = __byte_perm(ek[2], ek[3], 0x7632);
+                            } else {
+                                R0 = __byte_perm(__byte_perm(ek[0], ek[1], 0x0062), __byte_perm(ek[2], ek[3], 0x0062), 0x5410);
                             }
                             bp = cur;
                             if (kPer == 2)
-                                reinterpret_cast<uint2 *>(row)[grp] = make_uint2(R0, R1);
+                                reinterpret_cast<uint2 *>(row)[uint32_t(grp) ^ swz] = make_uint2(R0, R1);
                             else
-                                reinterpret_cast<uint32_t *>(row)[grp] = R0;
+                                reinterpret_cast<uint32_t *>(row)[((uint32_t(grp >> 1) ^ swz) << 1) | uint32_t(grp & 1)] = R0;
                         }
                     } else {
                         // partial round (a stream's end or a split pass): exact single codes
@@ -636,7 +645,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                                 win = gb.window();
                             }
                             uint32_t l;
-                            row[j] = uint8_t(single(win, l));
+                            row[row_byte(j, swz)] = uint8_t(single(win, l));
                             if (kStaged) bp += l; else gb.advance(l);
                         }
                     }
@@ -648,8 +657,8 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             const uint32_t m_len = piece_len(i);
                             if (v >= m_len) continue;
                             const uint32_t gw = uint32_t(i) * 4u + uint32_t(lane >> 3);
-                            const uint32_t *hrow = reinterpret_cast<const uint32_t *>(wrows + gw * kRowBytes + sub * 8u);
-                            const uint32_t hx = hrow[0], hy = hrow[1];
+                            const uint2 h = *reinterpret_cast<const uint2 *>(wrows + gw * kRowBytes + ((sub ^ row_swz(gw)) << 3));
+                            const uint32_t hx = h.x, hy = h.y;
                             uint4 o;
                             o.x = interleave_lo(ev[i].x, hx);
                             o.y = interleave_hi(ev[i].x, hx);
@@ -675,7 +684,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         const size_t v0 = size_t(g) * ss;
                         for (uint32_t vv = a0; vv < b0; ++vv) {
                             out[2 * (v0 + vv)] = even[v0 + vv];
-                            out[2 * (v0 + vv) + 1] = row[vv - a0];
+                            out[2 * (v0 + vv) + 1] = row[row_byte(vv - a0, swz)];
                         }
                     }
                     __syncwarp();

@@ -193,7 +193,8 @@ def test_fault_undecodable_window():
     blob[o + 16:o + 24] = np.frombuffer((15).to_bytes(8, "little"), np.uint8)
     blob[o + bits_off:o + bits_off + 2] = [0b10011100, 0b11100110]
     so = o + 32 + 4 * 1                                # sub-stream starts past the end: all at bit 15
-    blob[so:so + 14] = np.frombuffer(np.full(7, 15, "<u2").tobytes(), np.uint8)
+    k = int.from_bytes(blob[8:12].tobytes(), "little") // int.from_bytes(blob[56:60].tobytes(), "little") - 1
+    blob[so:so + 2 * k] = np.frombuffer(np.full(k, 15, "<u2").tobytes(), np.uint8)
     assert oracle.decode_layer(blob)[0] == 0
     out, st, _ = gpu_decode(blob)
     assert st == 0 and np.array_equal(out[:24].view(np.uint16), x)
