@@ -569,12 +569,19 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     }
                 };
                 load_even(0);
+                // full rounds (every sub-stream of the item has 64 more values in
+                // this pass): piece i sits 4 * i sub-streams after piece 0
+                const uint32_t q = uint32_t(lane) >> 3;
+                uint8_t *const out_p0 = out + 2 * (size_t(g0 + q) * ss + sub * 8u);
+                const uint8_t *const even_p0 = even + size_t(g0 + q) * ss + sub * 8u;
+                const size_t pstride = size_t(4) * ss;
 
                 for (uint32_t r = 0; r < n_rounds; ++r) {
                     const uint32_t rem = len > r * kRound ? len - r * kRound : 0u;
                     uint8_t *row = wrows + size_t(lane) * kRowBytes;
                     const uint32_t swz = row_swz(uint32_t(lane));
-                    if (kStaged && __all_sync(0xffffffffu, rem >= uint32_t(kRound))) {
+                    const bool full = __all_sync(0xffffffffu, rem >= uint32_t(kRound));
+                    if (kStaged && full) {
                         // lockstep round: every lookup yields exactly kPer codes, so
                         // each group of 4 lookups fills 4 * kPer bytes at a fixed place
 #pragma unroll 4
@@ -650,7 +657,27 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         }
                     }
                     __syncwarp();
-                    if (kVec) {
+                    if (kVec && full) {
+                        const uint32_t rv = r * kRound;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t gw = uint32_t(i) * 4u + q;
+                            const uint2 h = *reinterpret_cast<const uint2 *>(wrows + gw * kRowBytes + ((sub ^ row_swz(gw)) << 3));
+                            uint4 o;
+                            o.x = interleave_lo(ev[i].x, h.x);
+                            o.y = interleave_hi(ev[i].x, h.x);
+                            o.z = interleave_lo(ev[i].y, h.y);
+                            o.w = interleave_hi(ev[i].y, h.y);
+                            *reinterpret_cast<uint4 *>(out_p0 + 2 * (size_t(i) * pstride + rv)) = o;
+                        }
+                        if (__all_sync(0xffffffffu, rem >= uint32_t(2 * kRound))) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                ev[i] = __ldg(reinterpret_cast<const uint2 *>(even_p0 + size_t(i) * pstride + rv + kRound));
+                        } else if (r + 1 < n_rounds) {
+                            load_even(r + 1);
+                        }
+                    } else if (kVec) {
                         const uint32_t v = r * kRound + sub * 8u;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
