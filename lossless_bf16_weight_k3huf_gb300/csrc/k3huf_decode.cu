@@ -370,6 +370,8 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     __shared__ __align__(8) uint64_t s_bar[kWarps];
     __shared__ uint32_t s_heavy[kMaxHeavy];
     __shared__ uint32_t s_nheavy, s_next;
+    __shared__ uint32_t s_hdr[kMaxTasks][8];     // stripe headers, validated once per CTA
+    __shared__ uint8_t s_hok[kMaxTasks];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *wslot = smem + kSmemLut + kSmemL12 + size_t(warp) * kWarpSlot;
@@ -387,6 +389,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     if (lane == 0) {
         mbar_init(&s_bar[warp]);
         fence_proxy_async();
+    }
+    for (uint32_t u = uint32_t(tid); u < P.n_tasks; u += kThreads) {
+        uint32_t h[8];
+        s_hok[u] = stripe_header_ok(P, P.task[u], h) ? 1 : 0;
+        for (int i = 0; i < 8; ++i) s_hdr[u][i] = h[i];
     }
     __syncthreads();
 
@@ -440,8 +447,8 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             const uint32_t ti = find_task(P, wi);
             const StripeTask &T = P.task[ti];
             uint32_t hdr[8];
-            const bool ok = stripe_header_ok(P, T, hdr);      // every lane reads the same 32 bytes
-            if (!ok) {
+            for (int i = 0; i < 8; ++i) hdr[i] = s_hdr[ti][i];
+            if (!s_hok[ti]) {
                 if (lane == 0 && wi == T.item_begin) atomicOr(P.status, K3HUF_ST_HEADER);
                 continue;
             }
@@ -496,6 +503,31 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         mbar_arrive_expect_tx(&s_bar[warp], nbytes);
                         bulk_g2s(bitbuf, bits + byte_lo, nbytes, &s_bar[warp]);
                     }
+                }
+
+                // merge-phase assignment (vector path): piece i of this lane is the
+                // item's sub-stream (i * 4 + lane / 8), values [r*64 + (lane % 8) * 8, +8)
+                const uint32_t sub = uint32_t(lane) & 7u;
+                auto piece_len = [&](int i) -> uint32_t {
+                    const uint32_t t = uint32_t(i) * 4u + uint32_t(lane >> 3);
+                    return (t >= pa && t < pb) ? min(ss, n - (g0 + t) * ss) : 0u;
+                };
+                // low bytes of a round, loaded one round ahead (the first round's
+                // loads are in flight while the bit copy lands)
+                uint2 ev[8];
+                auto load_even = [&](uint32_t round) {
+                    const uint32_t v = round * kRound + sub * 8u;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t gi = g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
+                        ev[i] = kVec && v < piece_len(i)
+                                    ? __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v))
+                                    : make_uint2(0, 0);
+                    }
+                };
+                load_even(0);
+
+                if (kStaged) {
                     // bounded wait for the copy
                     uint32_t polls = 0;
                     bool landed = false;
@@ -531,14 +563,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 const uint32_t wlen = __reduce_max_sync(0xffffffffu, len);
                 const uint32_t n_rounds = (wlen + kRound - 1) / kRound;
 
-                // merge-phase assignment (vector path): piece i of this lane is the
-                // item's sub-stream (i * 4 + lane / 8), values [r*64 + (lane % 8) * 8, +8)
-                const uint32_t sub = uint32_t(lane) & 7u;
-                auto piece_len = [&](int i) -> uint32_t {
-                    const uint32_t t = uint32_t(i) * 4u + uint32_t(lane >> 3);
-                    return (t >= pa && t < pb) ? min(ss, n - (g0 + t) * ss) : 0u;
-                };
-
                 // 64-bit window at bit position `cur` of the staged stream
                 auto window = [&](uint32_t cur, uint32_t &hi, uint32_t &lo) {
                     const uint32_t i = min(cur >> 5, max_word);
@@ -556,19 +580,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     return a >> 4;
                 };
 
-                // low bytes of a round, loaded one round ahead
-                uint2 ev[8];
-                auto load_even = [&](uint32_t round) {
-                    const uint32_t v = round * kRound + sub * 8u;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t gi = g0 + uint32_t(i) * 4u + uint32_t(lane >> 3);
-                        ev[i] = kVec && v < piece_len(i)
-                                    ? __ldg(reinterpret_cast<const uint2 *>(even + size_t(gi) * ss + v))
-                                    : make_uint2(0, 0);
-                    }
-                };
-                load_even(0);
                 // full rounds (every sub-stream of the item has 64 more values in
                 // this pass): piece i sits 4 * i sub-streams after piece 0
                 const uint32_t q = uint32_t(lane) >> 3;
