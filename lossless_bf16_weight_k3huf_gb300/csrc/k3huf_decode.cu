@@ -210,83 +210,98 @@ struct GlobalBits {
     }
 };
 
-// Build the single-code and lockstep tables in shared memory from
-// codelen[256].  Returns
-// false, uniformly across the CTA, when the table fails the Kraft check.
-// All threads of the CTA must call it.
+// Build the single-code and lockstep tables in shared memory from the code
+// lengths (thread t < 256 passes the length of symbol t).  Returns false,
+// uniformly across the CTA, when the table fails the Kraft check.  All
+// threads of the CTA must call it.
+//  - warps 0..7 each rank 32 symbols among equal lengths (ascending symbol
+//    order) and count their lengths; warp 0 then walks the lengths from 12
+//    down to 1 for the first codes (longest first, each first code the
+//    previous one plus its count, halved and rounded up), the Kraft sum and
+//    the offsets of each length in the sorted symbol list;
+//  - the codes of length l take the 12-bit windows
+//    [first[l] << (12 - l), (first[l] + count[l]) << (12 - l)), disjoint
+//    across lengths, so every window finds its length by comparisons and its
+//    symbol by one index into the sorted list;
+//  - each lockstep entry reads the single-code table twice.
 template <int kPer>
-__device__ bool build_tables(const uint8_t *__restrict__ codelen_src, uint16_t *lut1, uint32_t *lut, uint8_t *s_len) {
-    __shared__ uint8_t s_rank[256];
+__device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
+    constexpr int L = K3HUF_MAXLEN;
+    __shared__ uint32_t s_wcnt[8][L + 1];          // per warp: symbols of each length
+    __shared__ uint32_t s_wbase[8][L + 1];         // per warp: symbols of each length in earlier warps
+    __shared__ uint32_t s_lo[L + 1], s_hi[L + 1];  // window range of each length
+    __shared__ int32_t s_adj[L + 1];               // sorted-list offset minus first code
+    __shared__ uint32_t s_off[L + 1];
     __shared__ uint8_t s_sorted[256];
-    __shared__ uint32_t s_first[K3HUF_MAXLEN + 1], s_count[K3HUF_MAXLEN + 1], s_off[K3HUF_MAXLEN + 2];
+    __shared__ uint32_t s_badlen;
     __shared__ int s_ok;
-    const int tid = threadIdx.x;
-    for (int i = tid; i < 256; i += kThreads) s_len[i] = codelen_src[i];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) s_badlen = 0;
+    uint32_t ls = 0, rank_in = 0;
     __syncthreads();
-    if (tid < 32) {
-        const int lane = tid;
-        uint32_t run = 0;          // lane j (1..12) counts symbols of length j seen so far
-        bool badlen = false;
-        for (int seg = 0; seg < 8; ++seg) {
-            const int s = seg * 32 + lane;
-            const uint32_t l = s_len[s];
-            badlen |= l > K3HUF_MAXLEN;
-            const uint32_t ls = l > K3HUF_MAXLEN ? 0 : l;
-            const uint32_t base = __shfl_sync(0xffffffffu, run, int(ls));
-            const uint32_t same = __match_any_sync(0xffffffffu, ls);
-            s_rank[s] = uint8_t(base + __popc(same & ((1u << lane) - 1u)));
-            for (int j = 1; j <= K3HUF_MAXLEN; ++j) {
-                const uint32_t b = __ballot_sync(0xffffffffu, ls == uint32_t(j));
-                if (lane == j) run += __popc(b);
+    if (tid < 256) {
+        ls = my_len <= uint32_t(L) ? my_len : 0u;
+        if (my_len > uint32_t(L)) atomicOr(&s_badlen, 1u);
+        const uint32_t same = __match_any_sync(0xffffffffu, ls);
+        rank_in = __popc(same & ((1u << lane) - 1u));
+#pragma unroll
+        for (int j = 1; j <= L; ++j) {
+            const uint32_t bj = __ballot_sync(0xffffffffu, ls == uint32_t(j));
+            if (lane == j) s_wcnt[warp][j] = __popc(bj);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // lane l (1..12): counts of length l before each warp, and in total
+        uint32_t c = 0;
+        if (lane >= 1 && lane <= L) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                s_wbase[w][lane] = c;
+                c += s_wcnt[w][lane];
             }
         }
-        badlen = __any_sync(0xffffffffu, badlen);
-        uint32_t code = 0, kraft = 0;
-        for (int l = K3HUF_MAXLEN; l >= 1; --l) {
-            const uint32_t c = __shfl_sync(0xffffffffu, run, l);
-            if (lane == 0) {
-                s_first[l] = code;
-                s_count[l] = c;
-            }
-            code = (code + c + 1) >> 1;
-            kraft += c << (K3HUF_MAXLEN - l);
+        uint32_t code = 0, kraft = 0, first_l = 0;
+        for (int l = L; l >= 1; --l) {
+            const uint32_t cnt = __shfl_sync(0xffffffffu, c, l);
+            if (lane == l) first_l = code;
+            code = (code + cnt + 1) >> 1;
+            kraft += cnt << (L - l);
         }
-        if (lane == 0) {
-            uint32_t off = 0;
-            for (int l = 1; l <= K3HUF_MAXLEN; ++l) {
-                s_off[l] = off;
-                off += s_count[l];
-            }
-            s_ok = (!badlen && kraft > 0 && kraft <= (1u << K3HUF_MAXLEN)) ? 1 : 0;
+        // offsets of each length in the sorted list (ascending length)
+        uint32_t incl = c;                                      // inclusive scan over lanes 1..12
+#pragma unroll
+        for (int d = 1; d < 16; d <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
         }
+        if (lane >= 1 && lane <= L) {
+            const uint32_t off = incl - c;
+            s_off[lane] = off;
+            s_lo[lane] = first_l << (L - lane);
+            s_hi[lane] = (first_l + c) << (L - lane);
+            s_adj[lane] = int32_t(off) - int32_t(first_l);
+        }
+        if (lane == 0) s_ok = (!s_badlen && kraft > 0 && kraft <= (1u << L)) ? 1 : 0;
     }
     __syncthreads();
     if (!s_ok) return false;
-    for (int s = tid; s < 256; s += kThreads) {
-        const uint32_t l = s_len[s];
-        if (l) s_sorted[s_off[l] + s_rank[s]] = uint8_t(s);
+    if (tid < 256 && ls) s_sorted[s_off[ls] + s_wbase[warp][ls] + rank_in] = uint8_t(tid);
+    uint32_t lo[L + 1], hi[L + 1];
+#pragma unroll
+    for (int j = 1; j <= L; ++j) {
+        lo[j] = s_lo[j];
+        hi[j] = s_hi[j];
     }
     __syncthreads();
-    // single-symbol 12-bit table: each thread fills consecutive windows,
-    // one search per run of equal entries
-    {
-        constexpr uint32_t kFill = (4096u + kThreads - 1) / kThreads;
-        const uint32_t e0 = min(uint32_t(tid) * kFill, 4096u), e1 = min(e0 + kFill, 4096u);
-        uint32_t e = e0;
-        while (e < e1) {
-            uint32_t val = 0, end = e + 1;
-            for (int l = 1; l <= K3HUF_MAXLEN; ++l) {
-                const uint32_t pre = e >> (K3HUF_MAXLEN - l);
-                const uint32_t r = pre - s_first[l];
-                if (r < s_count[l]) {
-                    val = (uint32_t(s_sorted[s_off[l] + r]) << 4) | uint32_t(l);
-                    end = (pre + 1) << (K3HUF_MAXLEN - l);
-                    break;
-                }
-            }
-            end = min(end, e1);
-            for (; e < end; ++e) lut1[e] = uint16_t(val);
-        }
+    // single-code 12-bit table: the shortest length whose range holds the window
+    for (uint32_t e = tid; e < 4096u; e += kThreads) {
+        uint32_t l = 0;
+#pragma unroll
+        for (int j = L; j >= 1; --j) l = (e >= lo[j] && e < hi[j]) ? uint32_t(j) : l;
+        uint32_t val = 0;
+        if (l) val = (uint32_t(s_sorted[s_adj[l] + int32_t(e >> (L - l))]) << 4) | l;
+        lut1[e] = uint16_t(val);
     }
     __syncthreads();
     // lockstep table: exactly kPer codes inside the 12-bit window
@@ -366,7 +381,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
     uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemLut);
-    __shared__ uint8_t s_len[256];
     __shared__ __align__(8) uint64_t s_bar[kWarps];
     __shared__ uint32_t s_heavy[kMaxHeavy];
     __shared__ uint32_t s_nheavy, s_next;
@@ -395,7 +409,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         s_hok[u] = stripe_header_ok(P, P.task[u], h) ? 1 : 0;
         for (int i = 0; i < 8; ++i) s_hdr[u][i] = h[i];
     }
-    __syncthreads();
+    // (the first phase's barrier publishes the headers and the mbarriers)
 
     // the CTA's items in phases of one code table each
     uint32_t item = it0;
@@ -408,10 +422,21 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 pend = P.task[u].item_begin;
                 break;
             }
+        // the phase's global reads go out before the barrier: the code
+        // lengths of a new table, and which of the phase's items take more
+        // than one pass (bit k: item item + tid + k * kThreads)
+        const bool rebuild = table != table_built;
+        uint32_t my_len = 0;
+        if (rebuild && tid < 256) my_len = (P.tables ? P.tables + 256ull * table : P.inline_table)[tid];
+        uint32_t hmask = 0;
+        for (uint32_t k = 0; k < 32u; ++k) {
+            const uint32_t i = item + uint32_t(tid) + k * kThreads;
+            if (i >= pend) break;
+            if (item_heavy(P, i)) hmask |= 1u << k;
+        }
         __syncthreads();                              // every warp done with the previous table
-        if (table != table_built) {
-            const uint8_t *codelen = P.tables ? P.tables + 256ull * table : P.inline_table;
-            table_bad = !build_tables<kPer>(codelen, lut1, lut, s_len);
+        if (rebuild) {
+            table_bad = !build_tables<kPer>(my_len, lut1, lut);
             table_built = table;
             if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
         }
@@ -422,11 +447,17 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         __syncthreads();
         // list the phase's multi-pass items; warps then take items from a
         // shared counter, listed items first, the rest in index order
-        for (uint32_t i = item + uint32_t(tid); i < pend && !table_bad; i += kThreads)
-            if (item_heavy(P, i)) {
+        if (!table_bad) {
+            for (; hmask; hmask &= hmask - 1u) {
                 const uint32_t k = atomicAdd(&s_nheavy, 1u);
-                if (k < kMaxHeavy) s_heavy[k] = i;
+                if (k < kMaxHeavy) s_heavy[k] = item + uint32_t(tid) + uint32_t(__ffs(hmask) - 1) * kThreads;
             }
+            for (uint32_t i = item + uint32_t(tid) + 32u * kThreads; i < pend; i += kThreads)
+                if (item_heavy(P, i)) {
+                    const uint32_t k = atomicAdd(&s_nheavy, 1u);
+                    if (k < kMaxHeavy) s_heavy[k] = i;
+                }
+        }
         __syncthreads();
         const uint32_t nheavy = s_nheavy <= uint32_t(kMaxHeavy) ? s_nheavy : 0u;   // overflow: index order only
 
