@@ -46,11 +46,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="projection",
-                    choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring"])
+                    choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring", "ring_file"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--variant", type=int, default=0, help="codes per lookup: 0 default (2), 1, 2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ring-layers", type=int, default=14)
+    ap.add_argument("--ring-layers", type=int, default=None, help="layers streamed (ring: 14, ring_file: 4)")
+    ap.add_argument("--feed-dir", default=None, help="directory of the ring_file container file (default: temp dir)")
+    ap.add_argument("--feed-threads", type=int, default=8, help="pread threads of the storage feed")
     ap.add_argument("--sub-syms", type=int, default=None, help="values per sub-stream in the container")
     return ap.parse_args()
 
@@ -199,7 +201,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    name = args.workload if args.workload != "ring" else "trunk_layer"
+    name = "trunk_layer" if args.workload in ("ring", "ring_file") else args.workload
     tensors, blob = make_layer(name)
     info = oracle.layer_info(blob)
     out = np.zeros(info["out_bytes"], dtype=np.uint8)
@@ -271,6 +273,8 @@ def main():
     k3.set_decoder_variant(args.variant)
     if args.workload == "ring":
         return bench_ring(args, rank, world, local, dev)
+    if args.workload == "ring_file":
+        return bench_ring_file(args, rank, world, local, dev)
 
     tensors, blob = make_layer(args.workload, args.sub_syms)
     info = k3.layer_info(blob)
@@ -426,7 +430,7 @@ def bench_ring(args, rank, world, local, dev):
     double-buffered H2D copies overlapped with the decode."""
     import torch
     import lossless_bf16_weight_k3huf_gb300 as k3
-    seeds = workloads.ring_layers(n_layers=args.ring_layers)
+    seeds = workloads.ring_layers(n_layers=args.ring_layers or 14)
     h_layers, infos = [], []
     for s in seeds:
         tensors = workloads.trunk_layer(seed=s)
@@ -472,6 +476,111 @@ def bench_ring(args, rank, world, local, dev):
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": None},
         "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": blob_total, "d2h_bytes_per_step": 0},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _fs_of(path):
+    """Filesystem type and device of the mount holding path (best effort)."""
+    best = ("?", "?", "")
+    try:
+        with open("/proc/mounts") as f:
+            for line in f:
+                dev, mnt, fstype = line.split()[:3]
+                if os.path.realpath(path).startswith(mnt) and len(mnt) >= len(best[2]):
+                    best = (fstype, dev, mnt)
+    except OSError:
+        pass
+    return {"fstype": best[0], "device": best[1], "mount": best[2]}
+
+
+def _drop_cache(path):
+    """Ask the kernel to drop the file's pages (a buffered feed then reads
+    the device, not the page cache)."""
+    fd = os.open(path, os.O_RDONLY)
+    try:
+        os.posix_fadvise(fd, 0, 0, os.POSIX_FADV_DONTNEED)
+    finally:
+        os.close(fd)
+
+
+def bench_ring_file(args, rank, world, local, dev):
+    """Storage feed: trunk layers written once to a container file, then read
+    back every step (O_DIRECT where the filesystem allows it, the file's
+    pages dropped from the page cache before each step) into the pinned
+    ring, copied to HBM and decoded.  The value is end to end: decoded bytes
+    over the host wall time from the first read to the last decode."""
+    import shutil
+    import tempfile
+    import torch
+    import lossless_bf16_weight_k3huf_gb300 as k3
+    n_layers = args.ring_layers or 4
+    seeds = workloads.ring_layers(n_layers=n_layers)
+    blobs, infos = [], []
+    for s in seeds:
+        tensors = workloads.trunk_layer(seed=s)
+        blobs.append(k3.encode_layer(tensors))
+        infos.append(k3.layer_info(blobs[-1]))
+        del tensors
+    total = sum(b.size for b in blobs)
+    d = tempfile.mkdtemp(prefix="k3huf_feed_", dir=args.feed_dir)
+    path = os.path.join(d, "layers.k3huf")
+    try:
+        if shutil.disk_usage(d).free < total + (1 << 30):
+            raise SystemExit(f"not enough free space in {d} for {total} bytes")
+        offs = k3.write_layers(path, blobs)
+        sizes = [b.size for b in blobs]
+        del blobs
+        feed = k3.Feed(path, threads=args.feed_threads)
+        out_bytes = max(i["out_bytes"] for i in infos)
+        outs = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+        d_outs = [outs[i % 2] for i in range(n_layers)]
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        ring = k3.Ring(max(sizes), 2, staged=True)
+        for _ in range(max(1, args.warmup)):
+            _drop_cache(path)
+            ring.run_file(feed, offs, sizes, d_outs, st)
+        if st.item() != 0:
+            raise SystemExit("file-fed decode reported a fault")
+        stats = []
+        with ClockSampler(dev.index) as clk:
+            for _ in range(args.steps):
+                _drop_cache(path)
+                stats.append(ring.run_file(feed, offs, sizes, d_outs, st))
+        direct = feed.direct
+        ring.close()
+        feed.close()
+        fs = _fs_of(d)
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+    raw = sum(i["raw_bytes"] for i in infos)
+    tot = sum(s["total_ms"] for s in stats)
+    rd = sum(s["read_ms"] for s in stats)
+    dec = sum(s["decode_ms"] for s in stats)
+    cp = sum(s["copy_ms"] for s in stats)
+    value = raw * args.steps / (tot / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = (total + raw) / (dec / args.steps / 1e3) / 1e9
+    launches = sum(-(-i["n_stripes"] // 64) for i in infos)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {**describe("ring_file"), "layers": n_layers, "raw_bytes": raw, "blob_bytes": total,
+                   "compression_ratio": round(raw / total, 4), "o_direct": bool(direct),
+                   "feed_threads": args.feed_threads, "filesystem": fs,
+                   "read_gbs": round(total * args.steps / (rd / 1e3) / 1e9, 2),
+                   "decode_only_gbs": round(raw * args.steps / (dec / 1e3) / 1e9, 2),
+                   "copy_only_gbs_h2d": round(total * args.steps / (cp / 1e3) / 1e9, 2),
+                   "read_share_of_wall": round(rd / tot, 3),
+                   "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": None},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": total, "d2h_bytes_per_step": 0},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }

@@ -77,6 +77,7 @@ extern "C" {
 #define K3HUF_E_FORMAT  -5   /* container malformed: magic, version, sizes, offsets */
 #define K3HUF_E_CUDA    -6   /* a CUDA runtime call failed; see k3huf_last_cuda_error */
 #define K3HUF_E_NOMEM   -7   /* host allocation failed (encoder / ring only) */
+#define K3HUF_E_IO      -8   /* file open or read failed (storage feed only) */
 
 /* bits OR-ed into *d_status by the decode kernels */
 #define K3HUF_ST_BADCODE  1u  /* a bit pattern that starts no code */
@@ -204,6 +205,57 @@ int k3huf_ring_run(k3huf_ring *ring, int n_layers, const void *const *h_layers, 
                    void *const *d_outs, const size_t *out_bytes, uint32_t *d_status,
                    k3huf_ring_stats_t *stats);
 int k3huf_ring_destroy(k3huf_ring *ring);
+
+/* Storage feed: containers read from a file straight into the ring's pinned
+ * host slots, then copied and decoded as above.  The article "Kimi K3 纯
+ * CPU 推理中的无损 Trunk 压缩" (section 让方案被搁置的测量) sets the
+ * decoder against a 3 GB/s SSD that streams the trunk; the article
+ * "AIBit-探索开源项目" (section 工作原理：架构, 读取检查点) reads the
+ * checkpoint with O_DIRECT, bypassing the page cache; the article "Kimi K3
+ * 极限部署技术解析：Deltafin 如何在 M1 Max 上运行 2.8T 参数模型" (section
+ * 5.1) reads the next layer on a background thread and contiguous byte
+ * spans with parallel pread calls.  This feed does both: one file descriptor opened with
+ * O_DIRECT where the filesystem allows it (else buffered), each read split
+ * into 8 MiB pieces read by n_threads threads with pread. */
+typedef struct k3huf_feed k3huf_feed;
+
+/* Open path read-only (O_DIRECT when the filesystem accepts it).
+ * n_threads: reader threads per read call (1..64).  K3HUF_E_IO when the
+ * file cannot be opened. */
+int k3huf_feed_open(const char *path, int n_threads, k3huf_feed **feed);
+/* 1 when reads bypass the page cache (O_DIRECT), 0 when buffered, or
+ * K3HUF_E_ARG. */
+int k3huf_feed_direct(const k3huf_feed *feed);
+/* Read bytes [offset, offset + bytes) of the file into h_buf.  offset and
+ * h_buf must be 4096-byte aligned and buf_bytes >= bytes rounded up to 4096
+ * (the read covers whole 4 KiB blocks; bytes past the end of the file are
+ * left as they were).  Blocks until done.  K3HUF_E_ARG on a bad argument,
+ * K3HUF_E_IO when a read fails or the file ends before offset + bytes. */
+int k3huf_feed_read(k3huf_feed *feed, uint64_t offset, size_t bytes, void *h_buf, size_t buf_bytes);
+int k3huf_feed_close(k3huf_feed *feed);
+
+/* A ring that also owns n_slots pinned host slots (slot_bytes rounded up to
+ * 4096 each) for k3huf_ring_run_file. */
+int k3huf_ring_create_staged(size_t slot_bytes, int n_slots, k3huf_ring **ring);
+
+typedef struct {
+    float total_ms;      /* host wall time, first read issued -> last decode finished */
+    float read_ms;       /* host time spent in the file reads */
+    float copy_ms;       /* sum of the host -> device copies' event times */
+    float decode_ms;     /* sum of the decode kernels' event times */
+    uint64_t read_bytes; /* container bytes read from the file */
+    uint64_t out_bytes;  /* bytes decoded */
+} k3huf_feed_stats_t;
+
+/* Decode n_layers containers stored in the feed's file at file_offsets[i]
+ * (4096-byte aligned), layer_bytes[i] bytes each (<= slot_bytes), into
+ * d_outs[i].  Layer i+1 is read into the next host slot while layer i is
+ * copied and decoded; a host slot is reused once its copy has finished and
+ * a device slot once its decode has finished.  Needs a staged ring.
+ * Blocks until done; fills *stats when non-NULL. */
+int k3huf_ring_run_file(k3huf_ring *ring, k3huf_feed *feed, int n_layers, const uint64_t *file_offsets,
+                        const size_t *layer_bytes, void *const *d_outs, const size_t *out_bytes, uint32_t *d_status,
+                        k3huf_feed_stats_t *stats);
 
 /* Last CUDA error code seen by this library on the calling thread. */
 int k3huf_last_cuda_error(void);

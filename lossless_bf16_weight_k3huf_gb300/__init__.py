@@ -19,7 +19,7 @@ import numpy as np
 
 from . import _build
 
-OK, E_ARG, E_EMPTY, E_OVERSUB, E_BADLEN, E_FORMAT, E_CUDA, E_NOMEM = 0, -1, -2, -3, -4, -5, -6, -7
+OK, E_ARG, E_EMPTY, E_OVERSUB, E_BADLEN, E_FORMAT, E_CUDA, E_NOMEM, E_IO = 0, -1, -2, -3, -4, -5, -6, -7, -8
 ST_BADCODE, ST_OVERRUN, ST_INDEX, ST_HEADER, ST_TIMEOUT = 1, 2, 4, 8, 16
 MAXLEN = 12
 STRIPE_VALUES = 1 << 25
@@ -27,8 +27,10 @@ STRIPE_VALUES = 1 << 25
 EXPORTS = [
     "k3huf_build", "k3huf_layer_info", "k3huf_tensor_info", "k3huf_decode_layer", "k3huf_decode_stripe",
     "k3huf_set_decoder_variant", "k3huf_encode_layer", "k3huf_ring_create", "k3huf_ring_run",
-    "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror",
+    "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
+    "k3huf_feed_read", "k3huf_feed_close", "k3huf_ring_create_staged", "k3huf_ring_run_file",
 ]
+FILE_ALIGN = 4096
 
 
 class K3HufError(RuntimeError):
@@ -55,6 +57,11 @@ class TensorInfo(ctypes.Structure):
 class RingStats(ctypes.Structure):
     _fields_ = [("total_ms", ctypes.c_float), ("decode_ms", ctypes.c_float), ("copy_ms", ctypes.c_float),
                 ("h2d_bytes", ctypes.c_uint64), ("out_bytes", ctypes.c_uint64)]
+
+
+class FeedStats(ctypes.Structure):
+    _fields_ = [("total_ms", ctypes.c_float), ("read_ms", ctypes.c_float), ("copy_ms", ctypes.c_float),
+                ("decode_ms", ctypes.c_float), ("read_bytes", ctypes.c_uint64), ("out_bytes", ctypes.c_uint64)]
 
 
 _lib_handle = None
@@ -90,6 +97,14 @@ def _lib():
             L.k3huf_ring_run.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(_vp), ctypes.POINTER(_sz),
                                          ctypes.POINTER(_vp), ctypes.POINTER(_sz), _vp, ctypes.POINTER(RingStats)]
             L.k3huf_ring_destroy.argtypes = [_vp]
+            L.k3huf_feed_open.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(_vp)]
+            L.k3huf_feed_direct.argtypes = [_vp]
+            L.k3huf_feed_read.argtypes = [_vp, ctypes.c_uint64, _sz, _vp, _sz]
+            L.k3huf_feed_close.argtypes = [_vp]
+            L.k3huf_ring_create_staged.argtypes = [_sz, ctypes.c_int, ctypes.POINTER(_vp)]
+            L.k3huf_ring_run_file.argtypes = [_vp, _vp, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64),
+                                              ctypes.POINTER(_sz), ctypes.POINTER(_vp), ctypes.POINTER(_sz), _vp,
+                                              ctypes.POINTER(FeedStats)]
             L.k3huf_strerror.restype = ctypes.c_char_p
             L.k3huf_strerror.argtypes = [ctypes.c_int]
             _lib_handle = L
@@ -214,12 +229,87 @@ def set_decoder_variant(variant: int) -> None:
     _check(_lib().k3huf_set_decoder_variant(variant), "k3huf_set_decoder_variant")
 
 
-class Ring:
-    """Pinned-host -> HBM double-buffered feed of layers into the decoder."""
+class Feed:
+    """A container file opened for the storage feed (O_DIRECT where the
+    filesystem allows it), read with parallel preads."""
 
-    def __init__(self, slot_bytes: int, n_slots: int = 2):
+    def __init__(self, path: str, threads: int = 8):
         self._h = _vp()
-        _check(_lib().k3huf_ring_create(slot_bytes, n_slots, ctypes.byref(self._h)), "k3huf_ring_create")
+        _check(_lib().k3huf_feed_open(os.fsencode(path), threads, ctypes.byref(self._h)), "k3huf_feed_open")
+
+    @property
+    def direct(self) -> bool:
+        return _lib().k3huf_feed_direct(self._h) == 1
+
+    def read(self, offset: int, nbytes: int, buf, buf_bytes: int | None = None) -> None:
+        """Read into host memory at ``buf`` (an address or a numpy/torch CPU
+        buffer); offset and the buffer 4096-byte aligned."""
+        if isinstance(buf, int):
+            addr, cap = buf, buf_bytes
+        elif hasattr(buf, "data_ptr"):
+            addr, cap = int(buf.data_ptr()), _nbytes(buf)
+        else:
+            addr, cap = buf.ctypes.data, buf.nbytes
+        _check(_lib().k3huf_feed_read(self._h, offset, nbytes, addr, cap), "k3huf_feed_read")
+
+    def close(self):
+        if self._h:
+            _lib().k3huf_feed_close(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def aligned_host(nbytes: int, align: int = FILE_ALIGN) -> np.ndarray:
+    """A uint8 host array of nbytes whose first byte is align-aligned."""
+    raw = np.empty(nbytes + align, dtype=np.uint8)
+    off = (-raw.ctypes.data) % align
+    return raw[off: off + nbytes]
+
+
+def write_layers(path: str, blobs) -> list:
+    """Write containers back to back into a file, each at a 4096-aligned
+    offset; returns the offsets."""
+    offs, pos = [], 0
+    with open(path, "wb") as f:
+        for b in blobs:
+            b = _host(b)
+            offs.append(pos)
+            f.write(b.tobytes())
+            pos += b.size
+            pad = (-pos) % FILE_ALIGN
+            f.write(b"\0" * pad)
+            pos += pad
+        f.flush()
+        os.fsync(f.fileno())
+    return offs
+
+
+class Ring:
+    """Pinned-host -> HBM double-buffered feed of layers into the decoder.
+    ``staged=True`` also allocates pinned host slots, for ``run_file``."""
+
+    def __init__(self, slot_bytes: int, n_slots: int = 2, staged: bool = False):
+        self._h = _vp()
+        create = _lib().k3huf_ring_create_staged if staged else _lib().k3huf_ring_create
+        _check(create(slot_bytes, n_slots, ctypes.byref(self._h)), "k3huf_ring_create")
+
+    def run_file(self, feed: "Feed", offsets, sizes, d_outs, d_status) -> dict:
+        """Decode the containers stored in the feed's file at ``offsets``
+        (``sizes`` bytes each) into ``d_outs`` (CUDA tensors)."""
+        n = len(offsets)
+        op = (ctypes.c_uint64 * n)(*[int(o) for o in offsets])
+        sp = (_sz * n)(*[int(x) for x in sizes])
+        dp = (_vp * n)(*[_dptr(d) for d in d_outs])
+        db = (_sz * n)(*[_nbytes(d) for d in d_outs])
+        st = FeedStats()
+        _check(_lib().k3huf_ring_run_file(self._h, feed._h, n, op, sp, dp, db, _dptr(d_status), ctypes.byref(st)),
+               "k3huf_ring_run_file")
+        return {f: getattr(st, f) for f, _ in FeedStats._fields_}
 
     def run(self, h_layers, d_outs, d_status) -> dict:
         """h_layers: pinned host uint8 tensors (containers); d_outs: CUDA tensors."""

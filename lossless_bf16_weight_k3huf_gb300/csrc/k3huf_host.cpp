@@ -259,6 +259,7 @@ extern "C" const char *k3huf_strerror(int code) {
         case K3HUF_E_FORMAT: return "malformed container";
         case K3HUF_E_CUDA: return "CUDA runtime error";
         case K3HUF_E_NOMEM: return "host allocation failed";
+        case K3HUF_E_IO: return "file open or read failed";
         default: return "unknown error";
     }
 }

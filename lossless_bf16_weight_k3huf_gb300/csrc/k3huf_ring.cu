@@ -8,9 +8,12 @@
 // cudaMemcpyAsync from pinned host memory on a copy stream, double (or
 // n-) buffered against the decode kernels on a compute stream, ordered by
 // events: copy i waits until slot (i mod n) was decoded, decode i waits
-// for copy i.
+// for copy i.  A staged ring also owns pinned host slots, filled from a
+// file by the storage feed (k3huf_feed.cpp) while the previous layer is
+// copied and decoded.
 #include <cuda_runtime.h>
 
+#include <chrono>
 #include <new>
 #include <vector>
 
@@ -21,6 +24,9 @@ struct k3huf_ring {
     int n_slots = 0;
     size_t slot_bytes = 0;
     std::vector<void *> slots;
+    size_t host_slot_bytes = 0;
+    std::vector<void *> host_raw;               // pinned allocations, staged rings only
+    std::vector<void *> host_slots;             // 4096-aligned slots inside them
     cudaStream_t copy = nullptr, compute = nullptr;
 };
 
@@ -34,6 +40,8 @@ int fail(cudaError_t e) {
 void release(k3huf_ring *r) {
     for (void *p : r->slots)
         if (p) cudaFree(p);
+    for (void *p : r->host_raw)
+        if (p) cudaFreeHost(p);
     if (r->copy) cudaStreamDestroy(r->copy);
     if (r->compute) cudaStreamDestroy(r->compute);
     delete r;
@@ -64,6 +72,28 @@ extern "C" int k3huf_ring_create(size_t slot_bytes, int n_slots, k3huf_ring **ri
         (e = cudaStreamCreateWithFlags(&r->compute, cudaStreamNonBlocking)) != cudaSuccess) {
         release(r);
         return fail(e);
+    }
+    *ring = r;
+    return K3HUF_OK;
+}
+
+extern "C" int k3huf_ring_create_staged(size_t slot_bytes, int n_slots, k3huf_ring **ring) {
+    k3huf_ring *r = nullptr;
+    int rc = k3huf_ring_create(slot_bytes, n_slots, &r);
+    if (rc != K3HUF_OK) return rc;
+    // file reads bypassing the page cache need 4096-byte aligned buffers; a
+    // small pinned allocation may be carved from a pool at a finer alignment
+    r->host_slot_bytes = (slot_bytes + 4095) / 4096 * 4096;
+    r->host_raw.assign(size_t(n_slots), nullptr);
+    r->host_slots.assign(size_t(n_slots), nullptr);
+    for (int i = 0; i < n_slots; ++i) {
+        cudaError_t e = cudaHostAlloc(&r->host_raw[size_t(i)], r->host_slot_bytes + 4096, cudaHostAllocDefault);
+        if (e != cudaSuccess) {
+            release(r);
+            return fail(e);
+        }
+        const uintptr_t a = reinterpret_cast<uintptr_t>(r->host_raw[size_t(i)]);
+        r->host_slots[size_t(i)] = reinterpret_cast<void *>((a + 4095) / 4096 * 4096);
     }
     *ring = r;
     return K3HUF_OK;
@@ -150,6 +180,96 @@ extern "C" int k3huf_ring_run(k3huf_ring *r, int n_layers, const void *const *h_
             stats->copy_ms += t;
         }
         stats->h2d_bytes = h2d;
+        stats->out_bytes = decoded;
+    }
+    cleanup();
+    if (rc != K3HUF_OK) return rc;
+    if (e != cudaSuccess) return fail(e);
+    return K3HUF_OK;
+}
+
+extern "C" int k3huf_ring_run_file(k3huf_ring *r, k3huf_feed *feed, int n_layers, const uint64_t *file_offsets,
+                                   const size_t *layer_bytes, void *const *d_outs, const size_t *out_bytes,
+                                   uint32_t *d_status, k3huf_feed_stats_t *stats) {
+    if (!r || !feed || n_layers < 1 || !file_offsets || !layer_bytes || !d_outs || !out_bytes || !d_status)
+        return K3HUF_E_ARG;
+    if (r->host_slots.empty()) return K3HUF_E_ARG;                 // not a staged ring
+    for (int i = 0; i < n_layers; ++i)
+        if (!d_outs[i] || layer_bytes[i] == 0 || layer_bytes[i] > r->slot_bytes || file_offsets[i] % 4096 != 0)
+            return K3HUF_E_ARG;
+    std::vector<cudaEvent_t> ev;
+    auto make = [&](cudaEvent_t *out) {
+        cudaError_t e = cudaEventCreate(out);
+        if (e == cudaSuccess) ev.push_back(*out);
+        return e;
+    };
+    auto cleanup = [&] {
+        for (cudaEvent_t x : ev) cudaEventDestroy(x);
+    };
+    std::vector<cudaEvent_t> c0(n_layers), c1(n_layers), d0(n_layers), d1(n_layers);
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < n_layers && e == cudaSuccess; ++i) {
+        if ((e = make(&c0[i])) != cudaSuccess) break;
+        if ((e = make(&c1[i])) != cudaSuccess) break;
+        if ((e = make(&d0[i])) != cudaSuccess) break;
+        e = make(&d1[i]);
+    }
+    if (e != cudaSuccess) {
+        cleanup();
+        return fail(e);
+    }
+    using clock = std::chrono::steady_clock;
+    const auto t_start = clock::now();
+    double read_ms = 0;
+    uint64_t read_bytes = 0, decoded = 0;
+    int rc = K3HUF_OK;
+    for (int i = 0; i < n_layers && e == cudaSuccess && rc == K3HUF_OK; ++i) {
+        const int slot = i % r->n_slots;
+        void *h = r->host_slots[size_t(slot)];
+        // the host slot is free once the copy that last used it has finished
+        if (i >= r->n_slots && (e = cudaEventSynchronize(c1[i - r->n_slots])) != cudaSuccess) break;
+        const auto t0 = clock::now();
+        rc = k3huf_feed_read(feed, file_offsets[i], layer_bytes[i], h, r->host_slot_bytes);
+        read_ms += std::chrono::duration<double, std::milli>(clock::now() - t0).count();
+        if (rc != K3HUF_OK) break;
+        k3huf_layer_info_t info;
+        if ((rc = k3huf_layer_info(h, layer_bytes[i], &info)) != K3HUF_OK) break;
+        if (info.blob_bytes > layer_bytes[i] || info.out_bytes > out_bytes[i]) {
+            rc = K3HUF_E_ARG;
+            break;
+        }
+        read_bytes += layer_bytes[i];
+        decoded += info.raw_bytes;
+        if (i >= r->n_slots) e = cudaStreamWaitEvent(r->copy, d1[i - r->n_slots], 0);   // device slot free
+        if (e == cudaSuccess) e = cudaEventRecord(c0[i], r->copy);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(r->slots[size_t(slot)], h, layer_bytes[i], cudaMemcpyHostToDevice, r->copy);
+        if (e == cudaSuccess) e = cudaEventRecord(c1[i], r->copy);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(r->compute, c1[i], 0);
+        if (e == cudaSuccess) e = cudaEventRecord(d0[i], r->compute);
+        if (e != cudaSuccess) break;
+        // the header is parsed from the host slot before this call returns
+        rc = k3huf_decode_layer(h, layer_bytes[i], r->slots[size_t(slot)], layer_bytes[i], d_outs[i], out_bytes[i],
+                                d_status, r->compute);
+        if (rc == K3HUF_OK) e = cudaEventRecord(d1[i], r->compute);
+    }
+    cudaError_t es = cudaStreamSynchronize(r->copy);
+    cudaError_t ec = cudaStreamSynchronize(r->compute);
+    if (e == cudaSuccess) e = es != cudaSuccess ? es : ec;
+    const double total_ms = std::chrono::duration<double, std::milli>(clock::now() - t_start).count();
+    if (rc == K3HUF_OK && e == cudaSuccess && stats) {
+        float t = 0;
+        stats->total_ms = float(total_ms);
+        stats->read_ms = float(read_ms);
+        stats->copy_ms = 0;
+        stats->decode_ms = 0;
+        for (int i = 0; i < n_layers && e == cudaSuccess; ++i) {
+            if ((e = cudaEventElapsedTime(&t, d0[i], d1[i])) != cudaSuccess) break;
+            stats->decode_ms += t;
+            if ((e = cudaEventElapsedTime(&t, c0[i], c1[i])) != cudaSuccess) break;
+            stats->copy_ms += t;
+        }
+        stats->read_bytes = read_bytes;
         stats->out_bytes = decoded;
     }
     cleanup();

@@ -267,6 +267,49 @@ def test_ring_small_layers():
             assert np.array_equal(oc[a:a + 2 * t["n_values"]].view(np.uint16), x.reshape(-1))
 
 
+def test_ring_from_file(tmp_path):
+    """Storage feed: containers written to a file are read back through the
+    staged ring (more layers than slots) and decode to the oracle's bytes."""
+    layers = [[workloads.normal_tensor((2000 + 13 * i, 64), 0.05, 60 + i)] for i in range(4)]
+    layers.append([workloads.normal_tensor((5,), 0.3, 70), workloads.normal_tensor((4097,), 0.02, 71)])
+    blobs = [oracle.encode_layer(ts) for ts in layers]
+    path = str(tmp_path / "layers.bin")
+    offs = k3.write_layers(path, blobs)
+    feed = k3.Feed(path, threads=3)
+    ring = k3.Ring(max(b.size for b in blobs), 2, staged=True)
+    outs = [torch.full((k3.layer_info(b)["out_bytes"],), SENTINEL, dtype=torch.uint8, device="cuda") for b in blobs]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stats = ring.run_file(feed, offs, [b.size for b in blobs], outs, st)
+    ring.close()
+    feed.close()
+    assert st.item() == 0
+    assert stats["read_bytes"] == sum(b.size for b in blobs)
+    assert stats["out_bytes"] == sum(k3.layer_info(b)["raw_bytes"] for b in blobs)
+    for ts, b, o in zip(layers, blobs, outs):
+        rc, ref = oracle.decode_layer(b)
+        assert rc == 0
+        oc = o.cpu().numpy()
+        for t, x in zip(tensor_regions(b), ts):
+            a0, a1 = t["out_offset"], t["out_offset"] + 2 * t["n_values"]
+            assert np.array_equal(oc[a0:a1], ref[a0:a1])
+            assert np.array_equal(oc[a0:a1].view(np.uint16), x.reshape(-1))
+
+
+def test_ring_from_file_needs_staged_ring(tmp_path):
+    blob = oracle.encode_layer([workloads.tiny()])
+    path = str(tmp_path / "one.bin")
+    offs = k3.write_layers(path, [blob])
+    feed = k3.Feed(path)
+    ring = k3.Ring(blob.size, 2)
+    out = torch.empty(k3.layer_info(blob)["out_bytes"], dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(k3.K3HufError) as e:
+        ring.run_file(feed, offs, [blob.size], [out], st)
+    assert e.value.code == k3.E_ARG
+    ring.close()
+    feed.close()
+
+
 # --- full-size workloads, launched as the benchmark launches them -------------------
 
 def _sampled_parity(blob, tensors, out_dev, n_sample=24, seed=0):
