@@ -43,6 +43,8 @@ void parallel_for(size_t n, int threads, F fn) {
     for (auto &th : pool) th.join();
 }
 
+}  // namespace
+
 // Canonical longest-first code of a length vector (lengths 0 = unused).
 // Returns the code of every used symbol in code[]; first[]/count[] per length.
 void canonical_codes(const uint8_t len[256], uint32_t code[256], uint32_t first[kMaxLen + 1],
@@ -132,7 +134,119 @@ void limit_depths(const uint64_t cnt[256], int depth[256]) {
     }
 }
 
-}  // namespace
+// ---------------------------------------------------------------------------
+// container layout, shared by the CPU and GPU encoders
+
+void plan_stripes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms, uint32_t sub_syms,
+                  bool shared_table, LayerPlan &L) {
+    L.n_tensors = n_tensors;
+    L.n_tables = shared_table ? 1u : n_tensors;
+    L.chunk_syms = chunk_syms;
+    L.sub_syms = sub_syms;
+    L.shared_table = shared_table;
+    L.n_values.assign(n_values, n_values + n_tensors);
+    L.tensor_out.assign(n_tensors, 0);
+    L.stripes.clear();
+    L.out = L.raw = 0;
+    for (uint32_t t = 0; t < n_tensors; ++t) {
+        L.out = align_up(L.out, 256);
+        L.tensor_out[t] = L.out;
+        for (uint64_t v0 = 0; v0 < n_values[t]; v0 += K3HUF_STRIPE_VALUES) {
+            PlanStripe p{};
+            p.tensor = t;
+            p.table = shared_table ? 0u : t;
+            p.v0 = v0;
+            p.n = std::min<uint64_t>(K3HUF_STRIPE_VALUES, n_values[t] - v0);
+            p.out_offset = L.out + 2 * v0;
+            p.n_chunks = uint32_t((p.n + chunk_syms - 1) / chunk_syms);
+            L.stripes.push_back(p);
+        }
+        L.out += 2 * n_values[t];
+        L.raw += 2 * n_values[t];
+    }
+}
+
+void plan_layout(const uint64_t *stripe_hist, LayerPlan &L) {
+    L.codelen.assign(256ull * L.n_tables, 0);
+    for (uint32_t tb = 0; tb < L.n_tables; ++tb) {
+        uint64_t cnt[256] = {};
+        for (size_t i = 0; i < L.stripes.size(); ++i)
+            if (L.stripes[i].table == tb)
+                for (int s = 0; s < 256; ++s) cnt[s] += stripe_hist[256 * i + s];
+        int depth[256];
+        huffman_depths(cnt, depth);
+        limit_depths(cnt, depth);
+        for (int s = 0; s < 256; ++s) L.codelen[256ull * tb + s] = uint8_t(depth[s]);
+    }
+    L.hdr = align_up(K3HUF_LAYER_HDR_BYTES + 256ull * L.n_tables + 32ull * L.n_tensors + 32ull * L.stripes.size(), 256);
+    uint64_t pos = L.hdr;
+    for (size_t i = 0; i < L.stripes.size(); ++i) {
+        PlanStripe &p = L.stripes[i];
+        const uint8_t *cl = &L.codelen[256ull * p.table];
+        uint64_t bits = 0;
+        for (int s = 0; s < 256; ++s) bits += stripe_hist[256 * i + s] * cl[s];
+        p.huff_bits = bits;
+        p.bits_offset = uint32_t(align_up(K3HUF_STRIPE_HDR_BYTES + index_bytes(p.n_chunks, L.chunk_syms, L.sub_syms), 16));
+        p.even_offset = uint32_t(p.bits_offset + align_up((bits + 7) / 8, 16) + kBitsSlack);
+        p.stripe_bytes = p.even_offset + align_up(p.n, 16);
+        pos = align_up(pos, 256);
+        p.blob_offset = pos;
+        pos += p.stripe_bytes;
+    }
+    L.total = pos;
+}
+
+void write_layer_header(const LayerPlan &L, uint8_t *blob) {
+    std::memset(blob, 0, L.hdr);
+    wr32(blob + 0, kLayerMagic);
+    wr16(blob + 4, K3HUF_FORMAT_VERSION);
+    wr16(blob + 6, K3HUF_MAXLEN);
+    wr32(blob + 8, L.chunk_syms);
+    wr32(blob + 12, L.n_tables);
+    wr32(blob + 16, L.n_tensors);
+    wr32(blob + 20, uint32_t(L.stripes.size()));
+    wr64(blob + 24, L.raw);
+    wr64(blob + 32, L.total);
+    wr32(blob + 40, K3HUF_STRIPE_VALUES);
+    wr32(blob + 44, uint32_t(L.hdr));
+    wr64(blob + 48, L.out);
+    wr32(blob + 56, L.sub_syms);
+    std::memcpy(blob + K3HUF_LAYER_HDR_BYTES, L.codelen.data(), L.codelen.size());
+    uint8_t *td = blob + K3HUF_LAYER_HDR_BYTES + 256ull * L.n_tables;
+    uint8_t *sd = td + 32ull * L.n_tensors;
+    uint32_t sid = 0;
+    for (uint32_t t = 0; t < L.n_tensors; ++t) {
+        const uint32_t ns = uint32_t((L.n_values[t] + K3HUF_STRIPE_VALUES - 1) / K3HUF_STRIPE_VALUES);
+        uint8_t *e = td + 32ull * t;
+        wr32(e + 0, L.shared_table ? 0u : t);
+        wr32(e + 4, sid);
+        wr32(e + 8, ns);
+        wr32(e + 12, 0);
+        wr64(e + 16, L.n_values[t]);
+        wr64(e + 24, L.tensor_out[t]);
+        sid += ns;
+    }
+    for (size_t i = 0; i < L.stripes.size(); ++i) {
+        const PlanStripe &p = L.stripes[i];
+        uint8_t *e = sd + 32 * i;
+        wr64(e + 0, p.blob_offset);
+        wr64(e + 8, p.stripe_bytes);
+        wr64(e + 16, p.out_offset);
+        wr32(e + 24, uint32_t(p.n));
+        wr32(e + 28, p.table);
+    }
+}
+
+void write_stripe_header(const PlanStripe &p, uint8_t *st) {
+    std::memset(st, 0, K3HUF_STRIPE_HDR_BYTES);
+    wr32(st + 0, kStripeMagic);
+    wr32(st + 4, p.table);
+    wr32(st + 8, uint32_t(p.n));
+    wr32(st + 12, p.n_chunks);
+    wr64(st + 16, p.huff_bits);
+    wr32(st + 24, p.bits_offset);
+    wr32(st + 28, p.even_offset);
+}
 
 // ---------------------------------------------------------------------------
 // header validation
@@ -271,14 +385,6 @@ namespace {
 
 constexpr uint64_t kSegValues = 1u << 20;   // values per encoder work item (a multiple of 2^12)
 
-struct StripePlan {
-    uint32_t tensor, table;
-    uint64_t v0, n;            // first value within the tensor, values
-    uint64_t blob_offset, stripe_bytes, out_offset;
-    uint64_t huff_bits;
-    uint32_t n_chunks, bits_offset, even_offset;
-    uint64_t hist[256];
-};
 
 // Append `len` code bits to a big-endian bit stream at bit offset `pos`.
 // Bytes fully owned by this writer are stored; the two partial edge bytes
@@ -328,27 +434,9 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
         if (!h_tensors[t] || n_values[t] == 0) return K3HUF_E_ARG;
     const int threads = n_threads > 0 ? n_threads : int(std::max(1u, std::thread::hardware_concurrency()));
     try {
-        const uint32_t n_tables = shared_table ? 1u : n_tensors;
-        // stripes
-        std::vector<StripePlan> sp;
-        std::vector<uint64_t> tensor_out(n_tensors);
-        uint64_t out = 0, raw = 0;
-        for (uint32_t t = 0; t < n_tensors; ++t) {
-            out = align_up(out, 256);
-            tensor_out[t] = out;
-            for (uint64_t v0 = 0; v0 < n_values[t]; v0 += K3HUF_STRIPE_VALUES) {
-                StripePlan p{};
-                p.tensor = t;
-                p.table = shared_table ? 0u : t;
-                p.v0 = v0;
-                p.n = std::min<uint64_t>(K3HUF_STRIPE_VALUES, n_values[t] - v0);
-                p.out_offset = out + 2 * v0;
-                p.n_chunks = uint32_t((p.n + chunk_syms - 1) / chunk_syms);
-                sp.push_back(p);
-            }
-            out += 2 * n_values[t];
-            raw += 2 * n_values[t];
-        }
+        LayerPlan L;
+        plan_stripes(n_tensors, n_values, chunk_syms, sub_syms, shared_table != 0, L);
+        std::vector<PlanStripe> &sp = L.stripes;
         // histograms, one work item per segment of a stripe
         struct Seg { uint32_t stripe; uint64_t a, b; };
         std::vector<Seg> segs;
@@ -358,7 +446,7 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
         std::vector<uint64_t> seg_hist(segs.size() * 256, 0);
         parallel_for(segs.size(), threads, [&](size_t i) {
             const Seg &g = segs[i];
-            const StripePlan &p = sp[g.stripe];
+            const PlanStripe &p = sp[g.stripe];
             const uint8_t *x = static_cast<const uint8_t *>(h_tensors[p.tensor]) + 2 * p.v0;
             uint64_t h[4][256] = {};
             uint64_t k = g.a;
@@ -372,96 +460,28 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
             uint64_t *dst = &seg_hist[i * 256];
             for (int s = 0; s < 256; ++s) dst[s] = h[0][s] + h[1][s] + h[2][s] + h[3][s];
         });
-        for (auto &p : sp) std::memset(p.hist, 0, sizeof p.hist);
+        std::vector<uint64_t> stripe_hist(sp.size() * 256, 0);
         for (size_t i = 0; i < segs.size(); ++i)
-            for (int s = 0; s < 256; ++s) sp[segs[i].stripe].hist[s] += seg_hist[i * 256 + s];
-        // code lengths per table
-        std::vector<uint8_t> codelen(256ull * n_tables, 0);
-        for (uint32_t tb = 0; tb < n_tables; ++tb) {
-            uint64_t cnt[256] = {};
-            for (auto &p : sp)
-                if (p.table == tb)
-                    for (int s = 0; s < 256; ++s) cnt[s] += p.hist[s];
-            int depth[256];
-            huffman_depths(cnt, depth);
-            limit_depths(cnt, depth);
-            for (int s = 0; s < 256; ++s) codelen[256ull * tb + s] = uint8_t(depth[s]);
-        }
-        // layout
-        const uint64_t hdr = align_up(K3HUF_LAYER_HDR_BYTES + 256ull * n_tables + 32ull * n_tensors + 32ull * sp.size(), 256);
-        uint64_t pos = hdr;
-        for (auto &p : sp) {
-            const uint8_t *cl = &codelen[256ull * p.table];
-            uint64_t bits = 0;
-            for (int s = 0; s < 256; ++s) bits += p.hist[s] * cl[s];
-            p.huff_bits = bits;
-            p.bits_offset = uint32_t(align_up(K3HUF_STRIPE_HDR_BYTES + index_bytes(p.n_chunks, chunk_syms, sub_syms), 16));
-            p.even_offset = uint32_t(p.bits_offset + align_up((bits + 7) / 8, 16) + kBitsSlack);
-            p.stripe_bytes = p.even_offset + align_up(p.n, 16);
-            pos = align_up(pos, 256);
-            p.blob_offset = pos;
-            pos += p.stripe_bytes;
-        }
+            for (int s = 0; s < 256; ++s) stripe_hist[256ull * segs[i].stripe + s] += seg_hist[i * 256 + s];
+        plan_layout(stripe_hist.data(), L);
+        const uint64_t hdr = L.hdr, pos = L.total;
+        const uint32_t n_tables = L.n_tables;
+        std::vector<uint8_t> &codelen = L.codelen;
         *blob_bytes = size_t(pos);
         if (!h_blob) return K3HUF_OK;
         if (blob_cap < pos) return K3HUF_E_ARG;
         uint8_t *blob = static_cast<uint8_t *>(h_blob);
 
-        // header, tables, directories
-        std::memset(blob, 0, hdr);
-        wr32(blob + 0, kLayerMagic);
-        wr16(blob + 4, K3HUF_FORMAT_VERSION);
-        wr16(blob + 6, K3HUF_MAXLEN);
-        wr32(blob + 8, chunk_syms);
-        wr32(blob + 12, n_tables);
-        wr32(blob + 16, n_tensors);
-        wr32(blob + 20, uint32_t(sp.size()));
-        wr64(blob + 24, raw);
-        wr64(blob + 32, pos);
-        wr32(blob + 40, K3HUF_STRIPE_VALUES);
-        wr32(blob + 44, uint32_t(hdr));
-        wr64(blob + 48, out);
-        wr32(blob + 56, sub_syms);
-        std::memcpy(blob + K3HUF_LAYER_HDR_BYTES, codelen.data(), codelen.size());
-        uint8_t *td = blob + K3HUF_LAYER_HDR_BYTES + 256ull * n_tables;
-        uint8_t *sd = td + 32ull * n_tensors;
-        {
-            uint32_t sid = 0;
-            for (uint32_t t = 0; t < n_tensors; ++t) {
-                const uint32_t ns = uint32_t((n_values[t] + K3HUF_STRIPE_VALUES - 1) / K3HUF_STRIPE_VALUES);
-                uint8_t *e = td + 32ull * t;
-                wr32(e + 0, shared_table ? 0u : t);
-                wr32(e + 4, sid);
-                wr32(e + 8, ns);
-                wr32(e + 12, 0);
-                wr64(e + 16, n_values[t]);
-                wr64(e + 24, tensor_out[t]);
-                sid += ns;
-            }
-        }
+        // header, tables, directories; zeroed gaps and stripes
+        write_layer_header(L, blob);
         for (size_t i = 0; i < sp.size(); ++i) {
-            const StripePlan &p = sp[i];
-            uint8_t *e = sd + 32 * i;
-            wr64(e + 0, p.blob_offset);
-            wr64(e + 8, p.stripe_bytes);
-            wr64(e + 16, p.out_offset);
-            wr32(e + 24, uint32_t(p.n));
-            wr32(e + 28, p.table);
-            // zero the gap before the stripe and the stripe itself
             const uint64_t prev_end = i ? sp[i - 1].blob_offset + sp[i - 1].stripe_bytes : hdr;
-            std::memset(blob + prev_end, 0, p.blob_offset - prev_end);
+            std::memset(blob + prev_end, 0, sp[i].blob_offset - prev_end);
         }
         parallel_for(sp.size(), threads, [&](size_t i) {
-            const StripePlan &p = sp[i];
+            const PlanStripe &p = sp[i];
             std::memset(blob + p.blob_offset, 0, p.stripe_bytes);
-            uint8_t *st = blob + p.blob_offset;
-            wr32(st + 0, kStripeMagic);
-            wr32(st + 4, p.table);
-            wr32(st + 8, uint32_t(p.n));
-            wr32(st + 12, p.n_chunks);
-            wr64(st + 16, p.huff_bits);
-            wr32(st + 24, p.bits_offset);
-            wr32(st + 28, p.even_offset);
+            write_stripe_header(p, blob + p.blob_offset);
         });
 
         // chunk bit offsets: bits per segment (segments hold whole chunks
@@ -477,7 +497,7 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
         for (size_t i = 0; i < sp.size(); ++i) chunk_bits[i].assign(sp[i].n_chunks, 0);
         parallel_for(segs.size(), threads, [&](size_t i) {
             const Seg &g = segs[i];
-            const StripePlan &p = sp[g.stripe];
+            const PlanStripe &p = sp[g.stripe];
             const uint8_t *cl = &codelen[256ull * p.table];
             const uint8_t *x = static_cast<const uint8_t *>(h_tensors[p.tensor]) + 2 * p.v0;
             uint8_t *sub = blob + p.blob_offset + K3HUF_STRIPE_HDR_BYTES + 4ull * p.n_chunks;
@@ -508,7 +528,7 @@ extern "C" int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tenso
         // bit packing and the raw low bytes, in parallel over segments
         parallel_for(segs.size(), threads, [&](size_t i) {
             const Seg &g = segs[i];
-            const StripePlan &p = sp[g.stripe];
+            const PlanStripe &p = sp[g.stripe];
             const uint8_t *cl = &codelen[256ull * p.table];
             const uint32_t *cd = &code[256ull * p.table];
             const uint8_t *x = static_cast<const uint8_t *>(h_tensors[p.tensor]) + 2 * p.v0;

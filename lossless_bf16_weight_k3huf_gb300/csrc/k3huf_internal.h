@@ -64,4 +64,42 @@ inline uint64_t index_bytes(uint64_t n_chunks, uint32_t chunk_syms, uint32_t sub
 // Record a CUDA error code for k3huf_last_cuda_error (thread-local).
 void set_cuda_error(int code);
 
+// --- code construction (host) ---------------------------------------------
+// Canonical longest-first codes of a length vector (0 = unused symbol).
+void canonical_codes(const uint8_t len[256], uint32_t code[256], uint32_t first[K3HUF_MAXLEN + 1],
+                     uint32_t count[K3HUF_MAXLEN + 1]);
+// Huffman code lengths of symbol counts, ties on (count, id).
+void huffman_depths(const uint64_t cnt[256], int depth[256]);
+// Cap the lengths at 12 bits (clamp, then lengthen the rarest shorter code
+// while the Kraft sum is over-full).
+void limit_depths(const uint64_t cnt[256], int depth[256]);
+
+// --- container layout, shared by the CPU and GPU encoders -------------------
+struct PlanStripe {
+    uint32_t tensor, table;
+    uint64_t v0, n;                // first value within the tensor, values
+    uint64_t blob_offset, stripe_bytes, out_offset, huff_bits;
+    uint32_t n_chunks, bits_offset, even_offset;
+};
+
+struct LayerPlan {
+    uint32_t n_tensors = 0, n_tables = 0, chunk_syms = 0, sub_syms = 0;
+    bool shared_table = false;
+    std::vector<uint64_t> n_values, tensor_out;
+    std::vector<PlanStripe> stripes;
+    std::vector<uint8_t> codelen;  // n_tables x 256
+    uint64_t raw = 0, out = 0, hdr = 0, total = 0;
+};
+
+// The layer's stripes (64 MiB of values each, per tensor, in order).
+void plan_stripes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms, uint32_t sub_syms,
+                  bool shared_table, LayerPlan &L);
+// Code lengths from per-stripe high-byte histograms (stripes x 256), then
+// every stripe's bit count, offsets and size.
+void plan_layout(const uint64_t *stripe_hist, LayerPlan &L);
+// Bytes [0, L.hdr): layer header, code tables, tensor and stripe directories.
+void write_layer_header(const LayerPlan &L, uint8_t *blob);
+// The 32-byte stripe header.
+void write_stripe_header(const PlanStripe &p, uint8_t *dst);
+
 }  // namespace k3huf
