@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="projection",
-                    choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring", "ring_file"])
+                    choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring", "ring_file", "encode"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--variant", type=int, default=0, help="codes per lookup: 0 default (2), 1, 2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -201,7 +201,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    name = "trunk_layer" if args.workload in ("ring", "ring_file") else args.workload
+    name = {"ring": "trunk_layer", "ring_file": "trunk_layer", "encode": "heavy_tail"}.get(args.workload, args.workload)
     tensors, blob = make_layer(name)
     info = oracle.layer_info(blob)
     out = np.zeros(info["out_bytes"], dtype=np.uint8)
@@ -275,6 +275,8 @@ def main():
         return bench_ring(args, rank, world, local, dev)
     if args.workload == "ring_file":
         return bench_ring_file(args, rank, world, local, dev)
+    if args.workload == "encode":
+        return bench_encode(args, rank, world, local, dev)
 
     tensors, blob = make_layer(args.workload, args.sub_syms)
     info = k3.layer_info(blob)
@@ -479,6 +481,80 @@ def bench_ring(args, rank, world, local, dev):
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_encode(args, rank, world, local, dev):
+    """GPU encoder on the heavy-tail tensor: the container built on the
+    device from a device-resident tensor (host wall time per call: the call
+    synchronises after its histogram pass and at the end).  The container is
+    checked byte for byte against the CPU encoder's (which the host tests
+    check against the oracle's)."""
+    import torch
+    import lossless_bf16_weight_k3huf_gb300 as k3
+    x = workloads.heavy_tail()
+    n = x.size
+    raw = 2 * n
+    t0 = time.perf_counter()
+    ref = k3.encode_layer([x])
+    cpu_enc_s = time.perf_counter() - t0
+    h_x = torch.from_numpy(x.view(np.int16)).pin_memory()
+    d_x = h_x.to(dev)
+    scratch = torch.empty(k3.encode_scratch_bytes([n]), dtype=torch.uint8, device=dev)
+    blob = k3.encode_layer_gpu([d_x], scratch=scratch)
+    if not np.array_equal(blob.cpu().numpy(), ref):
+        raise SystemExit("GPU container differs from the CPU encoder's")
+    for _ in range(max(0, args.warmup - 1)):
+        k3.encode_layer_gpu([d_x], scratch=scratch)
+    torch.cuda.synchronize()
+    times = []
+    with ClockSampler(dev.index) as clk:
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            k3.encode_layer_gpu([d_x], scratch=scratch)
+            torch.cuda.synchronize()
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    # end to end: input from pinned host memory, container back to pinned host memory
+    h_blob = torch.empty(blob.numel(), dtype=torch.uint8).pin_memory()
+    e2e = []
+    for _ in range(max(3, args.steps // 4)):
+        t0 = time.perf_counter()
+        d_in = h_x.to(dev, non_blocking=True)
+        b = k3.encode_layer_gpu([d_in], scratch=scratch)
+        h_blob.copy_(b, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e.append(time.perf_counter() - t0)
+    te = sum(e2e) / len(e2e)
+    peak, peak_kind = measured_peak()
+    alg = raw + blob.numel()                      # one read of the input, one write of the container
+    line = {
+        "metric": "encoded bf16 GB/s on 1 GB300 (GPU encoder, container identical to the CPU encoder's)",
+        "value": round(raw / t / 1e9, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {**describe("encode"), "values": n, "raw_bytes": raw, "blob_bytes": int(blob.numel()),
+                   "compression_ratio": round(raw / blob.numel(), 4),
+                   "passes": "histogram, bit counts, pack + low bytes (3 reads of the input), zeroed container",
+                   "cpu_encoder_gbs": round(raw / cpu_enc_s / 1e9, 3),
+                   "cpu_encoder_threads": os.cpu_count(), "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(alg / t / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(alg / t / 1e9 / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": None, "algorithmic_bytes_per_call": alg},
+        "e2e": {"value": round(raw / te / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": raw,
+                "d2h_bytes_per_step": int(blob.numel())},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        m = 1 << 25
+        oracle.encode_layer([x[:m]])
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(2 * m / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"first {m} values (one stripe, {2 * m >> 20} MiB) encoded by the oracle in {dt:.1f} s, one thread"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -181,6 +181,30 @@ int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tensors, const u
                        uint32_t chunk_syms, uint32_t sub_syms, int shared_table, int n_threads,
                        void *h_blob, size_t blob_cap, size_t *blob_bytes);
 
+/* GPU encoder: the same container as k3huf_encode_layer (byte for byte),
+ * built from bf16 tensors already in device memory.  The article "Kimi K3
+ * 纯 CPU 推理中的无损 Trunk 压缩" (section 已实现的部分) packs offline:
+ * high-byte histogram, 12-bit-capped Huffman lengths, canonical
+ * longest-first codes, MSB-first bit packing per stripe, low bytes raw.
+ * Here the passes over the values (histogram, bit counts, packing, low-byte
+ * copy) run on the GPU; code lengths and the layout are decided on the host
+ * with the CPU encoder's own functions between them.
+ *  d_tensors[t]: device, 16-byte aligned, n_values[t] (>= 1) bf16 values;
+ *  chunk_syms, sub_syms, shared_table: as for k3huf_encode_layer;
+ *  d_scratch: device, 256-byte aligned, scratch_bytes >=
+ *    k3huf_encode_scratch_bytes(...) (contents need not be initialised);
+ *  d_blob: device, 256-byte aligned, blob_cap bytes; with d_blob NULL only
+ *    *blob_bytes is set (the histogram pass still runs).
+ * Synchronises `stream` twice (after the histograms and at the end) and
+ * returns when the container is complete.  K3HUF_E_ARG on a bad argument
+ * or a short buffer, K3HUF_E_FORMAT if the packed bits disagree with the
+ * planned layout (an internal check), K3HUF_E_CUDA on a CUDA error. */
+int k3huf_encode_scratch_bytes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms,
+                               uint32_t sub_syms, int shared_table, size_t *scratch_bytes);
+int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
+                           uint32_t chunk_syms, uint32_t sub_syms, int shared_table, void *d_scratch,
+                           size_t scratch_bytes, void *d_blob, size_t blob_cap, size_t *blob_bytes, void *stream);
+
 /* Streaming ring: layers held in pinned host memory are copied to device
  * slots with cudaMemcpyAsync on a copy stream while the previous layer is
  * decoded on a compute stream, double buffered (the article's trunk ring,

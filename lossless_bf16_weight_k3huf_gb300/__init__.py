@@ -29,6 +29,7 @@ EXPORTS = [
     "k3huf_set_decoder_variant", "k3huf_encode_layer", "k3huf_ring_create", "k3huf_ring_run",
     "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
     "k3huf_feed_read", "k3huf_feed_close", "k3huf_ring_create_staged", "k3huf_ring_run_file",
+    "k3huf_encode_scratch_bytes", "k3huf_encode_layer_gpu",
 ]
 FILE_ALIGN = 4096
 
@@ -97,6 +98,11 @@ def _lib():
             L.k3huf_ring_run.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(_vp), ctypes.POINTER(_sz),
                                          ctypes.POINTER(_vp), ctypes.POINTER(_sz), _vp, ctypes.POINTER(RingStats)]
             L.k3huf_ring_destroy.argtypes = [_vp]
+            L.k3huf_encode_scratch_bytes.argtypes = [ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint64), ctypes.c_uint32,
+                                                     ctypes.c_uint32, ctypes.c_int, ctypes.POINTER(_sz)]
+            L.k3huf_encode_layer_gpu.argtypes = [ctypes.c_uint32, ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint64),
+                                                 ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, _vp, _sz, _vp, _sz,
+                                                 ctypes.POINTER(_sz), _vp]
             L.k3huf_feed_open.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(_vp)]
             L.k3huf_feed_direct.argtypes = [_vp]
             L.k3huf_feed_read.argtypes = [_vp, ctypes.c_uint64, _sz, _vp, _sz]
@@ -204,6 +210,42 @@ def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, th
     _check(L.k3huf_encode_layer(n, ptrs, nv, chunk_syms, sub_syms, int(shared_table), threads, out.ctypes.data,
                                 out.size, ctypes.byref(size)), "k3huf_encode_layer")
     return out[: size.value]
+
+
+def encode_scratch_bytes(n_values, chunk_syms: int = 4096, sub_syms: int = 256, shared_table: bool = False) -> int:
+    """Device scratch bytes that encode_layer_gpu needs for tensors of these sizes."""
+    n = len(n_values)
+    nv = (ctypes.c_uint64 * n)(*[int(v) for v in n_values])
+    out = _sz(0)
+    _check(_lib().k3huf_encode_scratch_bytes(n, nv, chunk_syms, sub_syms, int(shared_table), ctypes.byref(out)),
+           "k3huf_encode_scratch_bytes")
+    return int(out.value)
+
+
+def encode_layer_gpu(tensors, chunk_syms: int = 4096, sub_syms: int = 256, shared_table: bool = False,
+                     stream=None, scratch=None):
+    """Container of a layer of bf16 CUDA tensors (16-byte aligned), built on
+    the GPU; returns a CUDA uint8 tensor.  ``scratch`` (a CUDA tensor) is
+    allocated here when not given."""
+    import torch
+    n = len(tensors)
+    sizes = [int(t.numel()) for t in tensors]
+    dev = tensors[0].device
+    if scratch is None:
+        scratch = torch.empty(encode_scratch_bytes(sizes, chunk_syms, sub_syms, shared_table), dtype=torch.uint8,
+                              device=dev)
+    ptrs = (_vp * n)(*[int(t.data_ptr()) for t in tensors])
+    nv = (ctypes.c_uint64 * n)(*sizes)
+    size = _sz(0)
+    L = _lib()
+    s = _stream(stream)
+    _check(L.k3huf_encode_layer_gpu(n, ptrs, nv, chunk_syms, sub_syms, int(shared_table), _dptr(scratch),
+                                    _nbytes(scratch), None, 0, ctypes.byref(size), s), "k3huf_encode_layer_gpu")
+    blob = torch.empty(size.value, dtype=torch.uint8, device=dev)
+    _check(L.k3huf_encode_layer_gpu(n, ptrs, nv, chunk_syms, sub_syms, int(shared_table), _dptr(scratch),
+                                    _nbytes(scratch), _dptr(blob), _nbytes(blob), ctypes.byref(size), s),
+           "k3huf_encode_layer_gpu")
+    return blob
 
 
 def decode_layer(hdr, d_layer, d_out, d_status, stream=None, layer_bytes: int | None = None,

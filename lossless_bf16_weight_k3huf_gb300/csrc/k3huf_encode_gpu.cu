@@ -1,0 +1,386 @@
+// GPU encoder for k3_huf containers (pack time, sm_103a).
+//
+// The article "Kimi K3 纯 CPU 推理中的无损 Trunk 压缩：一次被解码速度判死刑的
+// Huffman 压缩实验" (section 已实现的部分) packs the trunk offline: a
+// histogram of the odd (high) bytes, Huffman code lengths capped at 12 bits,
+// canonical longest-first codes, the high bytes' codes packed MSB-first per
+// stripe, the even (low) bytes stored raw.  Here the passes over the values
+// run on the GPU, and the small decisions between them on the host:
+//  1. per-stripe histograms of the high bytes (per-warp shared-memory bins);
+//  2. host: code lengths, codes and the container layout, with the same
+//     functions as the CPU encoder (k3huf_host.cpp), so both write the same
+//     bytes; the blob is zeroed and the header copied in;
+//  3. per-sub-stream bit counts (one thread per sub-stream);
+//  4. per stripe, one CTA scans them into the chunk index, the sub-stream
+//     index and each sub-stream's first bit, writes the stripe header and
+//     checks the total against the planned bit count;
+//  5. one thread per sub-stream packs its codes MSB-first into 32-bit words
+//     (OR-ed atomically: a sub-stream shares its edge words with its
+//     neighbours) and copies its low bytes into the even plane.
+// Scratch (caller-owned device memory, k3huf_encode_scratch_bytes) holds
+// the stripe descriptors, histograms, code tables, bit counts and starts.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "k3huf_internal.h"
+
+namespace k3huf {
+namespace {
+
+struct EncStripe {
+    const uint8_t *src;    // device: the stripe's first value (tensor + 2 * v0)
+    uint8_t *dst;          // device: the stripe's first byte in the blob
+    uint64_t huff_bits;    // planned bits of the stripe's stream
+    uint32_t n, n_chunks;
+    uint32_t table, bits_offset;
+    uint32_t even_offset, sub_begin;   // first sub-stream of the stripe in the per-sub-stream arrays
+};
+
+struct EncParams {
+    const EncStripe *stripes;
+    const uint32_t *codes;     // n_tables x 256: (code << 4) | length
+    uint32_t *counts;          // n_stripes x 256
+    uint32_t *sub_bits;        // bits of every sub-stream
+    uint32_t *sub_start;       // first bit of every sub-stream within its stripe's stream
+    uint32_t *flag;            // nonzero: the packed bits disagree with the plan
+    uint32_t chunk_syms, sub_syms, S;
+};
+
+struct ScratchLayout {
+    size_t stripes, counts, codes, sub_bits, sub_start, flag, total;
+};
+
+constexpr int kHistThreads = 256;
+constexpr int kScanThreads = 1024;
+constexpr int kPackThreads = 256;
+
+ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_subs) {
+    ScratchLayout s{};
+    size_t at = 0;
+    auto take = [&](size_t bytes) {
+        const size_t here = at;
+        at = size_t(align_up(at + bytes, 256));
+        return here;
+    };
+    s.stripes = take(n_stripes * sizeof(EncStripe));
+    s.counts = take(n_stripes * 256 * sizeof(uint32_t));
+    s.codes = take(n_tables * 256 * sizeof(uint32_t));
+    s.sub_bits = take(size_t(n_subs) * sizeof(uint32_t));
+    s.sub_start = take(size_t(n_subs) * sizeof(uint32_t));
+    s.flag = take(sizeof(uint32_t));
+    s.total = at;
+    return s;
+}
+
+uint64_t count_subs(const LayerPlan &L) {
+    uint64_t n = 0;
+    const uint32_t S = L.chunk_syms / L.sub_syms;
+    for (const auto &p : L.stripes) n += uint64_t(p.n_chunks) * S;
+    return n;
+}
+
+// 1. histogram of the high bytes of one stripe's values, per CTA a slice
+__global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
+    __shared__ uint32_t h[kHistThreads / 32][256];
+    const EncStripe &T = P.stripes[blockIdx.y];
+    const int tid = threadIdx.x;
+    for (int i = tid; i < (kHistThreads / 32) * 256; i += kHistThreads) (&h[0][0])[i] = 0;
+    __syncthreads();
+    uint32_t *hw = h[tid >> 5];
+    const uint64_t per = ((uint64_t(T.n) + gridDim.x - 1) / gridDim.x + 7) / 8 * 8;
+    const uint64_t a = min(uint64_t(T.n), uint64_t(blockIdx.x) * per), b = min(uint64_t(T.n), a + per);
+    const uint64_t vend = a + (b - a) / 8 * 8;
+    for (uint64_t k = a + uint64_t(tid) * 8; k < vend; k += uint64_t(kHistThreads) * 8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(T.src + 2 * k);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            atomicAdd(&hw[(w[i] >> 8) & 0xFFu], 1u);
+            atomicAdd(&hw[w[i] >> 24], 1u);
+        }
+    }
+    for (uint64_t k = vend + uint64_t(tid); k < b; k += kHistThreads) atomicAdd(&hw[T.src[2 * k + 1]], 1u);
+    __syncthreads();
+    for (int s = tid; s < 256; s += kHistThreads) {
+        uint32_t c = 0;
+        for (int w = 0; w < kHistThreads / 32; ++w) c += h[w][s];
+        if (c) atomicAdd(&P.counts[size_t(blockIdx.y) * 256 + s], c);
+    }
+}
+
+// values [a, b) of sub-stream j (k-th of chunk c) of a stripe
+__device__ __forceinline__ void sub_range(const EncParams &P, const EncStripe &T, uint32_t j, uint64_t &a, uint64_t &b) {
+    const uint32_t c = j / P.S, k = j - c * P.S;
+    const uint64_t c0 = uint64_t(c) * P.chunk_syms;
+    const uint64_t len_c = min(uint64_t(P.chunk_syms), uint64_t(T.n) - c0);
+    a = c0 + min(uint64_t(k) * P.sub_syms, len_c);
+    b = c0 + min(uint64_t(k + 1) * P.sub_syms, len_c);
+}
+
+// 3. bits of every sub-stream
+__global__ void __launch_bounds__(kPackThreads) sub_bits_kernel(EncParams P) {
+    __shared__ uint8_t len[256];
+    const EncStripe &T = P.stripes[blockIdx.y];
+    for (int s = threadIdx.x; s < 256; s += kPackThreads) len[s] = uint8_t(P.codes[size_t(T.table) * 256 + s] & 15u);
+    __syncthreads();
+    const uint32_t nsub = T.n_chunks * P.S;
+    for (uint32_t j = blockIdx.x * kPackThreads + threadIdx.x; j < nsub; j += gridDim.x * kPackThreads) {
+        uint64_t a, b;
+        sub_range(P, T, j, a, b);
+        uint32_t bits = 0;
+        uint64_t v = a;
+        if ((a & 7) == 0)
+            for (; v + 8 <= b; v += 8) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(T.src + 2 * v);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) bits += len[(w[i] >> 8) & 0xFFu] + len[w[i] >> 24];
+            }
+        for (; v < b; ++v) bits += len[T.src[2 * v + 1]];
+        P.sub_bits[T.sub_begin + j] = bits;
+    }
+}
+
+// 4. one CTA per stripe: chunk index, sub-stream index, sub-stream starts,
+//    stripe header, and the check of the total against the plan
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(EncParams P) {
+    __shared__ uint64_t s_warp[kScanThreads / 32];
+    const EncStripe &T = P.stripes[blockIdx.x];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t nch = T.n_chunks, S = P.S;
+    const uint32_t per = (nch + kScanThreads - 1) / kScanThreads;
+    const uint32_t c_lo = min(nch, uint32_t(tid) * per), c_hi = min(nch, c_lo + per);
+    const uint32_t *bits = P.sub_bits + T.sub_begin;
+    uint64_t sum = 0;
+    for (uint32_t c = c_lo; c < c_hi; ++c)
+        for (uint32_t k = 0; k < S; ++k) sum += bits[size_t(c) * S + k];
+    // exclusive scan of the threads' sums
+    uint64_t incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint64_t v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    uint64_t base = 0;
+    for (int w = 0; w < warp; ++w) base += s_warp[w];
+    uint64_t off = base + incl - sum;
+    uint32_t *chunk_idx = reinterpret_cast<uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
+    uint16_t *sub_idx = reinterpret_cast<uint16_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES + 4ull * nch);
+    for (uint32_t c = c_lo; c < c_hi; ++c) {
+        chunk_idx[c] = uint32_t(off);
+        uint32_t rel = 0;
+        for (uint32_t k = 0; k < S; ++k) {
+            if (k > 0) sub_idx[size_t(c) * (S - 1) + k - 1] = uint16_t(rel);
+            P.sub_start[T.sub_begin + size_t(c) * S + k] = uint32_t(off) + rel;
+            rel += bits[size_t(c) * S + k];
+        }
+        off += rel;
+    }
+    if (c_hi == nch && c_lo < c_hi && off != T.huff_bits) atomicOr(P.flag, 1u);
+    if (tid == 0) {
+        uint32_t *h = reinterpret_cast<uint32_t *>(T.dst);
+        h[0] = kStripeMagic;
+        h[1] = T.table;
+        h[2] = T.n;
+        h[3] = nch;
+        h[4] = uint32_t(T.huff_bits);
+        h[5] = uint32_t(T.huff_bits >> 32);
+        h[6] = T.bits_offset;
+        h[7] = T.even_offset;
+    }
+}
+
+// 5. pack one sub-stream's codes MSB-first and copy its low bytes
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(EncParams P) {
+    __shared__ uint32_t code[256];
+    const EncStripe &T = P.stripes[blockIdx.y];
+    for (int s = threadIdx.x; s < 256; s += kPackThreads) code[s] = P.codes[size_t(T.table) * 256 + s];
+    __syncthreads();
+    uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
+    const uint32_t n_words = (T.even_offset - T.bits_offset) / 4;   // the stream region, padding included
+    uint8_t *even = T.dst + T.even_offset;
+    const uint32_t nsub = T.n_chunks * P.S;
+    for (uint32_t j = blockIdx.x * kPackThreads + threadIdx.x; j < nsub; j += gridDim.x * kPackThreads) {
+        uint64_t a, b;
+        sub_range(P, T, j, a, b);
+        const uint32_t pos = P.sub_start[T.sub_begin + j];
+        uint32_t w = pos >> 5, nb = pos & 31u;   // the word's leading bits belong to the previous sub-stream
+        uint64_t acc = 0;
+        auto put = [&](uint32_t hb) {
+            const uint32_t e = code[hb], l = e & 15u;
+            acc = (acc << l) | (e >> 4);
+            nb += l;
+            if (nb >= 32) {
+                nb -= 32;
+                const uint32_t word = uint32_t(acc >> nb);
+                if (word && w < n_words) atomicOr(&words[w], __byte_perm(word, 0, 0x0123));
+                ++w;
+                acc &= (uint64_t(1) << nb) - 1;
+            }
+        };
+        uint64_t v = a;
+        if ((a & 7) == 0)
+            for (; v + 8 <= b; v += 8) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(T.src + 2 * v);
+                const uint32_t q[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    put((q[i] >> 8) & 0xFFu);
+                    put(q[i] >> 24);
+                }
+                // low bytes of the 8 values, in order
+                const uint32_t lo0 = __byte_perm(q[0], q[1], 0x6420), lo1 = __byte_perm(q[2], q[3], 0x6420);
+                *reinterpret_cast<uint2 *>(even + v) = make_uint2(lo0, lo1);
+            }
+        for (; v < b; ++v) {
+            put(T.src[2 * v + 1]);
+            even[v] = T.src[2 * v];
+        }
+        if (nb > 0) {
+            const uint32_t word = uint32_t(acc << (32 - nb));
+            if (word && w < n_words) atomicOr(&words[w], __byte_perm(word, 0, 0x0123));
+        }
+    }
+}
+
+int cuda_fail(cudaError_t e) {
+    set_cuda_error(int(e));
+    return K3HUF_E_CUDA;
+}
+
+int check_inputs(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms) {
+    if (n_tensors == 0 || !n_values || chunk_syms == 0) return K3HUF_E_ARG;
+    for (uint32_t t = 0; t < n_tensors; ++t)
+        if (n_values[t] == 0) return K3HUF_E_ARG;
+    return K3HUF_OK;
+}
+
+}  // namespace
+}  // namespace k3huf
+
+using namespace k3huf;
+
+extern "C" int k3huf_encode_scratch_bytes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms,
+                                          uint32_t sub_syms, int shared_table, size_t *scratch_bytes) {
+    int rc = check_inputs(n_tensors, n_values, chunk_syms);
+    if (rc) return rc;
+    if (!scratch_bytes) return K3HUF_E_ARG;
+    try {
+        LayerPlan L;
+        plan_stripes(n_tensors, n_values, chunk_syms, effective_sub_syms(chunk_syms, sub_syms), shared_table != 0, L);
+        *scratch_bytes = scratch_layout(L.stripes.size(), L.n_tables, count_subs(L)).total;
+        return K3HUF_OK;
+    } catch (const std::bad_alloc &) {
+        return K3HUF_E_NOMEM;
+    }
+}
+
+extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
+                                      uint32_t chunk_syms, uint32_t sub_syms_req, int shared_table,
+                                      void *d_scratch, size_t scratch_bytes, void *d_blob, size_t blob_cap,
+                                      size_t *blob_bytes, void *stream) {
+    int rc = check_inputs(n_tensors, n_values, chunk_syms);
+    if (rc) return rc;
+    if (!d_tensors || !d_scratch || !blob_bytes || (reinterpret_cast<uintptr_t>(d_scratch) & 255u)) return K3HUF_E_ARG;
+    for (uint32_t t = 0; t < n_tensors; ++t)
+        if (!d_tensors[t] || (reinterpret_cast<uintptr_t>(d_tensors[t]) & 15u)) return K3HUF_E_ARG;
+    if (d_blob && (reinterpret_cast<uintptr_t>(d_blob) & 255u)) return K3HUF_E_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    try {
+        const uint32_t sub_syms = effective_sub_syms(chunk_syms, sub_syms_req);
+        LayerPlan L;
+        plan_stripes(n_tensors, n_values, chunk_syms, sub_syms, shared_table != 0, L);
+        const size_t ns = L.stripes.size();
+        const uint64_t n_subs = count_subs(L);
+        if (ns > 65535 || n_subs > 0xFFFFFFFFull) return K3HUF_E_ARG;
+        const ScratchLayout SL = scratch_layout(ns, L.n_tables, n_subs);
+        if (scratch_bytes < SL.total) return K3HUF_E_ARG;
+        uint8_t *scr = static_cast<uint8_t *>(d_scratch);
+        EncParams P{};
+        P.stripes = reinterpret_cast<const EncStripe *>(scr + SL.stripes);
+        P.counts = reinterpret_cast<uint32_t *>(scr + SL.counts);
+        P.codes = reinterpret_cast<const uint32_t *>(scr + SL.codes);
+        P.sub_bits = reinterpret_cast<uint32_t *>(scr + SL.sub_bits);
+        P.sub_start = reinterpret_cast<uint32_t *>(scr + SL.sub_start);
+        P.flag = reinterpret_cast<uint32_t *>(scr + SL.flag);
+        P.chunk_syms = chunk_syms;
+        P.sub_syms = sub_syms;
+        P.S = chunk_syms / sub_syms;
+
+        std::vector<EncStripe> desc(ns);
+        uint32_t max_n = 0, max_sub = 0;
+        uint64_t sub_begin = 0;
+        for (size_t i = 0; i < ns; ++i) {
+            const PlanStripe &p = L.stripes[i];
+            EncStripe &d = desc[i];
+            d.src = static_cast<const uint8_t *>(d_tensors[p.tensor]) + 2 * p.v0;
+            d.n = uint32_t(p.n);
+            d.n_chunks = p.n_chunks;
+            d.table = p.table;
+            d.sub_begin = uint32_t(sub_begin);
+            sub_begin += uint64_t(p.n_chunks) * P.S;
+            max_n = std::max(max_n, d.n);
+            max_sub = std::max(max_sub, p.n_chunks * P.S);
+        }
+        // 1. histograms
+        cudaError_t e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.counts, 0, ns * 256 * sizeof(uint32_t), st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const uint32_t gx = std::min<uint32_t>(512, std::max<uint32_t>(1, (max_n + 65535) / 65536));
+        hist_kernel<<<dim3(gx, uint32_t(ns)), kHistThreads, 0, st>>>(P);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        std::vector<uint32_t> counts(ns * 256);
+        e = cudaMemcpyAsync(counts.data(), scr + SL.counts, counts.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        // 2. code lengths, codes and layout on the host
+        std::vector<uint64_t> hist(counts.begin(), counts.end());
+        plan_layout(hist.data(), L);
+        *blob_bytes = size_t(L.total);
+        if (!d_blob) return K3HUF_OK;
+        if (blob_cap < L.total) return K3HUF_E_ARG;
+        std::vector<uint32_t> codes(size_t(L.n_tables) * 256);
+        for (uint32_t tb = 0; tb < L.n_tables; ++tb) {
+            uint32_t code[256], first[K3HUF_MAXLEN + 1], count[K3HUF_MAXLEN + 1];
+            const uint8_t *cl = &L.codelen[256ull * tb];
+            canonical_codes(cl, code, first, count);
+            for (int s = 0; s < 256; ++s) codes[256ull * tb + s] = (code[s] << 4) | cl[s];
+        }
+        uint8_t *blob = static_cast<uint8_t *>(d_blob);
+        for (size_t i = 0; i < ns; ++i) {
+            const PlanStripe &p = L.stripes[i];
+            desc[i].dst = blob + p.blob_offset;
+            desc[i].huff_bits = p.huff_bits;
+            desc[i].bits_offset = p.bits_offset;
+            desc[i].even_offset = p.even_offset;
+        }
+        std::vector<uint8_t> head(size_t(L.hdr));
+        write_layer_header(L, head.data());
+        e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(scr + SL.codes, codes.data(), codes.size() * sizeof(uint32_t), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.flag, 0, sizeof(uint32_t), st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(blob, 0, size_t(L.total), st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(blob, head.data(), head.size(), cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        // 3-5. bit counts, indexes, packing
+        const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_sub + kPackThreads - 1) / kPackThreads));
+        sub_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+        scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
+        pack_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        uint32_t flag = 0;
+        e = cudaMemcpyAsync(&flag, scr + SL.flag, sizeof flag, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return flag ? K3HUF_E_FORMAT : K3HUF_OK;
+    } catch (const std::bad_alloc &) {
+        return K3HUF_E_NOMEM;
+    }
+}

@@ -1,0 +1,97 @@
+"""GPU encoder parity: the container built on the GPU from device tensors
+equals the oracle's container byte for byte (integer work: the bar is
+bit-exact), over the same cases as the CPU encoder's tests, and decodes back
+to the input on the GPU."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+k3 = pytest.importorskip("lossless_bf16_weight_k3huf_gb300")
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    k3._build.build()
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x).reshape(-1).view(np.int16)).cuda()
+
+
+def gpu_blob(ts, **kw):
+    blob = k3.encode_layer_gpu([dev(x) for x in ts], **kw)
+    torch.cuda.synchronize()
+    return blob.cpu().numpy()
+
+
+CASES = {
+    "tiny": lambda: [workloads.tiny()],
+    "n1": lambda: [workloads.normal_tensor((1,), 0.02, 1)],
+    "n7": lambda: [workloads.normal_tensor((7,), 0.02, 5)],
+    "n4095": lambda: [workloads.normal_tensor((4095,), 0.02, 2)],
+    "n4097": lambda: [workloads.normal_tensor((4097,), 0.02, 3)],
+    "n100003": lambda: [workloads.normal_tensor((100_003,), 0.02, 4)],
+    "single": lambda: [workloads.single_symbol(30_001)],
+    "two": lambda: [workloads.two_symbol(30_001)],
+    "uniform": lambda: [workloads.uniform_bytes(300_000)],
+    "heavy": lambda: [workloads.heavy_tail(n=1 << 21)],
+    "multi": lambda: [workloads.normal_tensor((64, 96), 0.1, 3, 0), workloads.normal_tensor((5,), 0.3, 3, 1),
+                      workloads.normal_tensor((96, 640), 0.04, 3, 2)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_gpu_encoder_matches_oracle(name):
+    ts = CASES[name]()
+    assert np.array_equal(gpu_blob(ts), oracle.encode_layer(ts))
+
+
+@pytest.mark.parametrize("chunk_syms,sub_syms", [(1, 256), (7, 256), (1000, 200), (4096, 0), (4096, 512),
+                                                (4096, 8), (65536, 256), (1 << 21, 256), (5000, 1000), (64, 16)])
+def test_gpu_encoder_chunk_sizes(chunk_syms, sub_syms):
+    x = workloads.normal_tensor((300_001,), 0.05, 9)
+    assert np.array_equal(gpu_blob([x], chunk_syms=chunk_syms, sub_syms=sub_syms),
+                          oracle.encode_layer([x], chunk_syms=chunk_syms, sub_syms=sub_syms))
+
+
+def test_gpu_encoder_shared_table():
+    ts = CASES["multi"]()
+    assert np.array_equal(gpu_blob(ts, shared_table=True), oracle.encode_layer(ts, shared_table=True))
+
+
+def test_gpu_encoder_multi_stripe_and_many_tensors():
+    n = (1 << 25) + 12_345
+    x = np.tile(workloads.tiny(), n // (1 << 21) + 1)[:n]
+    assert np.array_equal(gpu_blob([x]), oracle.encode_layer([x]))
+    ts = [workloads.normal_tensor((4096 + 17 * i,), 0.02, 500 + i) for i in range(70)]
+    assert np.array_equal(gpu_blob(ts), oracle.encode_layer(ts))
+
+
+def test_gpu_encode_then_gpu_decode():
+    x = workloads.projection(rows=512, cols=16384)
+    d = dev(x)
+    blob = k3.encode_layer_gpu([d])
+    info = k3.layer_info(blob.cpu().numpy())
+    out = torch.empty(info["out_bytes"], dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3.decode_layer(blob[: info["hdr_bytes"]].cpu().numpy(), blob, out, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(out[: 2 * x.size].view(torch.int16), d)
+
+
+def test_gpu_encoder_scratch_reuse_needs_no_clearing():
+    """The scratch is reused uninitialised between calls."""
+    a, b = workloads.normal_tensor((50_000,), 0.02, 1), workloads.heavy_tail(n=1 << 18)
+    need = max(k3.encode_scratch_bytes([a.size]), k3.encode_scratch_bytes([b.size]))
+    scratch = torch.full((need,), 0xA5, dtype=torch.uint8, device="cuda")
+    for x in (a, b, a):
+        got = k3.encode_layer_gpu([dev(x)], scratch=scratch)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy(), oracle.encode_layer([x]))

@@ -224,3 +224,36 @@ def test_decode_argument_checks_need_no_device():
     assert st == k3.E_EMPTY
     assert L.k3huf_set_decoder_variant(3) == k3.E_ARG
     assert L.k3huf_set_decoder_variant(-1) == k3.E_ARG
+
+
+# --- GPU encoder: host-side size query and argument checks (no CUDA call) --------
+
+def test_encode_scratch_bytes():
+    small = k3.encode_scratch_bytes([4096])
+    big = k3.encode_scratch_bytes([1 << 26])
+    assert 0 < small < big
+    # per sub-stream: two u32 words; 2^26 values in 256-value sub-streams
+    assert big >= 2 * 4 * (1 << 26) // 256
+    assert k3.encode_scratch_bytes([1 << 26], sub_syms=512) < big
+    with pytest.raises(k3.K3HufError) as e:
+        k3.encode_scratch_bytes([0])
+    assert e.value.code == k3.E_ARG
+
+
+def test_encode_gpu_argument_checks_need_no_device():
+    """Misaligned pointers and short scratch are refused before any CUDA call."""
+    L = k3._lib()
+    n = 1000
+    nv = (ctypes.c_uint64 * 1)(n)
+    need = k3.encode_scratch_bytes([n])
+    size = ctypes.c_size_t(0)
+
+    def call(tensor, scratch, scratch_bytes, blob=None):
+        ptrs = (ctypes.c_void_p * 1)(tensor)
+        return L.k3huf_encode_layer_gpu(1, ptrs, nv, 4096, 256, 0, scratch, scratch_bytes, blob, 0,
+                                        ctypes.byref(size), None)
+    assert call(1 << 20, (1 << 21) + 8, need) == k3.E_ARG          # scratch not 256-byte aligned
+    assert call((1 << 20) + 2, 1 << 21, need) == k3.E_ARG          # tensor not 16-byte aligned
+    assert call(1 << 20, 1 << 21, need - 1) == k3.E_ARG            # scratch too small
+    assert call(1 << 20, 1 << 21, need, (1 << 22) + 16) == k3.E_ARG  # blob not 256-byte aligned
+    assert call(None, 1 << 21, need) == k3.E_ARG

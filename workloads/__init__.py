@@ -41,6 +41,7 @@ WORKLOADS = {
     "trunk_layer": "one trunk layer of 9 tensors N(0, 1/sqrt(fan_in)), one code table each, seed 3",
     "ring": "14 trunk layers (seeds 10..23) streamed from pinned host memory",
     "ring_file": "trunk layers (seeds 10..) read from a container file (O_DIRECT where allowed) into the pinned ring",
+    "encode": "GPU encoder: the heavy-tail 1 GiB bf16 tensor (seed 2) packed into a container on the device",
 }
 
 _THREADS = max(1, min(16, os.cpu_count() or 1))
