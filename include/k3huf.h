@@ -205,6 +205,25 @@ int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, con
                            uint32_t chunk_syms, uint32_t sub_syms, int shared_table, void *d_scratch,
                            size_t scratch_bytes, void *d_blob, size_t blob_cap, size_t *blob_bytes, void *stream);
 
+/* The GPU encoder without a scratch argument, for callers that may not
+ * allocate device memory themselves: for example a plugin or custom operator
+ * whose host framework hands it its inputs and outputs and owns the rest of
+ * the GPU's memory, where a cudaMalloc of its own could fail or synchronise
+ * the device in the middle of the framework's work.  The pages have no
+ * counterpart: they encode offline on the CPU.
+ * Its scratch is a fixed 32 MiB array inside the library, held by every GPU
+ * that loads the library until the process exits; a layer whose
+ * k3huf_encode_scratch_bytes exceeds 32 MiB (about 10^9 values with
+ * 256-value sub-streams) is refused with K3HUF_E_ARG.  Arguments, output and
+ * errors otherwise as k3huf_encode_layer_gpu; nothing is allocated on the
+ * device.  The first call on a device looks up the array's address on that
+ * device (make that first call before any stream capture).  All calls share
+ * the one array: calls whose work overlaps on the GPU (other streams, other
+ * host threads) race and must be serialised by the caller. */
+int k3huf_encode_layer_gpu_noalloc(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
+                                   uint32_t chunk_syms, uint32_t sub_syms, int shared_table, void *d_blob,
+                                   size_t blob_cap, size_t *blob_bytes, void *stream);
+
 /* Streaming ring: layers held in pinned host memory are copied to device
  * slots with cudaMemcpyAsync on a copy stream while the previous layer is
  * decoded on a compute stream, double buffered (the article's trunk ring,

@@ -384,3 +384,51 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         return K3HUF_E_NOMEM;
     }
 }
+
+// ---------------------------------------------------------------------------
+// The same encoder for callers that cannot allocate device memory: its
+// scratch is this fixed array, which every GPU that loads the library holds
+// until the process exits.  Host code must not use the array's name as a
+// device address; the address comes from cudaGetSymbolAddress, once per
+// device, with that device current.
+
+#include <mutex>
+
+namespace {
+
+constexpr size_t kFixedScratchBytes = size_t(32) << 20;
+constexpr int kFixedMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_encode_scratch[kFixedScratchBytes];
+
+std::mutex g_fixed_mutex;
+void *g_fixed_addr[kFixedMaxDevices] = {};
+
+}  // namespace
+
+extern "C" int k3huf_encode_layer_gpu_noalloc(uint32_t n_tensors, const void *const *d_tensors,
+                                              const uint64_t *n_values, uint32_t chunk_syms, uint32_t sub_syms,
+                                              int shared_table, void *d_blob, size_t blob_cap, size_t *blob_bytes,
+                                              void *stream) {
+    size_t need = 0;
+    int rc = k3huf_encode_scratch_bytes(n_tensors, n_values, chunk_syms, sub_syms, shared_table, &need);
+    if (rc != K3HUF_OK) return rc;
+    if (need > kFixedScratchBytes) return K3HUF_E_ARG;      // the layer is larger than the fixed scratch serves
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kFixedMaxDevices) return K3HUF_E_ARG;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_fixed_mutex);
+        if (!g_fixed_addr[dev]) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_encode_scratch);
+            if (e != cudaSuccess) return cuda_fail(e);
+            g_fixed_addr[dev] = p;
+        }
+        scratch = g_fixed_addr[dev];
+    }
+    return k3huf_encode_layer_gpu(n_tensors, d_tensors, n_values, chunk_syms, sub_syms, shared_table, scratch,
+                                  kFixedScratchBytes, d_blob, blob_cap, blob_bytes, stream);
+}
