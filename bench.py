@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="projection",
-                    choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring", "ring_file", "encode"])
+                    choices=["tiny", "projection", "heavy_tail", "trunk_layer", "ring", "ring_file", "encode", "gemv"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--variant", type=int, default=0, help="codes per lookup: 0 default (2), 1, 2")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -201,7 +201,8 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    name = {"ring": "trunk_layer", "ring_file": "trunk_layer", "encode": "heavy_tail"}.get(args.workload, args.workload)
+    name = {"ring": "trunk_layer", "ring_file": "trunk_layer", "encode": "heavy_tail",
+            "gemv": "projection"}.get(args.workload, args.workload)
     tensors, blob = make_layer(name)
     info = oracle.layer_info(blob)
     out = np.zeros(info["out_bytes"], dtype=np.uint8)
@@ -277,6 +278,8 @@ def main():
         return bench_ring_file(args, rank, world, local, dev)
     if args.workload == "encode":
         return bench_encode(args, rank, world, local, dev)
+    if args.workload == "gemv":
+        return bench_gemv(args, rank, world, local, dev)
 
     tensors, blob = make_layer(args.workload, args.sub_syms)
     info = k3.layer_info(blob)
@@ -555,6 +558,88 @@ def bench_encode(args, rank, world, local, dev):
         dt = time.perf_counter() - t0
         line["cpu_baseline"] = {"value": round(2 * m / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {m} values (one stripe, {2 * m >> 20} MiB) encoded by the oracle in {dt:.1f} s, one thread"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def bench_gemv(args, rank, world, local, dev):
+    """Decode fused into a matrix-vector product: y = W x with W held as a
+    k3huf container and decoded on chip, against the unfused path (decode W
+    into HBM, then cuBLAS GEMV through torch.mv on the bf16 weights).  The
+    value is weight bytes (bf16) per second of the fused call."""
+    import torch
+    import lossless_bf16_weight_k3huf_gb300 as k3
+    rows, cols = 8192, 16384
+    w = workloads.projection(rows=rows, cols=cols).reshape(rows, cols)
+    blob = k3.encode_layer([w])
+    info = k3.layer_info(blob)
+    hdr = blob[: info["hdr_bytes"]].copy()
+    d_blob = torch.from_numpy(blob).to(dev)
+    x_bits = workloads.normal_tensor((cols,), 1.0, 4).reshape(-1)
+    x = torch.from_numpy(x_bits.view(np.int16)).to(dev)
+    x_bf = x.view(torch.bfloat16)
+    y = torch.zeros(rows, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_out = torch.empty(info["out_bytes"], dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    # correctness against the unfused path
+    k3.gemv_layer(hdr, d_blob, 0, cols, x, y, st)
+    k3.decode_layer(hdr, d_blob, d_out, st)
+    W = d_out[: 2 * rows * cols].view(torch.bfloat16).view(rows, cols)
+    ref = (W.float() @ x_bf.float())
+    torch.cuda.synchronize()
+    if st.item() != 0:
+        raise SystemExit("fused GEMV reported a fault")
+    mag = W.float().abs() @ x_bf.float().abs()
+    if not bool(((y - ref).abs() <= 1e-4 * mag + 1e-30).all()):
+        raise SystemExit("fused GEMV disagrees with decode + matmul")
+
+    def fused():
+        y.zero_()
+        k3.gemv_layer(hdr, d_blob, 0, cols, x, y, st)
+
+    def unfused():
+        k3.decode_layer(hdr, d_blob, d_out, st)
+        torch.mv(W, x_bf)
+
+    def timed(fn, steps):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps / 1e3
+
+    with ClockSampler(dev.index) as clk:
+        t_f = timed(fused, args.steps)
+    t_u = timed(unfused, args.steps)
+    t_mv = timed(lambda: torch.mv(W, x_bf), args.steps)
+    raw = 2 * rows * cols
+    peak, peak_kind = measured_peak()
+    alg = info["blob_bytes"] + 2 * cols + 4 * rows * 2          # container, x, y read and written
+    line = {
+        "metric": "bf16 weight GB/s of y = W x with W decoded on chip (fused decode + GEMV) on 1 GB300",
+        "value": round(raw / t_f / 1e9, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_f * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {**describe("gemv"), "rows": rows, "cols": cols, "raw_bytes": raw,
+                   "blob_bytes": info["blob_bytes"], "compression_ratio": round(raw / info["blob_bytes"], 4),
+                   "unfused_ms": round(t_u * 1e3, 4), "speedup_vs_unfused": round(t_u / t_f, 3),
+                   "cublas_gemv_bf16_ms": round(t_mv * 1e3, 4),
+                   "note": "unfused = k3huf_decode_layer into HBM, then torch.mv (cuBLAS) on the bf16 weights",
+                   "l2": "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": round(alg / t_f / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(alg / t_f / 1e9 / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": None, "algorithmic_bytes_per_call": alg},
+        "e2e": {"value": round(raw / t_f / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "note": "weights resident compressed in HBM; no host traffic per call"},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -181,6 +181,25 @@ int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tensors, const u
                        uint32_t chunk_syms, uint32_t sub_syms, int shared_table, int n_threads,
                        void *h_blob, size_t blob_cap, size_t *blob_bytes);
 
+/* Decode fused into its consumer: y[r] += sum_c W[r][c] * x[c] for tensor
+ * `tensor` of the layer read as a row-major matrix of `cols` columns, with
+ * the weights decoded on chip and never written to device memory.  The
+ * article "Kimi K3 纯 CPU 推理中的无损 Trunk 压缩" (section 背景) streams
+ * the trunk to feed matrix-vector products; the ECF8 article ("1. 指数集中
+ * 现象", its PyTorch hook) decodes into a bf16 buffer and then copies it into
+ * the weight; here the decoded values go straight into fp32 dot products.
+ *  d_layer: as for k3huf_decode_layer; d_x: device, 16-byte aligned, cols
+ *    bf16 values; d_y: device, 4-byte aligned, n_values / cols floats,
+ *    accumulated (zero it for y = W x); atomic fp32 additions, so the
+ *    summation order, and the last bits, vary from run to run.
+ *  Needs: cols divides the tensor's values and is a multiple of 32 x
+ *    sub_syms (every work item lies in one row), sub_syms a multiple of 8
+ *    with 32 / (chunk_syms / sub_syms) whole, and sub-streams short enough
+ *    to stage (sub_syms x 12 / 8 + 64 <= 7744): K3HUF_E_ARG otherwise.
+ * Asynchronous on `stream`; stream faults set bits in *d_status. */
+int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                     uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status, void *stream);
+
 /* GPU encoder: the same container as k3huf_encode_layer (byte for byte),
  * built from bf16 tensors already in device memory.  The article "Kimi K3
  * 纯 CPU 推理中的无损 Trunk 压缩" (section 已实现的部分) packs offline:

@@ -29,7 +29,7 @@ EXPORTS = [
     "k3huf_set_decoder_variant", "k3huf_encode_layer", "k3huf_ring_create", "k3huf_ring_run",
     "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
     "k3huf_feed_read", "k3huf_feed_close", "k3huf_ring_create_staged", "k3huf_ring_run_file",
-    "k3huf_encode_scratch_bytes", "k3huf_encode_layer_gpu",
+    "k3huf_encode_scratch_bytes", "k3huf_encode_layer_gpu", "k3huf_gemv_layer",
 ]
 FILE_ALIGN = 4096
 
@@ -103,6 +103,7 @@ def _lib():
             L.k3huf_encode_layer_gpu.argtypes = [ctypes.c_uint32, ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint64),
                                                  ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, _vp, _sz, _vp, _sz,
                                                  ctypes.POINTER(_sz), _vp]
+            L.k3huf_gemv_layer.argtypes = [_vp, _sz, _vp, _sz, ctypes.c_uint32, ctypes.c_uint64, _vp, _vp, _vp, _vp]
             L.k3huf_feed_open.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(_vp)]
             L.k3huf_feed_direct.argtypes = [_vp]
             L.k3huf_feed_read.argtypes = [_vp, ctypes.c_uint64, _sz, _vp, _sz]
@@ -256,6 +257,16 @@ def decode_layer(hdr, d_layer, d_out, d_status, stream=None, layer_bytes: int | 
     ob = _nbytes(d_out) if out_bytes is None else out_bytes
     _check(_lib().k3huf_decode_layer(h.ctypes.data, h.size, _dptr(d_layer), lb, _dptr(d_out), ob,
                                      _dptr(d_status), _stream(stream)), "k3huf_decode_layer")
+
+
+def gemv_layer(hdr, d_layer, tensor: int, cols: int, d_x, d_y, d_status, stream=None,
+               layer_bytes: int | None = None) -> None:
+    """y += W x with tensor ``tensor`` of the layer as a row-major matrix of
+    ``cols`` columns, decoded on chip (never written out); asynchronous."""
+    h = _host(hdr)
+    lb = _nbytes(d_layer) if layer_bytes is None else layer_bytes
+    _check(_lib().k3huf_gemv_layer(h.ctypes.data, h.size, _dptr(d_layer), lb, tensor, cols, _dptr(d_x), _dptr(d_y),
+                                   _dptr(d_status), _stream(stream)), "k3huf_gemv_layer")
 
 
 def decode_stripe(codelen, chunk_syms: int, sub_syms: int, d_stripe, stripe_bytes: int, n_values: int, d_out,

@@ -82,7 +82,7 @@ struct StripeTask {
     uint32_t n_values;
     uint32_t table;
     uint32_t item_begin;        // first work item of this stripe in the launch
-    uint32_t reserved;
+    uint32_t tensor_stripe;     // index of the stripe within its tensor (fused GEMV)
 };
 
 struct DecodeParams {
@@ -93,10 +93,25 @@ struct DecodeParams {
     uint32_t sub_syms;
     uint32_t n_items;
     uint8_t inline_table[256];
+    const uint8_t *gemv_x;      // fused GEMV: device bf16 x[cols], or null
+    float *gemv_y;              // fused GEMV: device y[rows], accumulated
+    uint64_t gemv_cols;
     StripeTask task[kMaxTasks];
 };
 
 __device__ __forceinline__ uint32_t bswap32(uint32_t x) { return __byte_perm(x, 0, 0x0123); }
+
+// acc + the dot product of 8 bf16 weights and 8 bf16 inputs (bf16 -> fp32 is
+// exact: the 16 bits become the top half of the float)
+__device__ __forceinline__ float dot8(const uint4 w, const uint4 x, float acc) {
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w}, b[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        acc = fmaf(__uint_as_float(a[k] << 16), __uint_as_float(b[k] << 16), acc);
+        acc = fmaf(__uint_as_float(a[k] & 0xFFFF0000u), __uint_as_float(b[k] & 0xFFFF0000u), acc);
+    }
+    return acc;
+}
 
 // Row swizzle: 8-byte unit u of lane l's row sits at unit u ^ row_swz(l).
 // The 32 lanes' 8-byte stores of one unit, and the merge's 8-byte reads of
@@ -375,7 +390,7 @@ __device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, uin
     return ok;
 }
 
-template <int kPer, bool kVec, bool kStaged>
+template <int kPer, bool kVec, bool kStaged, bool kGemv>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -494,6 +509,15 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             uint8_t *out = T.out;
             const uint32_t n_streams = nch * S;
             const uint32_t g0 = (wi - T.item_begin) * kItem;
+            // fused GEMV: the item lies inside one row of the matrix (the row
+            // length is a multiple of the item's span)
+            float gacc = 0.f;
+            uint64_t grow = 0, gcol0 = 0;
+            if (kGemv) {
+                const uint64_t f0 = uint64_t(T.tensor_stripe) * K3HUF_STRIPE_VALUES + uint64_t(g0) * ss;
+                grow = f0 / P.gemv_cols;
+                gcol0 = f0 - grow * P.gemv_cols;
+            }
 
             // this lane's sub-stream g: values [g*ss, g*ss + len)
             const uint32_t g = g0 + uint32_t(lane);
@@ -615,6 +639,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 // this pass): piece i sits 4 * i sub-streams after piece 0
                 const uint32_t q = uint32_t(lane) >> 3;
                 uint8_t *const out_p0 = out + 2 * (size_t(g0 + q) * ss + sub * 8u);
+                const uint8_t *const x_p0 = kGemv ? P.gemv_x + 2 * (gcol0 + size_t(q) * ss + sub * 8u) : nullptr;
                 const uint8_t *const even_p0 = even + size_t(g0 + q) * ss + sub * 8u;
                 const size_t pstride = size_t(4) * ss;
 
@@ -710,7 +735,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             o.y = interleave_hi(ev[i].x, h.x);
                             o.z = interleave_lo(ev[i].y, h.y);
                             o.w = interleave_hi(ev[i].y, h.y);
-                            *reinterpret_cast<uint4 *>(out_p0 + 2 * (size_t(i) * pstride + rv)) = o;
+                            if (kGemv)
+                                gacc = dot8(o, __ldg(reinterpret_cast<const uint4 *>(x_p0 + 2 * (size_t(i) * pstride + rv))), gacc);
+                            else
+                                *reinterpret_cast<uint4 *>(out_p0 + 2 * (size_t(i) * pstride + rv)) = o;
                         }
                         if (__all_sync(0xffffffffu, rem >= uint32_t(2 * kRound))) {
 #pragma unroll
@@ -733,6 +761,19 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             o.y = interleave_hi(ev[i].x, hx);
                             o.z = interleave_lo(ev[i].y, hy);
                             o.w = interleave_hi(ev[i].y, hy);
+                            if (kGemv) {
+                                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(P.gemv_x + 2 * (gcol0 + size_t(gw) * ss + v)));
+                                uint4 wv = o;
+                                if (v + 8 > m_len) {          // weights past the sub-stream's end count zero
+                                    const uint32_t kk = m_len - v;
+                                    wv.x = kk >= 2 ? wv.x : kk == 1 ? (wv.x & 0xFFFFu) : 0u;
+                                    wv.y = kk >= 4 ? wv.y : kk == 3 ? (wv.y & 0xFFFFu) : 0u;
+                                    wv.z = kk >= 6 ? wv.z : kk == 5 ? (wv.z & 0xFFFFu) : 0u;
+                                    wv.w = kk >= 8 ? wv.w : kk == 7 ? (wv.w & 0xFFFFu) : 0u;
+                                }
+                                gacc = dot8(wv, xv, gacc);
+                                continue;
+                            }
                             uint8_t *dst = out + 2 * (size_t(g0 + gw) * ss + v);
                             if (v + 8 <= m_len) {
                                 *reinterpret_cast<uint4 *>(dst) = o;
@@ -771,12 +812,17 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 __syncwarp();                            // slot free for the next pass / item
                 pa = pb;
             }
+            if (kGemv) {
+#pragma unroll
+                for (int d = 16; d; d >>= 1) gacc += __shfl_xor_sync(0xffffffffu, gacc, d);
+                if (lane == 0 && gacc != 0.f) atomicAdd(P.gemv_y + grow, gacc);
+            }
         }
         item = pend;
     }
 }
 
-template <int kPer, bool kVec, bool kStaged>
+template <int kPer, bool kVec, bool kStaged, bool kGemv = false>
 int launch(DecodeParams &P, cudaStream_t stream) {
     static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
     static int grid_max[kMaxDevices] = {};
@@ -787,12 +833,12 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         return K3HUF_E_CUDA;
     }
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged, kGemv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(kSmemBytes));
         int sms = 0, per_sm = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged>, kThreads,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged, kGemv>, kThreads,
                                                               kSmemBytes);
         if (e != cudaSuccess) {
             set_cuda_error(int(e));
@@ -802,7 +848,7 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         attr_set[dev] = true;
     }
     const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(grid_max[dev]));
-    decode_kernel<kPer, kVec, kStaged><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    decode_kernel<kPer, kVec, kStaged, kGemv><<<grid, kThreads, kSmemBytes, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_cuda_error(int(e));
@@ -821,6 +867,14 @@ int launch_syms(DecodeParams &P, cudaStream_t stream) {
     const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= kBitBuf;
     if (staged) return vec ? launch<kPer, true, true>(P, stream) : launch<kPer, false, true>(P, stream);
     return vec ? launch<kPer, true, false>(P, stream) : launch<kPer, false, false>(P, stream);
+}
+
+// fused GEMV launches: staged bits and the vector merge only
+int launch_gemv(DecodeParams &P, cudaStream_t stream) {
+    switch (g_per) {
+        case 1: return launch<1, true, true, true>(P, stream);
+        default: return launch<2, true, true, true>(P, stream);
+    }
 }
 
 int launch_tasks(DecodeParams &P, cudaStream_t stream) {
@@ -861,7 +915,7 @@ extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, con
     if (layer_bytes < L.info.blob_bytes || out_bytes < L.info.out_bytes) return K3HUF_E_ARG;
     const uint8_t *blob = static_cast<const uint8_t *>(d_layer);
     uint8_t *out = static_cast<uint8_t *>(d_out);
-    DecodeParams P;
+    DecodeParams P{};
     P.tables = blob + K3HUF_LAYER_HDR_BYTES;
     P.status = d_status;
     P.chunk_syms = L.info.chunk_syms;
@@ -879,7 +933,7 @@ extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, con
             t.n_values = e.n_values;
             t.table = e.table;
             t.item_begin = items;
-            t.reserved = 0;
+            t.tensor_stripe = 0;
             items += items_of(e.n_values, P.chunk_syms, P.sub_syms);
         }
         P.n_items = items;
@@ -902,7 +956,7 @@ extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_sy
     if (stripe_bytes < align_up(K3HUF_STRIPE_HDR_BYTES + index_bytes(nch, chunk_syms, sub_syms), 16) + kBitsSlack +
                            n_values)
         return K3HUF_E_ARG;
-    DecodeParams P;
+    DecodeParams P{};
     P.tables = nullptr;
     P.status = d_status;
     P.chunk_syms = chunk_syms;
@@ -916,7 +970,57 @@ extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_sy
     t.n_values = n_values;
     t.table = 0;
     t.item_begin = 0;
-    t.reserved = 0;
+    t.tensor_stripe = 0;
     P.n_items = items_of(n_values, chunk_syms, sub_syms);
     return launch_tasks(P, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                                uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
+                                void *stream) {
+    using namespace k3huf;
+    if (!h_layer_hdr || !d_layer || !d_x || !d_y || !d_status || cols == 0) return K3HUF_E_ARG;
+    if (!aligned16(d_layer) || !aligned16(d_x) || (reinterpret_cast<uintptr_t>(d_y) & 3u) ||
+        (reinterpret_cast<uintptr_t>(d_status) & 3u))
+        return K3HUF_E_ARG;
+    Layer L;
+    int rc = parse_layer(h_layer_hdr, hdr_bytes, &L);
+    if (rc) return rc;
+    if (layer_bytes < L.info.blob_bytes || tensor >= L.tensors.size()) return K3HUF_E_ARG;
+    const TensorEntry &te = L.tensors[tensor];
+    const uint32_t ss = L.info.sub_syms, cs = L.info.chunk_syms;
+    // every work item (32 sub-streams of ss values, whole chunks) must lie in one row
+    if (te.n_values % cols != 0 || cols % (uint64_t(kItem) * ss) != 0 || ss % 8 != 0 || kItem % (cs / ss) != 0 ||
+        uint64_t(ss) * K3HUF_MAXLEN / 8 + 64 > kBitBuf)
+        return K3HUF_E_ARG;
+    const uint8_t *blob = static_cast<const uint8_t *>(d_layer);
+    DecodeParams P{};
+    P.tables = blob + K3HUF_LAYER_HDR_BYTES;
+    P.status = d_status;
+    P.chunk_syms = cs;
+    P.sub_syms = ss;
+    P.gemv_x = static_cast<const uint8_t *>(d_x);
+    P.gemv_y = d_y;
+    P.gemv_cols = cols;
+    for (uint32_t s0 = 0; s0 < te.n_stripes; s0 += kMaxTasks) {
+        const uint32_t s1 = std::min<uint32_t>(te.n_stripes, s0 + kMaxTasks);
+        uint32_t items = 0;
+        P.n_tasks = s1 - s0;
+        for (uint32_t s = s0; s < s1; ++s) {
+            const StripeEntry &e = L.stripes[te.first_stripe + s];
+            StripeTask &t = P.task[s - s0];
+            t.stripe = blob + e.blob_offset;
+            t.out = nullptr;
+            t.stripe_bytes = e.stripe_bytes;
+            t.n_values = e.n_values;
+            t.table = e.table;
+            t.item_begin = items;
+            t.tensor_stripe = s;
+            items += items_of(e.n_values, cs, ss);
+        }
+        P.n_items = items;
+        rc = launch_gemv(P, static_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+    }
+    return K3HUF_OK;
 }

@@ -1,0 +1,98 @@
+"""Decode fused into its consumer: y += W x with W held as a k3huf container
+and decoded on chip.  Compared with the oracle's decode of W multiplied by x
+in float64.  The GPU sums in fp32: each lane adds about sub_syms products in
+order, a warp reduction adds 5 levels and the row's work items are added
+atomically, so the error is below (256 + 5 + items per row) x 2^-24 of
+sum |W| |x|; the test allows 1e-4 of it."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+torch = pytest.importorskip("torch")
+k3 = pytest.importorskip("lossless_bf16_weight_k3huf_gb300")
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    k3._build.build()
+
+
+def bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def run_gemv(blob, tensor, cols, x_bits, y0=None):
+    info = k3.layer_info(blob)
+    d_blob = torch.from_numpy(blob).cuda()
+    n = k3.tensor_info(blob, tensor)["n_values"]
+    y = torch.zeros(n // cols, dtype=torch.float32, device="cuda") if y0 is None else y0
+    x = torch.from_numpy(x_bits.view(np.int16)).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k3.gemv_layer(blob[: info["hdr_bytes"]], d_blob, tensor, cols, x, y, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return y.cpu().numpy().astype(np.float64)
+
+
+def reference(blob, tensor, cols, x_bits):
+    rc, out = oracle.decode_layer(blob)
+    assert rc == 0
+    t = k3.tensor_info(blob, tensor)
+    w = out[t["out_offset"]: t["out_offset"] + 2 * t["n_values"]].view(np.uint16)
+    W = bf16_to_f64(w).reshape(-1, cols)
+    x = bf16_to_f64(x_bits)
+    return W @ x, np.abs(W) @ np.abs(x)
+
+
+def x_vector(cols, seed):
+    return workloads.normal_tensor((cols,), 1.0, seed).reshape(-1)
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 8192), (7, 8192), (64, 16384), (3, 24576)])
+def test_gemv_matches_oracle(rows, cols):
+    w = workloads.normal_tensor((rows, cols), 0.02, rows + cols)
+    blob = oracle.encode_layer([w])
+    x = x_vector(cols, 5)
+    y = run_gemv(blob, 0, cols, x)
+    ref, mag = reference(blob, 0, cols, x)
+    assert np.all(np.abs(y - ref) <= 1e-4 * mag + 1e-30)
+
+
+def test_gemv_multi_stripe_tensor_and_heavy_tail():
+    rows, cols = 4097, 8192                     # 2^25 + 8192 values: two stripes, the second one row
+    w = workloads.heavy_tail(n=rows * cols).reshape(rows, cols)
+    blob = oracle.encode_layer([w])
+    assert k3.layer_info(blob)["n_stripes"] == 2
+    x = x_vector(cols, 6)
+    y = run_gemv(blob, 0, cols, x)
+    ref, mag = reference(blob, 0, cols, x)
+    assert np.all(np.abs(y - ref) <= 1e-4 * mag + 1e-30)
+
+
+def test_gemv_picks_the_tensor_and_accumulates():
+    ts = [workloads.normal_tensor((5, 8192), 0.1, 1), workloads.normal_tensor((9, 16384), 0.03, 2),
+          workloads.normal_tensor((77,), 0.3, 3)]
+    blob = oracle.encode_layer(ts)
+    x = x_vector(16384, 7)
+    y0 = torch.full((9,), 0.5, dtype=torch.float32, device="cuda")
+    y = run_gemv(blob, 1, 16384, x, y0=y0)
+    ref, mag = reference(blob, 1, 16384, x)
+    assert np.all(np.abs(y - (ref + 0.5)) <= 1e-4 * mag + 1e-6)
+
+
+def test_gemv_refuses_unsupported_shapes():
+    blob = oracle.encode_layer([workloads.normal_tensor((24, 576), 0.02, 4), workloads.normal_tensor((2, 8192), 0.02, 5)])
+    info = k3.layer_info(blob)
+    d_blob = torch.from_numpy(blob).cuda()
+    x = torch.zeros(8192, dtype=torch.int16, device="cuda")
+    y = torch.zeros(64, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for tensor, cols in [(0, 576), (1, 4096), (1, 3000), (2, 8192)]:
+        with pytest.raises(k3.K3HufError) as e:
+            k3.gemv_layer(blob[: info["hdr_bytes"]], d_blob, tensor, cols, x, y, st)
+        assert e.value.code == k3.E_ARG

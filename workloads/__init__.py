@@ -42,6 +42,7 @@ WORKLOADS = {
     "ring": "14 trunk layers (seeds 10..23) streamed from pinned host memory",
     "ring_file": "trunk layers (seeds 10..) read from a container file (O_DIRECT where allowed) into the pinned ring",
     "encode": "GPU encoder: the heavy-tail 1 GiB bf16 tensor (seed 2) packed into a container on the device",
+    "gemv": "y = W x with the projection matrix W (8192x16384, seed 1) held compressed, x ~ N(0,1) bf16 (seed 4)",
 }
 
 _THREADS = max(1, min(16, os.cpu_count() or 1))
