@@ -10,15 +10,17 @@
 //  2. host: code lengths, codes and the container layout, with the same
 //     functions as the CPU encoder (k3huf_host.cpp), so both write the same
 //     bytes; the blob is zeroed and the header copied in;
-//  3. per-sub-stream bit counts (one thread per sub-stream);
-//  4. per stripe, one CTA scans them into the chunk index, the sub-stream
-//     index and each sub-stream's first bit, writes the stripe header and
-//     checks the total against the planned bit count;
-//  5. one thread per sub-stream packs its codes MSB-first into 32-bit words
-//     (OR-ed atomically: a sub-stream shares its edge words with its
-//     neighbours) and copies its low bytes into the even plane.
+//  3. bits of every chunk (one warp per chunk, coalesced 16-byte loads);
+//  4. per stripe, one CTA scans them into the chunk index, writes the stripe
+//     header and checks the total against the planned bit count;
+//  5. one warp per chunk packs its codes MSB-first: each step of 256 values
+//     gives every lane 8 codes, a warp scan of the lanes' bit counts places
+//     them, the codes are OR-ed into a shared staging window, whole words go
+//     out with plain coalesced stores and only the words a chunk shares with
+//     its neighbours with atomic ORs; the same pass writes the sub-stream
+//     index and the low bytes.
 // Scratch (caller-owned device memory, k3huf_encode_scratch_bytes) holds
-// the stripe descriptors, histograms, code tables, bit counts and starts.
+// the stripe descriptors, histograms, code tables, and two words per chunk.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -37,28 +39,29 @@ struct EncStripe {
     uint64_t huff_bits;    // planned bits of the stripe's stream
     uint32_t n, n_chunks;
     uint32_t table, bits_offset;
-    uint32_t even_offset, sub_begin;   // first sub-stream of the stripe in the per-sub-stream arrays
+    uint32_t even_offset, chunk_begin;   // first chunk of the stripe in the per-chunk arrays
 };
 
 struct EncParams {
     const EncStripe *stripes;
     const uint32_t *codes;     // n_tables x 256: (code << 4) | length
     uint32_t *counts;          // n_stripes x 256
-    uint32_t *sub_bits;        // bits of every sub-stream
-    uint32_t *sub_start;       // first bit of every sub-stream within its stripe's stream
+    uint32_t *chunk_bits;      // bits of every chunk
+    uint32_t *chunk_start;     // first bit of every chunk within its stripe's stream
     uint32_t *flag;            // nonzero: the packed bits disagree with the plan
     uint32_t chunk_syms, sub_syms, S;
 };
 
 struct ScratchLayout {
-    size_t stripes, counts, codes, sub_bits, sub_start, flag, total;
+    size_t stripes, counts, codes, chunk_bits, chunk_start, flag, total;
 };
 
 constexpr int kHistThreads = 256;
 constexpr int kScanThreads = 1024;
 constexpr int kPackThreads = 256;
+constexpr int kStageWords = 128;     // staging window of a packing warp (one step: <= 97 words)
 
-ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_subs) {
+ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_chunks) {
     ScratchLayout s{};
     size_t at = 0;
     auto take = [&](size_t bytes) {
@@ -69,17 +72,16 @@ ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_subs)
     s.stripes = take(n_stripes * sizeof(EncStripe));
     s.counts = take(n_stripes * 256 * sizeof(uint32_t));
     s.codes = take(n_tables * 256 * sizeof(uint32_t));
-    s.sub_bits = take(size_t(n_subs) * sizeof(uint32_t));
-    s.sub_start = take(size_t(n_subs) * sizeof(uint32_t));
+    s.chunk_bits = take(size_t(n_chunks) * sizeof(uint32_t));
+    s.chunk_start = take(size_t(n_chunks) * sizeof(uint32_t));
     s.flag = take(sizeof(uint32_t));
     s.total = at;
     return s;
 }
 
-uint64_t count_subs(const LayerPlan &L) {
+uint64_t count_chunks(const LayerPlan &L) {
     uint64_t n = 0;
-    const uint32_t S = L.chunk_syms / L.sub_syms;
-    for (const auto &p : L.stripes) n += uint64_t(p.n_chunks) * S;
+    for (const auto &p : L.stripes) n += p.n_chunks;
     return n;
 }
 
@@ -112,53 +114,45 @@ __global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
     }
 }
 
-// values [a, b) of sub-stream j (k-th of chunk c) of a stripe
-__device__ __forceinline__ void sub_range(const EncParams &P, const EncStripe &T, uint32_t j, uint64_t &a, uint64_t &b) {
-    const uint32_t c = j / P.S, k = j - c * P.S;
-    const uint64_t c0 = uint64_t(c) * P.chunk_syms;
-    const uint64_t len_c = min(uint64_t(P.chunk_syms), uint64_t(T.n) - c0);
-    a = c0 + min(uint64_t(k) * P.sub_syms, len_c);
-    b = c0 + min(uint64_t(k + 1) * P.sub_syms, len_c);
-}
-
-// 3. bits of every sub-stream
-__global__ void __launch_bounds__(kPackThreads) sub_bits_kernel(EncParams P) {
+// 3. bits of every chunk: one warp per chunk, 8 values per lane and step
+__global__ void __launch_bounds__(kPackThreads) chunk_bits_kernel(EncParams P) {
     __shared__ uint8_t len[256];
     const EncStripe &T = P.stripes[blockIdx.y];
     for (int s = threadIdx.x; s < 256; s += kPackThreads) len[s] = uint8_t(P.codes[size_t(T.table) * 256 + s] & 15u);
     __syncthreads();
-    const uint32_t nsub = T.n_chunks * P.S;
-    for (uint32_t j = blockIdx.x * kPackThreads + threadIdx.x; j < nsub; j += gridDim.x * kPackThreads) {
-        uint64_t a, b;
-        sub_range(P, T, j, a, b);
+    const int lane = threadIdx.x & 31;
+    const uint32_t warps = gridDim.x * (kPackThreads / 32);
+    const bool vec = P.chunk_syms % 8 == 0;
+    for (uint32_t c = blockIdx.x * (kPackThreads / 32) + (threadIdx.x >> 5); c < T.n_chunks; c += warps) {
+        const uint64_t a = uint64_t(c) * P.chunk_syms, b = min(uint64_t(T.n), a + P.chunk_syms);
         uint32_t bits = 0;
-        uint64_t v = a;
-        if ((a & 7) == 0)
-            for (; v + 8 <= b; v += 8) {
+        for (uint64_t v = a + 8 * uint64_t(lane); v < b; v += 256) {
+            if (vec && v + 8 <= b) {
                 const uint4 x = *reinterpret_cast<const uint4 *>(T.src + 2 * v);
                 const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) bits += len[(w[i] >> 8) & 0xFFu] + len[w[i] >> 24];
+            } else {
+                for (uint64_t u = v; u < min(b, v + 8); ++u) bits += len[T.src[2 * u + 1]];
             }
-        for (; v < b; ++v) bits += len[T.src[2 * v + 1]];
-        P.sub_bits[T.sub_begin + j] = bits;
+        }
+        bits = __reduce_add_sync(0xffffffffu, bits);
+        if (lane == 0) P.chunk_bits[T.chunk_begin + c] = bits;
     }
 }
 
-// 4. one CTA per stripe: chunk index, sub-stream index, sub-stream starts,
-//    stripe header, and the check of the total against the plan
+// 4. one CTA per stripe: the chunk index (exclusive prefix of the chunks'
+//    bits), the stripe header, and the check of the total against the plan
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(EncParams P) {
     __shared__ uint64_t s_warp[kScanThreads / 32];
     const EncStripe &T = P.stripes[blockIdx.x];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t nch = T.n_chunks, S = P.S;
+    const uint32_t nch = T.n_chunks;
     const uint32_t per = (nch + kScanThreads - 1) / kScanThreads;
     const uint32_t c_lo = min(nch, uint32_t(tid) * per), c_hi = min(nch, c_lo + per);
-    const uint32_t *bits = P.sub_bits + T.sub_begin;
+    const uint32_t *bits = P.chunk_bits + T.chunk_begin;
     uint64_t sum = 0;
-    for (uint32_t c = c_lo; c < c_hi; ++c)
-        for (uint32_t k = 0; k < S; ++k) sum += bits[size_t(c) * S + k];
-    // exclusive scan of the threads' sums
+    for (uint32_t c = c_lo; c < c_hi; ++c) sum += bits[c];
     uint64_t incl = sum;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -167,20 +161,13 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(EncParams P) {
     }
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    uint64_t base = 0;
-    for (int w = 0; w < warp; ++w) base += s_warp[w];
-    uint64_t off = base + incl - sum;
+    uint64_t off = incl - sum;
+    for (int w = 0; w < warp; ++w) off += s_warp[w];
     uint32_t *chunk_idx = reinterpret_cast<uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
-    uint16_t *sub_idx = reinterpret_cast<uint16_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES + 4ull * nch);
     for (uint32_t c = c_lo; c < c_hi; ++c) {
         chunk_idx[c] = uint32_t(off);
-        uint32_t rel = 0;
-        for (uint32_t k = 0; k < S; ++k) {
-            if (k > 0) sub_idx[size_t(c) * (S - 1) + k - 1] = uint16_t(rel);
-            P.sub_start[T.sub_begin + size_t(c) * S + k] = uint32_t(off) + rel;
-            rel += bits[size_t(c) * S + k];
-        }
-        off += rel;
+        P.chunk_start[T.chunk_begin + c] = uint32_t(off);
+        off += bits[c];
     }
     if (c_hi == nch && c_lo < c_hi && off != T.huff_bits) atomicOr(P.flag, 1u);
     if (tid == 0) {
@@ -196,56 +183,176 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(EncParams P) {
     }
 }
 
-// 5. pack one sub-stream's codes MSB-first and copy its low bytes
+// 5. one warp per chunk: codes packed MSB-first, sub-stream index, low bytes
 __global__ void __launch_bounds__(kPackThreads) pack_kernel(EncParams P) {
     __shared__ uint32_t code[256];
+    __shared__ uint32_t s_stage[kPackThreads / 32][kStageWords];
     const EncStripe &T = P.stripes[blockIdx.y];
     for (int s = threadIdx.x; s < 256; s += kPackThreads) code[s] = P.codes[size_t(T.table) * 256 + s];
     __syncthreads();
+    const int lane = threadIdx.x & 31;
+    uint32_t *stage = s_stage[threadIdx.x >> 5];
     uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
     const uint32_t n_words = (T.even_offset - T.bits_offset) / 4;   // the stream region, padding included
     uint8_t *even = T.dst + T.even_offset;
-    const uint32_t nsub = T.n_chunks * P.S;
-    for (uint32_t j = blockIdx.x * kPackThreads + threadIdx.x; j < nsub; j += gridDim.x * kPackThreads) {
-        uint64_t a, b;
-        sub_range(P, T, j, a, b);
-        const uint32_t pos = P.sub_start[T.sub_begin + j];
-        uint32_t w = pos >> 5, nb = pos & 31u;   // the word's leading bits belong to the previous sub-stream
-        uint64_t acc = 0;
-        auto put = [&](uint32_t hb) {
-            const uint32_t e = code[hb], l = e & 15u;
-            acc = (acc << l) | (e >> 4);
-            nb += l;
-            if (nb >= 32) {
-                nb -= 32;
-                const uint32_t word = uint32_t(acc >> nb);
-                if (word && w < n_words) atomicOr(&words[w], __byte_perm(word, 0, 0x0123));
-                ++w;
-                acc &= (uint64_t(1) << nb) - 1;
-            }
+    uint16_t *sub_idx = reinterpret_cast<uint16_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES + 4ull * T.n_chunks);
+    const uint32_t S = P.S, ss = P.sub_syms;
+    const bool ss_pow2 = (ss & (ss - 1)) == 0;
+    const uint32_t ss_shift = ss_pow2 ? uint32_t(__ffs(int(ss)) - 1) : 0u;
+    const bool vec = P.chunk_syms % 8 == 0;
+    const uint32_t warps = gridDim.x * (kPackThreads / 32);
+    // value indices within a stripe (at most 2^25) fit in 32 bits
+    for (uint32_t c = blockIdx.x * (kPackThreads / 32) + (threadIdx.x >> 5); c < T.n_chunks; c += warps) {
+        const uint32_t a = c * P.chunk_syms, b = min(T.n, a + P.chunk_syms);
+        const uint32_t c_pos = P.chunk_start[T.chunk_begin + c];
+        uint32_t pos = c_pos;                 // next bit of the stream
+        uint32_t win = pos >> 5;              // stream word held by stage[0]
+        bool first_shared = (pos & 31u) != 0; // stage[0] is shared with the previous chunk
+        for (int j = lane; j < kStageWords; j += 32) stage[j] = 0;
+        __syncwarp();
+        // the next step's 16 values are loaded one step ahead
+        auto load8 = [&](uint32_t v) -> uint4 {
+            return vec && v + 8 <= b ? *reinterpret_cast<const uint4 *>(T.src + 2 * size_t(v)) : make_uint4(0, 0, 0, 0);
         };
-        uint64_t v = a;
-        if ((a & 7) == 0)
-            for (; v + 8 <= b; v += 8) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(T.src + 2 * v);
-                const uint32_t q[4] = {x.x, x.y, x.z, x.w};
+        uint4 x_next = load8(a + 8 * uint32_t(lane));
+        for (uint32_t v0 = a; v0 < b; v0 += 256) {
+            const uint32_t v = v0 + 8 * uint32_t(lane);
+            const uint4 x = x_next;
+            x_next = load8(v + 256);
+            uint32_t hb[8], lb[8], nv = 0;
+            if (v < b) {
+                nv = min(8u, b - v);
+                if (vec && nv == 8) {
+                    const uint32_t q[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    put((q[i] >> 8) & 0xFFu);
-                    put(q[i] >> 24);
+                    for (int i = 0; i < 4; ++i) {
+                        hb[2 * i] = (q[i] >> 8) & 0xFFu;
+                        hb[2 * i + 1] = q[i] >> 24;
+                        lb[2 * i] = q[i] & 0xFFu;
+                        lb[2 * i + 1] = (q[i] >> 16) & 0xFFu;
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        hb[i] = i < int(nv) ? T.src[2 * size_t(v + i) + 1] : 0u;
+                        lb[i] = i < int(nv) ? T.src[2 * size_t(v + i)] : 0u;
+                    }
                 }
-                // low bytes of the 8 values, in order
-                const uint32_t lo0 = __byte_perm(q[0], q[1], 0x6420), lo1 = __byte_perm(q[2], q[3], 0x6420);
-                *reinterpret_cast<uint2 *>(even + v) = make_uint2(lo0, lo1);
             }
-        for (; v < b; ++v) {
-            put(T.src[2 * v + 1]);
-            even[v] = T.src[2 * v];
+            uint32_t e[8], my = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                e[i] = i < int(nv) ? code[hb[i]] : 0u;
+                my += e[i] & 15u;
+            }
+            // place the lanes' bits: exclusive scan of the bit counts
+            uint32_t incl = my;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += t;
+            }
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            uint32_t p = pos + incl - my;            // this lane's first bit (stream-relative)
+            // sub-stream boundaries among the lane's values: value k of the
+            // chunk starts sub-stream k / ss when k % ss == 0
+            if (S > 1 && nv) {
+                const uint32_t k0 = v - a;
+                const uint32_t q = ss_pow2 ? k0 >> ss_shift : k0 / ss, r = k0 - q * ss;
+                if (ss >= 8) {
+                    // at most one boundary among 8 values
+                    const uint32_t i = r ? ss - r : 0u, e_idx = r ? q + 1 : q;
+                    if (i < nv && e_idx > 0) {
+                        uint32_t off = p;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) off += uint32_t(j) < i ? (e[j] & 15u) : 0u;
+                        sub_idx[size_t(c) * (S - 1) + e_idx - 1] = uint16_t(off - c_pos);
+                    }
+                } else {
+                    uint32_t sub_e = q, sub_r = r, off = p;
+                    for (uint32_t i = 0; i < nv; ++i) {
+                        if (sub_r == 0 && sub_e > 0) sub_idx[size_t(c) * (S - 1) + sub_e - 1] = uint16_t(off - c_pos);
+                        if (++sub_r == ss) {
+                            sub_r = 0;
+                            ++sub_e;
+                        }
+                        off += e[i] & 15u;
+                    }
+                }
+            }
+            p += my;
+            // the lane's bits, assembled in a register: words wholly inside the
+            // lane's range are its own (plain stores); the first and the last
+            // word may be shared with the neighbouring lanes (atomic ORs)
+            {
+                const uint32_t q0 = p - my - win * 32u;            // window-relative first bit
+                uint32_t w = q0 >> 5, nb = q0 & 31u;
+                uint64_t acc = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t l = e[i] & 15u;
+                    acc = (acc << l) | (e[i] >> 4);
+                    nb += l;
+                    if (nb >= 32) {
+                        nb -= 32;
+                        const uint32_t word = uint32_t(acc >> nb);
+                        if (w == (q0 >> 5) && (q0 & 31u))
+                            atomicOr(&stage[w], word);                 // shared with the previous lane
+                        else
+                            stage[w] = word;
+                        ++w;
+                        acc &= (uint64_t(1) << nb) - 1;
+                    }
+                }
+                // the pending word holds lane bits beyond its leading offset (the
+                // offset is only there while no word was emitted): it may be
+                // shared with the next lane, and with the previous one
+                const bool real = w == (q0 >> 5) ? nb > (q0 & 31u) : nb > 0;
+                if (real) atomicOr(&stage[w], uint32_t(acc << (32 - nb)));
+            }
+            if (nv) {
+                if (vec && nv == 8 && (v & 7u) == 0) {
+                    const uint32_t lo0 = lb[0] | (lb[1] << 8) | (lb[2] << 16) | (lb[3] << 24);
+                    const uint32_t lo1 = lb[4] | (lb[5] << 8) | (lb[6] << 16) | (lb[7] << 24);
+                    *reinterpret_cast<uint2 *>(even + v) = make_uint2(lo0, lo1);
+                } else {
+                    for (uint32_t i = 0; i < nv; ++i) even[v + i] = uint8_t(lb[i]);
+                }
+            }
+            __syncwarp();
+            // whole words leave: stage[0 .. full) is complete
+            const uint32_t end = pos + tot;
+            const uint32_t full = (end >> 5) - win;
+            for (uint32_t j = lane; j < full; j += 32) {
+                const uint32_t gw = win + j;
+                const uint32_t word = __byte_perm(stage[j], 0, 0x0123);
+                if (gw < n_words) {
+                    if (j == 0 && first_shared)
+                        atomicOr(&words[gw], word);
+                    else
+                        words[gw] = word;
+                }
+            }
+            __syncwarp();
+            // the partial word moves to stage[0]; the rest of the window is cleared
+            const uint32_t carry = stage[full];
+            __syncwarp();
+            for (int j = lane; j < kStageWords; j += 32) stage[j] = j == 0 ? carry : 0u;
+            __syncwarp();
+            if (full) first_shared = false;
+            win += full;
+            pos = end;
         }
-        if (nb > 0) {
-            const uint32_t word = uint32_t(acc << (32 - nb));
-            if (word && w < n_words) atomicOr(&words[w], __byte_perm(word, 0, 0x0123));
+        // sub-streams that start at or past the chunk's end begin at its last bit
+        if (S > 1)
+            for (uint32_t k = uint32_t(lane) + 1; k < S; k += 32)
+                if (uint64_t(k) * ss >= uint64_t(b - a)) sub_idx[size_t(c) * (S - 1) + k - 1] = uint16_t(pos - c_pos);
+        // the last, partial word is shared with the next chunk
+        if (lane == 0 && (pos & 31u) && win < n_words) {
+            const uint32_t word = __byte_perm(stage[0], 0, 0x0123);
+            if (word) atomicOr(&words[win], word);
         }
+        __syncwarp();
     }
 }
 
@@ -274,7 +381,7 @@ extern "C" int k3huf_encode_scratch_bytes(uint32_t n_tensors, const uint64_t *n_
     try {
         LayerPlan L;
         plan_stripes(n_tensors, n_values, chunk_syms, effective_sub_syms(chunk_syms, sub_syms), shared_table != 0, L);
-        *scratch_bytes = scratch_layout(L.stripes.size(), L.n_tables, count_subs(L)).total;
+        *scratch_bytes = scratch_layout(L.stripes.size(), L.n_tables, count_chunks(L)).total;
         return K3HUF_OK;
     } catch (const std::bad_alloc &) {
         return K3HUF_E_NOMEM;
@@ -297,25 +404,25 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         LayerPlan L;
         plan_stripes(n_tensors, n_values, chunk_syms, sub_syms, shared_table != 0, L);
         const size_t ns = L.stripes.size();
-        const uint64_t n_subs = count_subs(L);
-        if (ns > 65535 || n_subs > 0xFFFFFFFFull) return K3HUF_E_ARG;
-        const ScratchLayout SL = scratch_layout(ns, L.n_tables, n_subs);
+        const uint64_t n_chunks = count_chunks(L);
+        if (ns > 65535 || n_chunks > 0xFFFFFFFFull) return K3HUF_E_ARG;
+        const ScratchLayout SL = scratch_layout(ns, L.n_tables, n_chunks);
         if (scratch_bytes < SL.total) return K3HUF_E_ARG;
         uint8_t *scr = static_cast<uint8_t *>(d_scratch);
         EncParams P{};
         P.stripes = reinterpret_cast<const EncStripe *>(scr + SL.stripes);
         P.counts = reinterpret_cast<uint32_t *>(scr + SL.counts);
         P.codes = reinterpret_cast<const uint32_t *>(scr + SL.codes);
-        P.sub_bits = reinterpret_cast<uint32_t *>(scr + SL.sub_bits);
-        P.sub_start = reinterpret_cast<uint32_t *>(scr + SL.sub_start);
+        P.chunk_bits = reinterpret_cast<uint32_t *>(scr + SL.chunk_bits);
+        P.chunk_start = reinterpret_cast<uint32_t *>(scr + SL.chunk_start);
         P.flag = reinterpret_cast<uint32_t *>(scr + SL.flag);
         P.chunk_syms = chunk_syms;
         P.sub_syms = sub_syms;
         P.S = chunk_syms / sub_syms;
 
         std::vector<EncStripe> desc(ns);
-        uint32_t max_n = 0, max_sub = 0;
-        uint64_t sub_begin = 0;
+        uint32_t max_n = 0, max_chunks = 0;
+        uint64_t chunk_begin = 0;
         for (size_t i = 0; i < ns; ++i) {
             const PlanStripe &p = L.stripes[i];
             EncStripe &d = desc[i];
@@ -323,10 +430,10 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
             d.n = uint32_t(p.n);
             d.n_chunks = p.n_chunks;
             d.table = p.table;
-            d.sub_begin = uint32_t(sub_begin);
-            sub_begin += uint64_t(p.n_chunks) * P.S;
+            d.chunk_begin = uint32_t(chunk_begin);
+            chunk_begin += p.n_chunks;
             max_n = std::max(max_n, d.n);
-            max_sub = std::max(max_sub, p.n_chunks * P.S);
+            max_chunks = std::max(max_chunks, p.n_chunks);
         }
         // 1. histograms
         cudaError_t e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
@@ -369,9 +476,10 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         if (e == cudaSuccess) e = cudaMemsetAsync(blob, 0, size_t(L.total), st);
         if (e == cudaSuccess) e = cudaMemcpyAsync(blob, head.data(), head.size(), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return cuda_fail(e);
-        // 3-5. bit counts, indexes, packing
-        const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_sub + kPackThreads - 1) / kPackThreads));
-        sub_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+        // 3-5. chunk bits, chunk index, packing
+        const uint32_t wpb = kPackThreads / 32;
+        const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_chunks + wpb - 1) / wpb));
+        chunk_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
         scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
         pack_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);

@@ -56,8 +56,13 @@ def test_noalloc_encoder_matches_scratch_encoder_on_two_calls(noalloc):
 
 
 def test_noalloc_encoder_refuses_layers_beyond_its_scratch(noalloc):
-    """2^31 values need more than the fixed 32 MiB: refused before any CUDA call."""
-    nv = (ctypes.c_uint64 * 1)(1 << 31)
+    """A layer whose scratch exceeds the fixed 32 MiB is refused before any
+    CUDA call.  The tensor pointer is a placeholder that must never reach the
+    device, so the size is checked first: the call is made only when the
+    scratch the layer needs is known to be larger than the fixed array."""
+    n = 1 << 35
+    assert k3.encode_scratch_bytes([n]) > 32 << 20
+    nv = (ctypes.c_uint64 * 1)(n)
     ptrs = (ctypes.c_void_p * 1)(1 << 20)
     size = ctypes.c_size_t(0)
     assert noalloc(1, ptrs, nv, 4096, 256, 0, None, 0, ctypes.byref(size), None) == k3.E_ARG
