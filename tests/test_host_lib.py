@@ -232,9 +232,10 @@ def test_encode_scratch_bytes():
     small = k3.encode_scratch_bytes([4096])
     big = k3.encode_scratch_bytes([1 << 26])
     assert 0 < small < big
-    # per sub-stream: two u32 words; 2^26 values in 256-value sub-streams
-    assert big >= 2 * 4 * (1 << 26) // 256
-    assert k3.encode_scratch_bytes([1 << 26], sub_syms=512) < big
+    # per chunk: two u32 words (its bits and its first bit); 2^26 values in 4096-value chunks
+    assert big >= 2 * 4 * (1 << 26) // 4096
+    assert k3.encode_scratch_bytes([1 << 26], chunk_syms=1024) > big
+    assert k3.encode_scratch_bytes([1 << 26], sub_syms=512) == big
     with pytest.raises(k3.K3HufError) as e:
         k3.encode_scratch_bytes([0])
     assert e.value.code == k3.E_ARG
