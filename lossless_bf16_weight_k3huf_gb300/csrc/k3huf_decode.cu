@@ -57,20 +57,27 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kItem = 32;                     // sub-streams per work item (one warp)
 constexpr int kRound = 64;                    // values per lane between merges
 constexpr int kRowBytes = 64;                 // per-lane row: one round of high bytes (8-byte units, swizzled)
-constexpr uint32_t kBitBuf = 7744;            // bytes of staged bit stream per warp and pass
+constexpr uint32_t kBitBuf = 5056;            // bytes of staged bit stream per warp and pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
 constexpr int kMaxHeavy = 64;                 // items listed for the first sweep of a table phase
 
-// Lockstep table, indexed by the next 12 bits: exactly kPer whole codes.
+// Lockstep table, indexed by the next lock_bits(kPer) bits (14 for two codes
+// per lookup, 12 for one): exactly kPer whole codes.
 //   [4:0] bits used by the kPer codes (the shift, taken straight from the
 //   entry by a wrapping funnel shift) [23:16] first symbol [31:24] second
 //   symbol.  0 in [4:0] when the window does not hold kPer whole codes: then
-//   [11:8] is the first code's length (0: no code starts here) and the
-//   second code is read from the single-code table.
-// Single-code table: the 4096-entry (sym << 4) | length table.
-constexpr size_t kSmemLut = 4096 * sizeof(uint32_t);
+//   [11:8] is the first code's length and the second code is read from the
+//   single-code table.
+// Single-code table: the 4096-entry (sym << 4) | length table, indexed by
+// the next 12 bits.
+// A window where no code starts decodes as symbol 0 of length 1 with
+// kBadCode set (bit 12 in both tables): the decoder ORs the entries it
+// falls back on into one word and tests that bit once per pass.
+constexpr uint32_t kBadCode = 1u << 12;
+template <int kPer> __host__ __device__ constexpr int lock_bits() { return kPer == 2 ? 14 : 12; }
+constexpr size_t kSmemLut = (size_t(1) << 14) * sizeof(uint32_t);
 constexpr size_t kSmemL12 = 4096 * sizeof(uint16_t);
 constexpr size_t kWarpSlot = kBitBuf + 16 + size_t(32) * kRowBytes;   // bits + rows of one warp
 constexpr size_t kSmemBytes = kSmemLut + kSmemL12 + size_t(kWarps) * kWarpSlot;
@@ -314,27 +321,31 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
         uint32_t l = 0;
 #pragma unroll
         for (int j = L; j >= 1; --j) l = (e >= lo[j] && e < hi[j]) ? uint32_t(j) : l;
-        uint32_t val = 0;
+        uint32_t val = kBadCode | 1u;
         if (l) val = (uint32_t(s_sorted[s_adj[l] + int32_t(e >> (L - l))]) << 4) | l;
         lut1[e] = uint16_t(val);
     }
     __syncthreads();
-    // lockstep table: exactly kPer codes inside the 12-bit window
-    for (uint32_t e = tid; e < 4096u; e += kThreads) {
-        const uint32_t a = lut1[e];
+    // lockstep table: exactly kPer codes inside the window.  The second code
+    // is looked up on the window's bits after the first code with zeros
+    // after the window's end; a code that fits in the window's bits is
+    // found the same way whatever those bits are
+    constexpr int W = lock_bits<kPer>();
+    for (uint32_t e = tid; e < (1u << W); e += kThreads) {
+        const uint32_t a = lut1[e >> (W - L)];
         const uint32_t l1 = a & 15u;
-        uint32_t ent = 0;
-        if (l1 != 0) {
-            if (kPer == 1) {
-                ent = ((a >> 4) << 16) | l1;
-            } else {
-                const uint32_t b = lut1[(e << l1) & 4095u];
-                const uint32_t l2 = b & 15u;
-                if (l2 != 0 && l1 + l2 <= K3HUF_MAXLEN)
-                    ent = ((a >> 4) << 16) | ((b >> 4) << 24) | (l1 + l2);
-                else
-                    ent = ((a >> 4) << 16) | (l1 << 8);        // second code read separately
-            }
+        uint32_t ent;
+        if (a & kBadCode) {
+            ent = kBadCode | (1u << 8);                            // read by the fallback
+        } else if (kPer == 1) {
+            ent = ((a >> 4) << 16) | l1;
+        } else {
+            const uint32_t b = lut1[((e << l1) & ((1u << W) - 1u)) >> (W - L)];
+            const uint32_t l2 = b & 15u;
+            if (!(b & kBadCode) && l1 + l2 <= uint32_t(W))
+                ent = ((a >> 4) << 16) | ((b >> 4) << 24) | (l1 + l2);
+            else
+                ent = ((a >> 4) << 16) | (l1 << 8);                // second code read separately
         }
         lut[e] = ent;
     }
@@ -614,6 +625,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     gb.init(reinterpret_cast<const uint4 *>(bits), reinterpret_cast<const uint4 *>(even) - 1, c_off);
                 uint32_t bad = 0;
 
+                constexpr int kW = lock_bits<kPer>();
                 // rounds: the same number for every lane of the warp
                 const uint32_t wlen = __reduce_max_sync(0xffffffffu, len);
                 const uint32_t n_rounds = (wlen + kRound - 1) / kRound;
@@ -626,12 +638,12 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     lo = __funnelshift_l(w2, w1, cur);
                 };
                 // one code from the 12-bit single-code table; an undecodable
-                // window gives symbol 0 and one bit, and raises `bad`
+                // window gives symbol 0 and one bit, and sets kBadCode in `bad`.
+                // The symbol's bit 8 carries that flag: callers keep the low byte
                 auto single = [&](uint32_t win, uint32_t &len_out) -> uint32_t {
                     const uint32_t a = lut1[win >> 20];
-                    const uint32_t l = a & 15u;
-                    bad |= l == 0;
-                    len_out = l + (l == 0);
+                    bad |= a;
+                    len_out = a & 15u;
                     return a >> 4;
                 };
 
@@ -658,35 +670,38 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             uint32_t ek[4];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                uint32_t e = lut[hi >> 20];
+                                uint32_t e = lut[hi >> (32 - kW)];
                                 uint32_t t = e & 31u;
                                 // a whole-pair entry shifts the window by its low five bits
                                 uint32_t nhi = __funnelshift_l(lo, hi, e), nlo = __funnelshift_l(0u, lo, e);
-                                {
-                                    if (t == 0u) {
-                                        // the window does not hold kPer whole codes: take the
-                                        // first code from the entry, read the second one alone.
-                                        // The 64-bit window must still cover this lookup (up to
-                                        // 24 bits) and the group's remaining normal lookups (up
-                                        // to 12 bits each): reload it when it might not
-                                        if (cur - cur0 > 4u + 12u * uint32_t(k)) {
-                                            window(cur, hi, lo);
-                                            cur0 = cur;
-                                        }
-                                        uint32_t l = (e >> 8) & 15u;
-                                        bad |= l == 0;
-                                        l += l == 0;
-                                        uint32_t syms = e & 0x00FF0000u;
-                                        nhi = __funnelshift_l(lo, hi, l);
-                                        nlo = lo << l;
-                                        t = l;
-                                        if (kPer == 2) {
-                                            syms |= single(nhi, l) << 24;
-                                            t += l;
-                                            nhi = __funnelshift_l(nlo, nhi, l);
-                                            nlo <<= l;
-                                        }
-                                        e = syms;
+                                if (t == 0u) {
+                                    // the window does not hold kPer whole codes: take the
+                                    // first code from the entry, read the second one alone.
+                                    // The 64-bit window must cover these codes (up to 12
+                                    // bits each) ...
+                                    if (cur - cur0 > 64u - 12u * kPer) {
+                                        window(cur, hi, lo);
+                                        cur0 = cur;
+                                    }
+                                    const uint32_t l = (e >> 8) & 15u;
+                                    bad |= e;
+                                    uint32_t syms = e & 0x00FF0000u;
+                                    nhi = __funnelshift_l(lo, hi, l);
+                                    nlo = lo << l;
+                                    t = l;
+                                    if (kPer == 2) {
+                                        uint32_t l2;
+                                        syms |= single(nhi, l2) << 24;
+                                        t += l2;
+                                        nhi = __funnelshift_l(nlo, nhi, l2);
+                                        nlo <<= l2;
+                                    }
+                                    e = syms;
+                                    // ... and afterwards the group's remaining lookups (kW
+                                    // bits each): reload it when it might not
+                                    if (k < 3 && cur + t - cur0 > 64u - uint32_t(kW) * uint32_t(3 - k)) {
+                                        window(cur + t, nhi, nlo);
+                                        cur0 = cur + t;
                                     }
                                 }
                                 hi = nhi;
@@ -802,7 +817,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
 
                 uint32_t st = 0;
                 if (len) {
-                    if (bad) st |= K3HUF_ST_BADCODE;
+                    if (bad & kBadCode) st |= K3HUF_ST_BADCODE;
                     const uint32_t pos = kStaged ? bp + byte_lo * 8u : gb.position();
                     if (my_off > huff_bits || my_end > huff_bits) st |= K3HUF_ST_OVERRUN;
                     if (pos != my_end) st |= K3HUF_ST_INDEX;

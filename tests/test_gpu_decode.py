@@ -93,6 +93,18 @@ def test_degenerate_planes(variant):
     check_parity([workloads.uniform_bytes(300_000)], variant)
 
 
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_long_code_pairs(variant):
+    """One value in 32 carries a 12-bit code, so pairs that miss the lockstep
+    window (and pairs of two 12-bit codes, 24 bits) come often, at every
+    position of the four-lookup group."""
+    x = workloads.dyadic_long_codes((1 << 20) + 4099)
+    blob = check_parity([x], variant)
+    lens = oracle.code_lengths(oracle.histogram(x))
+    assert lens.max() == 12 and (lens == 12).sum() >= 100
+    check_parity([x[: 300_001]], variant, sub_syms=64)
+
+
 def test_limiter_fired_alphabet():
     x = workloads.heavy_tail(n=1 << 22)
     blob = check_parity([x])

@@ -199,6 +199,16 @@ def test_uniform_bytes_all_symbols():
     assert (h["tables"][0] > 0).all()
 
 
+def test_dyadic_plane_gets_dyadic_lengths():
+    # symbol probabilities 2^-l give Huffman lengths l exactly (the entropy
+    # bound is met with equality), here 1, 2, 3, 4, 6, 6 and 128 codes of 12
+    x = workloads.dyadic_long_codes(1 << 19)
+    blob, h = roundtrip([x])
+    check_layout(blob, [x])
+    lens = h["tables"][0].astype(int)
+    assert sorted(lens[lens > 0].tolist()) == [1, 2, 3, 4, 6, 6] + [12] * 128
+
+
 def test_heavy_tail_sample_fires_limiter():
     x = workloads.heavy_tail(n=1 << 21)
     cnt = oracle.histogram(x)

@@ -158,6 +158,19 @@ def uniform_bytes(n: int, seed: int = 102) -> np.ndarray:
     return np.random.default_rng(seed).integers(0, 1 << 16, n).astype(np.uint16)
 
 
+def dyadic_long_codes(n: int, seed: int = 104) -> np.ndarray:
+    """High bytes drawn with dyadic probabilities: four symbols of probability
+    1/2, 1/4, 1/8, 1/16, two of 1/64 and 128 of 1/4096, so that about 3% of
+    the values carry the rarest symbols and about one pair in a thousand
+    consecutive values is two of them; random low bytes."""
+    r = np.random.default_rng(seed)
+    probs = np.array([2.0 ** -1, 2.0 ** -2, 2.0 ** -3, 2.0 ** -4] + [2.0 ** -6] * 2 + [2.0 ** -12] * 128)
+    syms = r.permutation(256)[: probs.size]
+    hi = syms[r.choice(probs.size, n, p=probs / probs.sum())].astype(np.uint16)
+    lo = r.integers(0, 256, n).astype(np.uint16)
+    return ((hi << 8) | lo).astype(np.uint16)
+
+
 def geometric_exponent_symbols(n: int, alpha: float, seed: int = 103) -> np.ndarray:
     """Integers k with P(k) = (1-q)/(1+q) q^|k|, q = 2^-alpha (two-sided
     geometric law of a floating-point exponent), via the difference of two
