@@ -160,6 +160,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// 4-byte global -> shared copy that lands asynchronously (cp.async), and
+// the wait for all of this thread's such copies
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -266,7 +275,9 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
         if (my_len > uint32_t(L)) atomicOr(&s_badlen, 1u);
         const uint32_t same = __match_any_sync(0xffffffffu, ls);
         rank_in = __popc(same & ((1u << lane) - 1u));
-#pragma unroll
+        // (rolled loops in this code that runs once per table: fresh
+        // instructions cost an instruction-cache fill each)
+#pragma unroll 1
         for (int j = 1; j <= L; ++j) {
             const uint32_t bj = __ballot_sync(0xffffffffu, ls == uint32_t(j));
             if (lane == j) s_wcnt[warp][j] = __popc(bj);
@@ -277,13 +288,14 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
         // lane l (1..12): counts of length l before each warp, and in total
         uint32_t c = 0;
         if (lane >= 1 && lane <= L) {
-#pragma unroll
+#pragma unroll 1
             for (int w = 0; w < 8; ++w) {
                 s_wbase[w][lane] = c;
                 c += s_wcnt[w][lane];
             }
         }
         uint32_t code = 0, kraft = 0, first_l = 0;
+#pragma unroll 1
         for (int l = L; l >= 1; --l) {
             const uint32_t cnt = __shfl_sync(0xffffffffu, c, l);
             if (lane == l) first_l = code;
@@ -292,7 +304,7 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
         }
         // offsets of each length in the sorted list (ascending length)
         uint32_t incl = c;                                      // inclusive scan over lanes 1..12
-#pragma unroll
+#pragma unroll 1
         for (int d = 1; d < 16; d <<= 1) {
             const uint32_t v = __shfl_up_sync(0xffffffffu, incl, d);
             if (lane >= d) incl += v;
@@ -330,34 +342,45 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
     // is looked up on the window's bits after the first code with zeros
     // after the window's end; a code that fits in the window's bits is
     // found the same way whatever those bits are
+    // Four consecutive entries per thread and step, stored as one 16-byte
+    // word; with a 14-bit window they share their first code.
     constexpr int W = lock_bits<kPer>();
-    for (uint32_t e = tid; e < (1u << W); e += kThreads) {
-        const uint32_t a = lut1[e >> (W - L)];
-        const uint32_t l1 = a & 15u;
-        uint32_t ent;
-        if (a & kBadCode) {
-            ent = kBadCode | (1u << 8);                            // read by the fallback
-        } else if (kPer == 1) {
-            ent = ((a >> 4) << 16) | l1;
-        } else {
-            const uint32_t b = lut1[((e << l1) & ((1u << W) - 1u)) >> (W - L)];
-            const uint32_t l2 = b & 15u;
-            if (!(b & kBadCode) && l1 + l2 <= uint32_t(W))
-                ent = ((a >> 4) << 16) | ((b >> 4) << 24) | (l1 + l2);
-            else
-                ent = ((a >> 4) << 16) | (l1 << 8);                // second code read separately
+    for (uint32_t m = tid; m < (1u << W) / 4; m += kThreads) {
+        const uint32_t a0 = lut1[(4 * m) >> (W - L)];
+        uint32_t v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t e = 4 * m + uint32_t(i);
+            const uint32_t a = W - L >= 2 ? a0 : lut1[e >> (W - L)];
+            const uint32_t l1 = a & 15u;
+            uint32_t ent;
+            if (a & kBadCode) {
+                ent = kBadCode | (1u << 8);                        // read by the fallback
+            } else if (kPer == 1) {
+                ent = ((a >> 4) << 16) | l1;
+            } else {
+                const uint32_t b = lut1[((e << l1) & ((1u << W) - 1u)) >> (W - L)];
+                const uint32_t l2 = b & 15u;
+                if (!(b & kBadCode) && l1 + l2 <= uint32_t(W))
+                    ent = ((a >> 4) << 16) | ((b >> 4) << 24) | (l1 + l2);
+                else
+                    ent = ((a >> 4) << 16) | (l1 << 8);            // second code read separately
+            }
+            v[i] = ent;
         }
-        lut[e] = ent;
+        reinterpret_cast<uint4 *>(lut)[m] = make_uint4(v[0], v[1], v[2], v[3]);
     }
     __syncthreads();
     return true;
 }
 
-__device__ __forceinline__ uint32_t find_task(const DecodeParams &P, uint32_t item) {
-    uint32_t lo = 0, hi = P.n_tasks - 1;
+// The stripe task holding work item `item` (tasks: the launch's table, in
+// shared memory)
+__device__ __forceinline__ uint32_t find_task(const StripeTask *task, uint32_t n_tasks, uint32_t item) {
+    uint32_t lo = 0, hi = n_tasks - 1;
     while (lo < hi) {
         const uint32_t mid = (lo + hi + 1) >> 1;
-        if (P.task[mid].item_begin <= item) lo = mid; else hi = mid - 1;
+        if (task[mid].item_begin <= item) lo = mid; else hi = mid - 1;
     }
     return lo;
 }
@@ -366,8 +389,8 @@ __device__ __forceinline__ uint32_t find_task(const DecodeParams &P, uint32_t it
 // chunk offsets) overflow one staging pass.  Such items take two or more
 // passes and are started first.  Deterministic in the container bytes, so
 // every warp classifies an item the same way; reads stay inside the stripe.
-__device__ bool item_heavy(const DecodeParams &P, uint32_t wi) {
-    const StripeTask &T = P.task[find_task(P, wi)];
+__device__ bool item_heavy(const DecodeParams &P, const StripeTask *task, uint32_t wi) {
+    const StripeTask &T = task[find_task(task, P.n_tasks, wi)];
     const uint32_t cs = P.chunk_syms, S = cs / P.sub_syms;
     const uint32_t nch = (T.n_values + cs - 1) / cs;
     if (uint64_t(K3HUF_STRIPE_HDR_BYTES) + 4ull * nch > T.stripe_bytes) return false;
@@ -383,10 +406,9 @@ __device__ bool item_heavy(const DecodeParams &P, uint32_t wi) {
 __device__ __forceinline__ uint32_t interleave_lo(uint32_t even4, uint32_t hi4) { return __byte_perm(even4, hi4, 0x5140); }
 __device__ __forceinline__ uint32_t interleave_hi(uint32_t even4, uint32_t hi4) { return __byte_perm(even4, hi4, 0x7362); }
 
-// Validate the device copy of a stripe header against the launch's view of it.
-__device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, uint32_t hdr[8]) {
-    const uint32_t *h = reinterpret_cast<const uint32_t *>(T.stripe);
-    for (int i = 0; i < 8; ++i) hdr[i] = h[i];
+// Validate the device copy of a stripe header (its eight words in hdr)
+// against the launch's view of it.
+__device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, const uint32_t hdr[8]) {
     const uint32_t n = T.n_values, cs = P.chunk_syms, ss = P.sub_syms;
     const uint32_t nch = (n + cs - 1) / cs;
     const uint64_t huff_bits = uint64_t(hdr[4]) | (uint64_t(hdr[5]) << 32);
@@ -412,6 +434,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     __shared__ uint32_t s_nheavy, s_next;
     __shared__ uint32_t s_hdr[kMaxTasks][8];     // stripe headers, validated once per CTA
     __shared__ uint8_t s_hok[kMaxTasks];
+    __shared__ __align__(16) StripeTask s_task[kMaxTasks];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint8_t *wslot = smem + kSmemLut + kSmemL12 + size_t(warp) * kWarpSlot;
@@ -430,22 +453,35 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         mbar_init(&s_bar[warp]);
         fence_proxy_async();
     }
-    for (uint32_t u = uint32_t(tid); u < P.n_tasks; u += kThreads) {
-        uint32_t h[8];
-        s_hok[u] = stripe_header_ok(P, P.task[u], h) ? 1 : 0;
-        for (int i = 0; i < 8; ++i) s_hdr[u][i] = h[i];
+    // the task table in shared memory (the prologue indexes it differently
+    // in every lane, which parameter space serialises): warp w copies tasks
+    // w, w + kWarps, ... one word per lane
+    {
+        constexpr uint32_t kWords = sizeof(StripeTask) / 4;
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(P.task);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(s_task);
+        for (uint32_t u = uint32_t(warp); u < P.n_tasks; u += kWarps)
+            if (uint32_t(lane) < kWords) dst[u * kWords + lane] = src[u * kWords + lane];
     }
-    // (the first phase's barrier publishes the headers and the mbarriers)
+    __syncthreads();
+    // stripe headers: copied now (thread u: task u), checked once the first
+    // table is built
+    const bool hown = uint32_t(tid) < P.n_tasks;
+    if (hown) {
+        const uint32_t *h = reinterpret_cast<const uint32_t *>(s_task[tid].stripe);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cp_async4(&s_hdr[tid][i], h + i);
+    }
 
     // the CTA's items in phases of one code table each
     uint32_t item = it0;
     while (item < it1) {                              // CTA-uniform
-        const uint32_t ti0 = find_task(P, item);
-        const int table = P.tables ? int(P.task[ti0].table) : 0;
+        const uint32_t ti0 = find_task(s_task, P.n_tasks, item);
+        const int table = P.tables ? int(s_task[ti0].table) : 0;
         uint32_t pend = it1;
-        for (uint32_t u = ti0 + 1; u < P.n_tasks && P.task[u].item_begin < it1; ++u)
-            if (P.tables && int(P.task[u].table) != table) {
-                pend = P.task[u].item_begin;
+        for (uint32_t u = ti0 + 1; u < P.n_tasks && s_task[u].item_begin < it1; ++u)
+            if (P.tables && int(s_task[u].table) != table) {
+                pend = s_task[u].item_begin;
                 break;
             }
         // the phase's global reads go out before the barrier: the code
@@ -458,13 +494,17 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         for (uint32_t k = 0; k < 32u; ++k) {
             const uint32_t i = item + uint32_t(tid) + k * kThreads;
             if (i >= pend) break;
-            if (item_heavy(P, i)) hmask |= 1u << k;
+            if (item_heavy(P, s_task, i)) hmask |= 1u << k;
         }
         __syncthreads();                              // every warp done with the previous table
         if (rebuild) {
             table_bad = !build_tables<kPer>(my_len, lut1, lut);
             table_built = table;
             if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
+        }
+        if (item == it0 && hown) {                    // published by the next barrier
+            cp_async_wait_all();
+            s_hok[tid] = stripe_header_ok(P, s_task[tid], s_hdr[tid]) ? 1 : 0;
         }
         if (tid == 0) {
             s_nheavy = 0;
@@ -479,7 +519,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 if (k < kMaxHeavy) s_heavy[k] = item + uint32_t(tid) + uint32_t(__ffs(hmask) - 1) * kThreads;
             }
             for (uint32_t i = item + uint32_t(tid) + 32u * kThreads; i < pend; i += kThreads)
-                if (item_heavy(P, i)) {
+                if (item_heavy(P, s_task, i)) {
                     const uint32_t k = atomicAdd(&s_nheavy, 1u);
                     if (k < kMaxHeavy) s_heavy[k] = i;
                 }
@@ -501,7 +541,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 for (uint32_t k = uint32_t(lane); k < nheavy; k += 32) listed |= s_heavy[k] == wi;
                 if (__any_sync(0xffffffffu, listed)) continue;       // taken in the first sweep
             }
-            const uint32_t ti = find_task(P, wi);
+            const uint32_t ti = find_task(P.task, P.n_tasks, wi);   // warp-uniform: parameter reads
             const StripeTask &T = P.task[ti];
             uint32_t hdr[8];
             for (int i = 0; i < 8; ++i) hdr[i] = s_hdr[ti][i];
