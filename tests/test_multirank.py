@@ -41,3 +41,15 @@ def test_max_over_ranks_and_whole_job_value():
     # two ranks, 256 MiB each, 10 steps in 20 ms
     assert bench.whole_job_gbs(1 << 28, 2, 10, 20.0) == pytest.approx(2 * 10 * (1 << 28) / 0.020 / 1e9)
     assert bench.max_over_ranks(3.0, torch.device("cpu"), 1) == 3.0
+
+
+def test_cpu_baseline_parallel_fields():
+    """The all-core oracle baseline reports the threads it ran and the
+    values it decoded (a 4-stripe layer cut to a few chunks per stripe)."""
+    import bench
+    import oracle
+    import workloads
+    blob = oracle.encode_layer([workloads.normal_tensor((3, 4096 * 64 + 5), 0.02, seed=5)])
+    r = bench.cpu_baseline_parallel(blob, budget_s=5.0, threads=3)
+    assert r["cores"] == 3 and r["kind"] == "oracle" and r["value"] > 0
+    assert r["sample"].startswith("193 chunks of 4096 values")
