@@ -695,6 +695,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 const uint8_t *const even_p0 = even + size_t(g0 + q) * ss + sub * 8u;
                 const size_t pstride = size_t(4) * ss;
 
+                // staged words rw_i .. rw_i + 2 held in registers from one group to
+                // the next: a lane moves on by 0-2 words per group, so most groups
+                // load one word, and their first lookup starts from registers
+                // (the fused GEMV, short of registers, reloads all three)
+                uint32_t rw_i = 0u - 8u, rw0 = 0, rw1 = 0, rw2 = 0;
                 for (uint32_t r = 0; r < n_rounds; ++r) {
                     const uint32_t rem = len > r * kRound ? len - r * kRound : 0u;
                     uint8_t *row = wrows + size_t(lane) * kRowBytes;
@@ -703,10 +708,30 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     if (kStaged && full) {
                         // lockstep round: every lookup yields exactly kPer codes, so
                         // each group of 4 lookups fills 4 * kPer bytes at a fixed place
-#pragma unroll 4
+#pragma unroll(kGemv ? 4 : 2)                    // (4 or 8 for decode: more code, slower)
                         for (int grp = 0; grp < kRound / (4 * kPer); ++grp) {
                             uint32_t cur = bp, cur0 = bp, hi, lo;
-                            window(cur, hi, lo);
+                            if (kGemv) {
+                                window(cur, hi, lo);           // (no registers to spare)
+                            } else {
+                                const uint32_t i = min(cur >> 5, max_word);
+                                const uint32_t d = i - rw_i;        // words moved since the last group
+                                const uint32_t n2 = bitbuf[i + 2];
+                                uint32_t n1 = rw2, n0 = rw1;
+                                if (d >= 2) n1 = bitbuf[i + 1];
+                                if (d >= 3) n0 = bitbuf[i];
+                                if (d == 2) n0 = rw2;
+                                if (d == 0) {
+                                    n0 = rw0;
+                                    n1 = rw1;
+                                }
+                                rw0 = n0;
+                                rw1 = n1;
+                                rw2 = n2;
+                                rw_i = i;
+                                hi = __funnelshift_l(n1, n0, cur);
+                                lo = __funnelshift_l(n2, n1, cur);
+                            }
                             uint32_t ek[4];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
