@@ -733,12 +733,17 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                                 lo = __funnelshift_l(n2, n1, cur);
                             }
                             uint32_t ek[4];
+                            uint32_t e_next = lut[hi >> (32 - kW)];
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
-                                uint32_t e = lut[hi >> (32 - kW)];
+                                uint32_t e = e_next;
                                 uint32_t t = e & 31u;
                                 // a whole-pair entry shifts the window by its low five bits
                                 uint32_t nhi = __funnelshift_l(lo, hi, e), nlo = __funnelshift_l(0u, lo, e);
+                                // the next lookup goes out before the fallback test (and is
+                                // redone after a fallback), which keeps the test and its
+                                // branch off the chain of dependent lookups
+                                if (k < 3) e_next = lut[nhi >> (32 - kW)];
                                 if (t == 0u) {
                                     // the window does not hold kPer whole codes: take the
                                     // first code from the entry, read the second one alone.
@@ -768,6 +773,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                                         window(cur + t, nhi, nlo);
                                         cur0 = cur + t;
                                     }
+                                    if (k < 3) e_next = lut[nhi >> (32 - kW)];
                                 }
                                 hi = nhi;
                                 lo = nlo;
