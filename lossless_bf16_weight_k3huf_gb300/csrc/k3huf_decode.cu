@@ -328,14 +328,30 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
         hi[j] = s_hi[j];
     }
     __syncthreads();
-    // single-code 12-bit table: the shortest length whose range holds the window
-    for (uint32_t e = tid; e < 4096u; e += kThreads) {
+    // single-code 12-bit table: the shortest length whose range holds the
+    // window.  Eight windows per thread and step, stored as one 16-byte word:
+    // a code of 9 bits or fewer owns an aligned range of at least 8 windows,
+    // so when the block's first window falls in one, the whole block does
+    auto entry1 = [&](uint32_t e) -> uint32_t {
         uint32_t l = 0;
 #pragma unroll
         for (int j = L; j >= 1; --j) l = (e >= lo[j] && e < hi[j]) ? uint32_t(j) : l;
-        uint32_t val = kBadCode | 1u;
-        if (l) val = (uint32_t(s_sorted[s_adj[l] + int32_t(e >> (L - l))]) << 4) | l;
-        lut1[e] = uint16_t(val);
+        return l ? (uint32_t(s_sorted[s_adj[l] + int32_t(e >> (L - l))]) << 4) | l : (kBadCode | 1u);
+    };
+    for (uint32_t m = tid; m < 4096u / 8; m += kThreads) {
+        const uint32_t v0 = entry1(8 * m);
+        uint32_t w[4];
+        if (!(v0 & kBadCode) && (v0 & 15u) <= uint32_t(L - 3)) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = v0 | (v0 << 16);
+        } else {
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t lo16 = i ? entry1(8 * m + 2 * i) : v0;
+                w[i] = lo16 | (entry1(8 * m + 2 * i + 1) << 16);
+            }
+        }
+        reinterpret_cast<uint4 *>(lut1)[m] = make_uint4(w[0], w[1], w[2], w[3]);
     }
     __syncthreads();
     // lockstep table: exactly kPer codes inside the window.  The second code
@@ -343,13 +359,18 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
     // after the window's end; a code that fits in the window's bits is
     // found the same way whatever those bits are
     // Four consecutive entries per thread and step, stored as one 16-byte
-    // word; with a 14-bit window they share their first code.
+    // word; with a 14-bit window they share their first code, and when the
+    // first entry's pair uses 12 bits or fewer, all four are that entry.
     constexpr int W = lock_bits<kPer>();
     for (uint32_t m = tid; m < (1u << W) / 4; m += kThreads) {
         const uint32_t a0 = lut1[(4 * m) >> (W - L)];
         uint32_t v[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+            if (W - L >= 2 && i > 0 && (v[0] & 31u) != 0 && (v[0] & 31u) <= uint32_t(L)) {
+                v[i] = v[0];
+                continue;
+            }
             const uint32_t e = 4 * m + uint32_t(i);
             const uint32_t a = W - L >= 2 ? a0 : lut1[e >> (W - L)];
             const uint32_t l1 = a & 15u;
