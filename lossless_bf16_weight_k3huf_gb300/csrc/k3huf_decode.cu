@@ -444,7 +444,10 @@ __device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, con
     return ok;
 }
 
-template <int kPer, bool kVec, bool kStaged, bool kGemv>
+// kFixed: the container's default sizes (chunks of 4096 values, sub-streams
+// of 256) as compile-time constants, so that sub-stream and piece offsets
+// fold into immediates and divisions by them into shifts
+template <int kPer, bool kVec, bool kStaged, bool kGemv, bool kFixed = false>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -462,7 +465,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     uint32_t *bitbuf = reinterpret_cast<uint32_t *>(wslot);
     uint8_t *wrows = wslot + kBitBuf + 16;
 
-    const uint32_t cs = P.chunk_syms, ss = P.sub_syms, S = cs / ss;
+    const uint32_t cs = kFixed ? 4096u : P.chunk_syms, ss = kFixed ? 256u : P.sub_syms, S = cs / ss;
     // contiguous item ranges whose sizes differ by at most one
     const uint32_t it0 = uint32_t(uint64_t(blockIdx.x) * P.n_items / gridDim.x);
     const uint32_t it1 = uint32_t(uint64_t(blockIdx.x + 1) * P.n_items / gridDim.x);
@@ -929,7 +932,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     }
 }
 
-template <int kPer, bool kVec, bool kStaged, bool kGemv = false>
+template <int kPer, bool kVec, bool kStaged, bool kGemv = false, bool kFixed = false>
 int launch(DecodeParams &P, cudaStream_t stream) {
     static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
     static int grid_max[kMaxDevices] = {};
@@ -940,12 +943,12 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         return K3HUF_E_CUDA;
     }
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged, kGemv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged, kGemv, kFixed>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(kSmemBytes));
         int sms = 0, per_sm = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged, kGemv>, kThreads,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged, kGemv, kFixed>, kThreads,
                                                               kSmemBytes);
         if (e != cudaSuccess) {
             set_cuda_error(int(e));
@@ -955,7 +958,7 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         attr_set[dev] = true;
     }
     const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(grid_max[dev]));
-    decode_kernel<kPer, kVec, kStaged, kGemv><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    decode_kernel<kPer, kVec, kStaged, kGemv, kFixed><<<grid, kThreads, kSmemBytes, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_cuda_error(int(e));
@@ -972,6 +975,8 @@ int launch_syms(DecodeParams &P, cudaStream_t stream) {
     const bool vec = P.sub_syms % 8 == 0;
     // a sub-stream's bits (at most 12 per value) must fit the shared buffer
     const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= kBitBuf;
+    if constexpr (kPer == 2)
+        if (staged && P.chunk_syms == 4096 && P.sub_syms == 256) return launch<2, true, true, false, true>(P, stream);
     if (staged) return vec ? launch<kPer, true, true>(P, stream) : launch<kPer, false, true>(P, stream);
     return vec ? launch<kPer, true, false>(P, stream) : launch<kPer, false, false>(P, stream);
 }
@@ -980,7 +985,9 @@ int launch_syms(DecodeParams &P, cudaStream_t stream) {
 int launch_gemv(DecodeParams &P, cudaStream_t stream) {
     switch (g_per) {
         case 1: return launch<1, true, true, true>(P, stream);
-        default: return launch<2, true, true, true>(P, stream);
+        default:
+            if (P.chunk_syms == 4096 && P.sub_syms == 256) return launch<2, true, true, true, true>(P, stream);
+            return launch<2, true, true, true>(P, stream);
     }
 }
 
