@@ -195,7 +195,8 @@ int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tensors, const u
  *  Needs: cols divides the tensor's values and is a multiple of 32 x
  *    sub_syms (every work item lies in one row), sub_syms a multiple of 8
  *    with 32 / (chunk_syms / sub_syms) whole, and sub-streams short enough
- *    to stage (sub_syms x 12 / 8 + 64 <= 7744): K3HUF_E_ARG otherwise.
+ *    to stage (sub_syms x 12 / 8 + 64 <= 5056, so sub_syms <= 2048 for
+ *    powers of two): K3HUF_E_ARG otherwise.
  * Asynchronous on `stream`; stream faults set bits in *d_status. */
 int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
                      uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status, void *stream);

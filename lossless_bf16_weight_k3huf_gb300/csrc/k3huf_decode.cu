@@ -23,12 +23,15 @@
 //  - one persistent CTA of 16 warps per SM takes a contiguous item range and
 //    rebuilds the code table only when it changes; inside a table phase the
 //    warps take items from a shared counter, multi-pass items first;
-//  - every lockstep lookup emits exactly two codes from a 12-bit
-//    double-symbol table (a window that does not hold two whole codes gives
-//    the first code and the second is read from the single-code table), so
-//    all lanes of the warp advance by the same number of values per step and
-//    never diverge; the window is a funnel shift of three shared words,
-//    reloaded every four lookups;
+//  - every lockstep lookup emits exactly two codes from a double-symbol
+//    table indexed by the next 14 bits (the codes stay 12-bit limited; the
+//    wider window halves the pairs that do not fit): a window that does not
+//    hold two whole codes gives the first code and the second is read from
+//    the 12-bit single-code table, so all lanes of the warp advance by the
+//    same number of values per step.  The 64-bit window is a funnel shift
+//    of three stream words kept in registers from one group of four lookups
+//    to the next, and each lookup's successor is issued before the
+//    fallback test;
 //  - a round's 64 high bytes per lane are built in registers and stored to a
 //    per-lane row in shared memory; every 64 values the warp merges its 32
 //    sub-streams' high bytes with their raw low bytes (loads issued one round
