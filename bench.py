@@ -340,6 +340,7 @@ def main():
     d_blob = torch.from_numpy(blob).to(dev)
     d_out = torch.empty(info["out_bytes"], dtype=torch.uint8, device=dev)
     d_st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device=dev)   # pool of the last items
     stream = torch.cuda.Stream(device=dev)
     launches_per_step = -(-info["n_stripes"] // 64)
     l2_note = ("inputs larger than L2" if info["blob_bytes"] + info["out_bytes"] > 2 * L2_BYTES
@@ -350,7 +351,7 @@ def main():
     def step():
         if flush is not None:
             flush.fill_(1)
-        k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream)
+        k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream, work=d_work)
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -380,7 +381,7 @@ def main():
                 if flush is not None:
                     flush.fill_(1)
                 ev[i][0].record(stream)
-                k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream)
+                k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream, work=d_work)
                 ev[i][1].record(stream)
             t_end.record(stream)
         stream.synchronize()
@@ -412,6 +413,8 @@ def main():
                    "blob_bytes": info["blob_bytes"], "compression_ratio": round(raw / info["blob_bytes"], 4),
                    "compression_rate": round(info["blob_bytes"] / raw, 4), "stripes": info["n_stripes"],
                    "chunk_syms": info["chunk_syms"], "sub_syms": info["sub_syms"], "decoder": ["2 codes/lookup", "1 code/lookup", "2 codes/lookup"][args.variant],
+                   "call": "k3huf_decode_layer_ws (8-byte work area: the last sixteenth of each CTA's items "
+                           "pooled when the layer has one code table)",
                    "l2": l2_note, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
@@ -443,6 +446,7 @@ def bench_e2e(k3, blob, hdr, info, dev, stream, steps):
     d_blob = [torch.empty(blob.size, dtype=torch.uint8, device=dev) for _ in range(2)]
     d_out = [torch.empty(info["out_bytes"], dtype=torch.uint8, device=dev) for _ in range(2)]
     d_st = torch.zeros(1, dtype=torch.int32, device=dev)
+    d_work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device=dev)   # pool of the last items
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_dec = [torch.cuda.Event() for _ in range(2)]
@@ -459,7 +463,7 @@ def bench_e2e(k3, blob, hdr, info, dev, stream, steps):
             stream.wait_event(ev_in[b])
             if i >= 2:
                 stream.wait_event(ev_out[b])          # copy-out i-2 finished reading d_out[b]
-            k3.decode_layer(hdr, d_blob[b], d_out[b], d_st, stream=stream)
+            k3.decode_layer(hdr, d_blob[b], d_out[b], d_st, stream=stream, work=d_work)
             ev_dec[b].record(stream)
             s_out.wait_event(ev_dec[b])
             with torch.cuda.stream(s_out):

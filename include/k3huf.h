@@ -140,6 +140,29 @@ int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes,
                        void *d_out, size_t out_bytes,
                        uint32_t *d_status, void *stream);
 
+/* Bytes of the work area of k3huf_decode_layer_ws. */
+#define K3HUF_WORK_BYTES 8
+
+/* k3huf_decode_layer with a work area that spreads the end of each launch
+ * over all CTAs.  Not from the article: its decoder is a scalar loop per
+ * stripe.  With fixed item ranges the launch ends with the CTAs whose items
+ * were heaviest; here, in launches whose stripes share one code table, the
+ * last sixteenth of every CTA's range goes to a pool that CTAs draw from
+ * once their own items are taken (launches over several tables, and
+ * containers without the default 4096 / 256 chunk and sub-stream sizes,
+ * decode as k3huf_decode_layer does).
+ *  d_work / work_bytes: device memory, 4-byte aligned, >= K3HUF_WORK_BYTES,
+ *    all zero before the first call; every launch leaves it zero.  The
+ *    caller owns it and must not give it to two launches that may run at
+ *    the same time (on two streams, or in graphs that may run together).
+ *  Other arguments as for k3huf_decode_layer; the output is the same bytes.
+ * Errors: K3HUF_E_ARG for a null, unaligned or short work area, else as
+ * k3huf_decode_layer. */
+int k3huf_decode_layer_ws(const void *h_layer_hdr, size_t hdr_bytes,
+                          const void *d_layer, size_t layer_bytes,
+                          void *d_out, size_t out_bytes,
+                          uint32_t *d_status, void *d_work, size_t work_bytes, void *stream);
+
 /* Decode one stripe on the GPU (the article's per-stripe decode).
  *  codelen: host copy of the stripe's table (validated with k3huf_build);
  *  chunk_syms, sub_syms: values per indexed chunk and per sub-stream, as

@@ -106,6 +106,8 @@ struct DecodeParams {
     const uint8_t *gemv_x;      // fused GEMV: device bf16 x[cols], or null
     float *gemv_y;              // fused GEMV: device y[rows], accumulated
     uint64_t gemv_cols;
+    uint32_t *work;             // single-table launches with a work area: [0] the shared
+                                // pool's next slot, [1] CTAs finished (both left zero), or null
     StripeTask task[kMaxTasks];
 };
 
@@ -450,7 +452,7 @@ __device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, con
 // kFixed: the container's default sizes (chunks of 4096 values, sub-streams
 // of 256) as compile-time constants, so that sub-stream and piece offsets
 // fold into immediates and divisions by them into shifts
-template <int kPer, bool kVec, bool kStaged, bool kGemv, bool kFixed = false>
+template <int kPer, bool kVec, bool kStaged, bool kGemv, bool kFixed = false, bool kPool = false>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -472,6 +474,18 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     // contiguous item ranges whose sizes differ by at most one
     const uint32_t it0 = uint32_t(uint64_t(blockIdx.x) * P.n_items / gridDim.x);
     const uint32_t it1 = uint32_t(uint64_t(blockIdx.x + 1) * P.n_items / gridDim.x);
+    // kPool (a work area, one code table in the launch): the last sixteenth
+    // of every CTA's range goes to a pool that all CTAs draw from, round-robin
+    // over the CTAs, once their own items are taken: fixed ranges leave the
+    // CTAs whose items happen to be heavier finishing last.  (A quarter or an
+    // eighth pooled was slower: multi-pass items in the pool start late.)
+    const bool pool = kPool && P.work != nullptr;
+    auto tail_of = [&](uint32_t b) -> uint32_t {            // first pool item of CTA b's range
+        const uint32_t a0 = uint32_t(uint64_t(b) * P.n_items / gridDim.x);
+        const uint32_t a1 = uint32_t(uint64_t(b + 1) * P.n_items / gridDim.x);
+        return a1 - ((a1 - a0) >> 4);
+    };
+    const uint32_t it_own = pool ? tail_of(blockIdx.x) : it1;
     int table_built = -1;
     bool table_bad = false, dead = false;
     uint32_t phase = 0;
@@ -514,13 +528,14 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         // the phase's global reads go out before the barrier: the code
         // lengths of a new table, and which of the phase's items take more
         // than one pass (bit k: item item + tid + k * kThreads)
+        const uint32_t pend_own = min(pend, it_own);
         const bool rebuild = table != table_built;
         uint32_t my_len = 0;
         if (rebuild && tid < 256) my_len = (P.tables ? P.tables + 256ull * table : P.inline_table)[tid];
         uint32_t hmask = 0;
         for (uint32_t k = 0; k < 32u; ++k) {
             const uint32_t i = item + uint32_t(tid) + k * kThreads;
-            if (i >= pend) break;
+            if (i >= pend_own) break;
             if (item_heavy(P, s_task, i)) hmask |= 1u << k;
         }
         __syncthreads();                              // every warp done with the previous table
@@ -545,7 +560,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 const uint32_t k = atomicAdd(&s_nheavy, 1u);
                 if (k < kMaxHeavy) s_heavy[k] = item + uint32_t(tid) + uint32_t(__ffs(hmask) - 1) * kThreads;
             }
-            for (uint32_t i = item + uint32_t(tid) + 32u * kThreads; i < pend; i += kThreads)
+            for (uint32_t i = item + uint32_t(tid) + 32u * kThreads; i < pend_own; i += kThreads)
                 if (item_heavy(P, s_task, i)) {
                     const uint32_t k = atomicAdd(&s_nheavy, 1u);
                     if (k < kMaxHeavy) s_heavy[k] = i;
@@ -562,11 +577,31 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             if (v < nheavy) {
                 wi = s_heavy[v];
             } else {
-                if (v - nheavy >= pend - item) break;
-                wi = item + (v - nheavy);
-                bool listed = false;
-                for (uint32_t k = uint32_t(lane); k < nheavy; k += 32) listed |= s_heavy[k] == wi;
-                if (__any_sync(0xffffffffu, listed)) continue;       // taken in the first sweep
+                if (v - nheavy >= pend_own - item) {
+                    if (!pool || pend != it1) break;
+                    // the pool: slot p is item k = p / grid of CTA (p % grid)'s last
+                    // sixteenth; slots past a shorter one are skipped
+                    const uint32_t max_tail = ((P.n_items / gridDim.x + 1u) >> 4) + 1u;
+                    wi = ~0u;
+                    for (;;) {
+                        uint32_t p = 0;
+                        if (lane == 0) p = atomicAdd(P.work, 1u);
+                        p = __shfl_sync(0xffffffffu, p, 0);
+                        const uint32_t b = p % gridDim.x, k = p / gridDim.x;
+                        if (k >= max_tail) break;
+                        const uint32_t a1 = uint32_t(uint64_t(b + 1) * P.n_items / gridDim.x);
+                        if (tail_of(b) + k < a1) {
+                            wi = tail_of(b) + k;
+                            break;
+                        }
+                    }
+                    if (wi == ~0u) break;
+                } else {
+                    wi = item + (v - nheavy);
+                    bool listed = false;
+                    for (uint32_t k = uint32_t(lane); k < nheavy; k += 32) listed |= s_heavy[k] == wi;
+                    if (__any_sync(0xffffffffu, listed)) continue;   // taken in the first sweep
+                }
             }
             const uint32_t ti = find_task(P.task, P.n_tasks, wi);   // warp-uniform: parameter reads
             const StripeTask &T = P.task[ti];
@@ -933,9 +968,21 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         }
         item = pend;
     }
+    // the last CTA to finish returns the work area to zero for the next launch
+    if (pool) {
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            if (atomicAdd(P.work + 1, 1u) == gridDim.x - 1u) {
+                atomicExch(P.work, 0u);
+                atomicExch(P.work + 1, 0u);
+                __threadfence();
+            }
+        }
+    }
 }
 
-template <int kPer, bool kVec, bool kStaged, bool kGemv = false, bool kFixed = false>
+template <int kPer, bool kVec, bool kStaged, bool kGemv = false, bool kFixed = false, bool kPool = false>
 int launch(DecodeParams &P, cudaStream_t stream) {
     static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
     static int grid_max[kMaxDevices] = {};
@@ -946,12 +993,12 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         return K3HUF_E_CUDA;
     }
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged, kGemv, kFixed>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(kSmemBytes));
         int sms = 0, per_sm = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged, kGemv, kFixed>, kThreads,
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool>, kThreads,
                                                               kSmemBytes);
         if (e != cudaSuccess) {
             set_cuda_error(int(e));
@@ -961,7 +1008,7 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         attr_set[dev] = true;
     }
     const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(grid_max[dev]));
-    decode_kernel<kPer, kVec, kStaged, kGemv, kFixed><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool><<<grid, kThreads, kSmemBytes, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_cuda_error(int(e));
@@ -979,7 +1026,10 @@ int launch_syms(DecodeParams &P, cudaStream_t stream) {
     // a sub-stream's bits (at most 12 per value) must fit the shared buffer
     const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= kBitBuf;
     if constexpr (kPer == 2)
-        if (staged && P.chunk_syms == 4096 && P.sub_syms == 256) return launch<2, true, true, false, true>(P, stream);
+        if (staged && P.chunk_syms == 4096 && P.sub_syms == 256)
+            return P.work ? launch<2, true, true, false, true, true>(P, stream)
+                          : launch<2, true, true, false, true>(P, stream);
+    P.work = nullptr;                                    // (the pool has the default sizes only)
     if (staged) return vec ? launch<kPer, true, true>(P, stream) : launch<kPer, false, true>(P, stream);
     return vec ? launch<kPer, true, false>(P, stream) : launch<kPer, false, false>(P, stream);
 }
@@ -1022,8 +1072,9 @@ extern "C" int k3huf_set_decoder_variant(int variant) {
     return K3HUF_OK;
 }
 
-extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
-                                  void *d_out, size_t out_bytes, uint32_t *d_status, void *stream) {
+namespace {
+int decode_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes, void *d_out,
+                      size_t out_bytes, uint32_t *d_status, uint32_t *d_work, void *stream) {
     if (!h_layer_hdr || !d_layer || !d_out || !d_status) return K3HUF_E_ARG;
     if (!aligned16(d_layer) || !aligned16(d_out) || (reinterpret_cast<uintptr_t>(d_status) & 3u)) return K3HUF_E_ARG;
     Layer L;
@@ -1054,10 +1105,28 @@ extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, con
             items += items_of(e.n_values, P.chunk_syms, P.sub_syms);
         }
         P.n_items = items;
+        // the work pool needs one code table across the launch
+        bool one_table = true;
+        for (uint32_t u = 1; u < P.n_tasks; ++u) one_table &= P.task[u].table == P.task[0].table;
+        P.work = one_table ? d_work : nullptr;
         rc = launch_tasks(P, static_cast<cudaStream_t>(stream));
         if (rc) return rc;
     }
     return K3HUF_OK;
+}
+}  // namespace
+
+extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                                  void *d_out, size_t out_bytes, uint32_t *d_status, void *stream) {
+    return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status, nullptr, stream);
+}
+
+extern "C" int k3huf_decode_layer_ws(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                                     void *d_out, size_t out_bytes, uint32_t *d_status, void *d_work, size_t work_bytes,
+                                     void *stream) {
+    if (!d_work || work_bytes < K3HUF_WORK_BYTES || (reinterpret_cast<uintptr_t>(d_work) & 3u)) return K3HUF_E_ARG;
+    return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status,
+                             static_cast<uint32_t *>(d_work), stream);
 }
 
 extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms, uint32_t sub_syms,

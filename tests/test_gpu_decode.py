@@ -105,6 +105,28 @@ def test_long_code_pairs(variant):
     check_parity([x[: 300_001]], variant, sub_syms=64)
 
 
+def test_work_pool_parity_and_reset():
+    """With a work area the last sixteenth of every CTA's items is shared: the
+    output is the same bytes, the area is zero again after every launch, and
+    layers over several tables (which skip the pool) decode the same way."""
+    one = [workloads.normal_tensor((1 << 25,), 0.02, seed=21)]           # 4096 items: ~27 per CTA, one pooled
+    several = [workloads.normal_tensor((1 << 21,), 0.02, seed=22), workloads.uniform_bytes(1 << 20, seed=23)]
+    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for tensors in (one, several):
+        blob = oracle.encode_layer(tensors)
+        info = k3.layer_info(blob)
+        d_blob = torch.from_numpy(blob).cuda()
+        ref = torch.from_numpy(oracle.decode_layer(blob)[1]).cuda()
+        for _ in range(3):
+            d_out = torch.zeros(info["out_bytes"], dtype=torch.uint8, device="cuda")
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, d_out, st, work=work)
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0
+            assert torch.equal(d_out, ref)
+            assert int(work.abs().sum().item()) == 0
+
+
 def test_limiter_fired_alphabet():
     x = workloads.heavy_tail(n=1 << 22)
     blob = check_parity([x])
