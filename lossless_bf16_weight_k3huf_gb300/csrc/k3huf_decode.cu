@@ -22,7 +22,8 @@
 //    long for the slot is decoded in passes over prefixes of its lanes;
 //  - one persistent CTA of 16 warps per SM takes a contiguous item range and
 //    rebuilds the code table only when it changes; inside a table phase the
-//    warps take items from a shared counter, multi-pass items first;
+//    warps take items from a shared counter, multi-pass items first (with a
+//    work area, the last sixteenth of every range is pooled across CTAs);
 //  - every lockstep lookup emits exactly two codes from a double-symbol
 //    table indexed by the next 14 bits (the codes stay 12-bit limited; the
 //    wider window halves the pairs that do not fit): a window that does not
@@ -259,7 +260,9 @@ struct GlobalBits {
 //    [first[l] << (12 - l), (first[l] + count[l]) << (12 - l)), disjoint
 //    across lengths, so every window finds its length by comparisons and its
 //    symbol by one index into the sorted list;
-//  - each lockstep entry reads the single-code table twice.
+//  - a lockstep entry reads the single-code table for each of its two codes
+//    (a block of four entries shares the first read, and fills all four
+//    from one pair of at most 12 bits).
 template <int kPer>
 __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
     constexpr int L = K3HUF_MAXLEN;
