@@ -281,34 +281,46 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(EncParams P) {
                 }
             }
             p += my;
-            // the lane's bits, assembled in a register: words wholly inside the
-            // lane's range are its own (plain stores); the first and the last
-            // word may be shared with the neighbouring lanes (atomic ORs)
+            // the lane's bits (at most 96), assembled without a branch per code:
+            // codes 0-3 and 4-7 left-aligned in two 64-bit words (at most 48
+            // bits each), joined into one 128-bit string and shifted to the
+            // lane's first bit.  Words wholly inside the lane's range are its
+            // own (plain stores); the first and the last may be shared with
+            // the neighbouring lanes (atomic ORs)
             {
                 const uint32_t q0 = p - my - win * 32u;            // window-relative first bit
-                uint32_t w = q0 >> 5, nb = q0 & 31u;
-                uint64_t acc = 0;
+                const uint32_t s0 = q0 & 31u, w0 = q0 >> 5;
+                uint64_t A = 0, B = 0;
+                uint32_t la = 0, lb = 0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     const uint32_t l = e[i] & 15u;
-                    acc = (acc << l) | (e[i] >> 4);
-                    nb += l;
-                    if (nb >= 32) {
-                        nb -= 32;
-                        const uint32_t word = uint32_t(acc >> nb);
-                        if (w == (q0 >> 5) && (q0 & 31u))
-                            atomicOr(&stage[w], word);                 // shared with the previous lane
+                    la += l;
+                    if (l) A |= uint64_t(e[i] >> 4) << (64u - la);
+                }
+#pragma unroll
+                for (int i = 4; i < 8; ++i) {
+                    const uint32_t l = e[i] & 15u;
+                    lb += l;
+                    if (l) B |= uint64_t(e[i] >> 4) << (64u - lb);
+                }
+                // A then B (la >= 1 whenever the lane has a code: value 0 comes first)
+                const uint64_t s_hi = la ? A | (B >> la) : B;
+                const uint64_t s_lo = la ? B << (64u - la) : 0u;
+                const uint32_t t0 = uint32_t(s_hi >> 32), t1 = uint32_t(s_hi), t2 = uint32_t(s_lo >> 32),
+                               t3 = uint32_t(s_lo);
+                const uint32_t x[4] = {t0 >> s0, __funnelshift_r(t1, t0, s0), __funnelshift_r(t2, t1, s0),
+                                       __funnelshift_r(t3, t2, s0)};
+                const uint32_t nw = my ? (s0 + my + 31u) >> 5 : 0u;   // at most 4
+#pragma unroll
+                for (uint32_t k = 0; k < 4; ++k) {
+                    if (k < nw) {
+                        if (k == 0 || k + 1 == nw)
+                            atomicOr(&stage[w0 + k], x[k]);
                         else
-                            stage[w] = word;
-                        ++w;
-                        acc &= (uint64_t(1) << nb) - 1;
+                            stage[w0 + k] = x[k];
                     }
                 }
-                // the pending word holds lane bits beyond its leading offset (the
-                // offset is only there while no word was emitted): it may be
-                // shared with the next lane, and with the previous one
-                const bool real = w == (q0 >> 5) ? nb > (q0 & 31u) : nb > 0;
-                if (real) atomicOr(&stage[w], uint32_t(acc << (32 - nb)));
             }
             if (nv) {
                 if (vec && nv == 8 && (v & 7u) == 0) {
