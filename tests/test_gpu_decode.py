@@ -267,6 +267,33 @@ def test_fault_random_bitstream(seed):
     assert _decode_device_copy(blob, bad) != 0
 
 
+def test_fault_random_bitstream_pooled():
+    """A corrupt stretch of the bit stream of a layer large enough that every
+    CTA pools items (the work-area instantiation): a status bit, the guard
+    bytes intact, and the work area zero again after each launch."""
+    blob = oracle.encode_layer([workloads.normal_tensor((1 << 25,), 0.02, 31)])
+    info = k3.layer_info(blob)
+    o = _stripe0(blob)
+    bits_off = int.from_bytes(blob[o + 24:o + 28].tobytes(), "little")
+    even_off = int.from_bytes(blob[o + 28:o + 32].tobytes(), "little")
+    bad = blob.copy()
+    rng = np.random.default_rng(31)
+    lo = bits_off + (even_off - bits_off) * 15 // 16         # inside the last, pooled, items
+    hi = even_off - 64                                        # the stream's padding stays zero
+    bad[lo:hi] = rng.integers(0, 256, hi - lo, dtype=np.uint8)
+    d_blob = torch.from_numpy(bad).cuda()
+    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        buf = torch.full((info["out_bytes"] + 2 * GUARD,), SENTINEL, dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, buf[GUARD:GUARD + info["out_bytes"]], st, work=work)
+        torch.cuda.synchronize()
+        h = buf.cpu().numpy()
+        assert (h[:GUARD] == SENTINEL).all() and (h[GUARD + info["out_bytes"]:] == SENTINEL).all()
+        assert int(st.item()) & (k3.ST_BADCODE | k3.ST_INDEX)
+        assert int(work.abs().sum().item()) == 0
+
+
 def test_host_side_errors_raise():
     blob = oracle.encode_layer([workloads.tiny()])
     info = k3.layer_info(blob)
