@@ -242,7 +242,7 @@ def cpu_baseline_parallel(blob, budget_s=10.0, threads=None):
         raise RuntimeError(f"oracle decode failed: {state['rc']}")
     return {"value": round(2 * state["values"] / dt / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{state['chunks']} chunks of {cs} values ({2 * state['values'] / 2**20:.1f} MiB decoded) "
-                      f"in {dt:.1f} s, bit-serial oracle decoder, {threads} threads over stripe-interleaved "
+                      f"in {dt:.3f} s, bit-serial oracle decoder, {threads} threads over stripe-interleaved "
                       f"64-chunk blocks"}
 
 
