@@ -413,8 +413,8 @@ def main():
                    "blob_bytes": info["blob_bytes"], "compression_ratio": round(raw / info["blob_bytes"], 4),
                    "compression_rate": round(info["blob_bytes"] / raw, 4), "stripes": info["n_stripes"],
                    "chunk_syms": info["chunk_syms"], "sub_syms": info["sub_syms"], "decoder": ["2 codes/lookup", "1 code/lookup", "2 codes/lookup"][args.variant],
-                   "call": "k3huf_decode_layer_ws (8-byte work area: the last sixteenth of each CTA's items "
-                           "pooled when the layer has one code table)",
+                   "call": "k3huf_decode_layer_ws (work area: the last sixteenth of each CTA's items pooled "
+                           "across the CTAs)",
                    "l2": l2_note, "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",

@@ -141,16 +141,17 @@ int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes,
                        uint32_t *d_status, void *stream);
 
 /* Bytes of the work area of k3huf_decode_layer_ws. */
-#define K3HUF_WORK_BYTES 8
+#define K3HUF_WORK_BYTES 68
 
 /* k3huf_decode_layer with a work area that spreads the end of each launch
  * over all CTAs.  Not from the article: its decoder is a scalar loop per
  * stripe.  With fixed item ranges the launch ends with the CTAs whose items
- * were heaviest; here, in launches whose stripes share one code table, the
- * last sixteenth of every CTA's range goes to a pool that CTAs draw from
- * once their own items are taken (launches over several tables, and
- * containers without the default 4096 / 256 chunk and sub-stream sizes,
- * decode as k3huf_decode_layer does).
+ * were heaviest; here the last sixteenth of every CTA's range goes to the
+ * pool of the CTAs whose ranges end in the same code table.  CTAs draw from
+ * their own pool once their own items are taken, then from any pool with
+ * items left, rebuilding their tables for it.  Containers without the
+ * default 4096 / 256 chunk and sub-stream sizes, and launches of more than
+ * 160 CTAs or 16 pools, decode as k3huf_decode_layer does.
  *  d_work / work_bytes: device memory, 4-byte aligned, >= K3HUF_WORK_BYTES,
  *    all zero before the first call; every launch leaves it zero.  The
  *    caller owns it and must not give it to two launches that may run at

@@ -251,7 +251,7 @@ def encode_layer_gpu(tensors, chunk_syms: int = 4096, sub_syms: int = 256, share
     return blob
 
 
-WORK_BYTES = 8
+WORK_BYTES = 68
 
 
 def decode_layer(hdr, d_layer, d_out, d_status, stream=None, layer_bytes: int | None = None,

@@ -66,6 +66,8 @@ constexpr int kMaxTasks = 64;                 // stripes per launch (kernel para
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
 constexpr int kMaxHeavy = 64;                 // items listed for the first sweep of a table phase
+constexpr int kMaxPoolCtas = 160;             // pooled launches: CTAs, and pools (runs of CTAs whose
+constexpr int kMaxPools = 16;                 // ranges end in one code table)
 
 // Lockstep table, indexed by the next lock_bits(kPer) bits (14 for two codes
 // per lookup, 12 for one): exactly kPer whole codes.
@@ -107,10 +109,16 @@ struct DecodeParams {
     const uint8_t *gemv_x;      // fused GEMV: device bf16 x[cols], or null
     float *gemv_y;              // fused GEMV: device y[rows], accumulated
     uint64_t gemv_cols;
-    uint32_t *work;             // single-table launches with a work area: [0] the shared
-                                // pool's next slot, [1] CTAs finished (both left zero), or null
+    uint32_t *work;             // work area: [0] CTAs finished, [1 + j] next slot of pool j
+                                // (all left zero), or null
+    uint32_t n_pools;
+    uint32_t pool_table[kMaxPools];     // code table of pool j's items
+    uint16_t pool_cta[kMaxPools + 1];   // pool j: CTAs pool_cta[j] .. pool_cta[j + 1] - 1
+    uint16_t pool_tail[kMaxPools];      // most items in one CTA's share of pool j
+    uint32_t tail_begin[kMaxPoolCtas];  // CTA b's pooled items: tail_begin[b] .. the end of its range
     StripeTask task[kMaxTasks];
 };
+static_assert(sizeof(DecodeParams) <= 4096, "kernel parameters");
 
 __device__ __forceinline__ uint32_t bswap32(uint32_t x) { return __byte_perm(x, 0, 0x0123); }
 
@@ -464,6 +472,9 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     __shared__ __align__(8) uint64_t s_bar[kWarps];
     __shared__ uint32_t s_heavy[kMaxHeavy];
     __shared__ uint32_t s_nheavy, s_next;
+    __shared__ int s_pick;
+    __shared__ uint32_t s_dead;                  // some warp stopped (a timed-out copy)
+    __shared__ uint32_t s_empty;                 // bit j: pool j found empty by a warp of this CTA
     __shared__ uint32_t s_hdr[kMaxTasks][8];     // stripe headers, validated once per CTA
     __shared__ uint8_t s_hok[kMaxTasks];
     __shared__ __align__(16) StripeTask s_task[kMaxTasks];
@@ -477,18 +488,32 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     // contiguous item ranges whose sizes differ by at most one
     const uint32_t it0 = uint32_t(uint64_t(blockIdx.x) * P.n_items / gridDim.x);
     const uint32_t it1 = uint32_t(uint64_t(blockIdx.x + 1) * P.n_items / gridDim.x);
-    // kPool (a work area, one code table in the launch): the last sixteenth
-    // of every CTA's range goes to a pool that all CTAs draw from, round-robin
-    // over the CTAs, once their own items are taken: fixed ranges leave the
-    // CTAs whose items happen to be heavier finishing last.  (A quarter or an
+    // kPool (a work area): the last sixteenth of every CTA's range (inside
+    // its last table phase) goes to the pool of the CTAs whose ranges end in
+    // the same code table.  CTAs draw from their own pool, round-robin over
+    // its CTAs, once their own items are taken, then from any pool with items
+    // left (rebuilding their tables for it): fixed ranges leave the CTAs
+    // whose items happen to be heavier finishing last.  (A quarter or an
     // eighth pooled was slower: multi-pass items in the pool start late.)
     const bool pool = kPool && P.work != nullptr;
-    auto tail_of = [&](uint32_t b) -> uint32_t {            // first pool item of CTA b's range
-        const uint32_t a0 = uint32_t(uint64_t(b) * P.n_items / gridDim.x);
-        const uint32_t a1 = uint32_t(uint64_t(b + 1) * P.n_items / gridDim.x);
-        return a1 - ((a1 - a0) >> 4);
+    const uint32_t it_own = pool ? P.tail_begin[blockIdx.x] : it1;
+    uint32_t j_me = 0;
+    if (pool)
+        while (j_me + 1 < P.n_pools && P.pool_cta[j_me + 1] <= blockIdx.x) ++j_me;
+    // the next item of pool j for this warp, or ~0u once the pool is empty
+    // (slot p: item p / n of CTA pool_cta[j] + p % n's share)
+    auto pool_grab = [&](uint32_t j) -> uint32_t {
+        const uint32_t c0 = P.pool_cta[j], nb = uint32_t(P.pool_cta[j + 1]) - c0, max_tail = P.pool_tail[j];
+        for (;;) {
+            uint32_t p = 0;
+            if (lane == 0) p = atomicAdd(P.work + 1 + j, 1u);
+            p = __shfl_sync(0xffffffffu, p, 0);
+            const uint32_t b = c0 + p % nb, k = p / nb;
+            if (k >= max_tail) return ~0u;
+            const uint32_t a1 = uint32_t(uint64_t(b + 1) * P.n_items / gridDim.x);
+            if (P.tail_begin[b] + k < a1) return P.tail_begin[b] + k;
+        }
     };
-    const uint32_t it_own = pool ? tail_of(blockIdx.x) : it1;
     int table_built = -1;
     bool table_bad = false, dead = false;
     uint32_t phase = 0;
@@ -496,6 +521,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     if (lane == 0) {
         mbar_init(&s_bar[warp]);
         fence_proxy_async();
+    }
+    if (tid == 0) {
+        s_dead = 0;
+        s_empty = 0;
     }
     // the task table in shared memory (the prologue indexes it differently
     // in every lane, which parameter space serialises): warp w copies tasks
@@ -519,19 +548,45 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
 
     // the CTA's items in phases of one code table each
     uint32_t item = it0;
-    while (item < it1) {                              // CTA-uniform
-        const uint32_t ti0 = find_task(s_task, P.n_tasks, item);
-        const int table = P.tables ? int(s_task[ti0].table) : 0;
-        uint32_t pend = it1;
-        for (uint32_t u = ti0 + 1; u < P.n_tasks && s_task[u].item_begin < it1; ++u)
-            if (P.tables && int(s_task[u].table) != table) {
-                pend = s_task[u].item_begin;
-                break;
+    int steal = -1;                                   // pool drained after the CTA's own range
+    for (;;) {                                        // CTA-uniform
+        int table;
+        uint32_t pend;
+        if (item < it1) {
+            const uint32_t ti0 = find_task(s_task, P.n_tasks, item);
+            table = P.tables ? int(s_task[ti0].table) : 0;
+            pend = it1;
+            for (uint32_t u = ti0 + 1; u < P.n_tasks && s_task[u].item_begin < it1; ++u)
+                if (P.tables && int(s_task[u].table) != table) {
+                    pend = s_task[u].item_begin;
+                    break;
+                }
+        } else {
+            if (!pool || P.n_pools == 1) break;       // (one pool: drained in the last phase)
+            // a pool with items left, the CTA's own first; none once a warp of
+            // the CTA has stopped
+            if (dead && lane == 0) atomicOr(&s_dead, 1u);
+            __syncthreads();
+            if (tid == 0) {
+                int pick = -1;
+                for (uint32_t q = 0; q < P.n_pools && pick < 0 && !s_dead; ++q) {
+                    const uint32_t j = (j_me + q) % P.n_pools;
+                    if ((s_empty >> j) & 1u) continue;       // (slots only grow)
+                    const uint32_t size = (uint32_t(P.pool_cta[j + 1]) - P.pool_cta[j]) * uint32_t(P.pool_tail[j]);
+                    if (atomicAdd(P.work + 1 + j, 0u) < size) pick = int(j);
+                }
+                s_pick = pick;
             }
+            __syncthreads();
+            steal = s_pick;
+            if (steal < 0) break;
+            table = P.tables ? int(P.pool_table[steal]) : 0;
+            pend = item;                              // no own items in this phase
+        }
         // the phase's global reads go out before the barrier: the code
         // lengths of a new table, and which of the phase's items take more
         // than one pass (bit k: item item + tid + k * kThreads)
-        const uint32_t pend_own = min(pend, it_own);
+        const uint32_t pend_own = steal >= 0 ? item : min(pend, it_own);
         const bool rebuild = table != table_built;
         uint32_t my_len = 0;
         if (rebuild && tid < 256) my_len = (P.tables ? P.tables + 256ull * table : P.inline_table)[tid];
@@ -547,6 +602,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             table_built = table;
             if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
         }
+        if (steal >= 0 && table_bad) break;           // (CTA-uniform) its items cannot be taken
         if (item == it0 && hown) {                    // published by the next barrier
             cp_async_wait_all();
             s_hok[tid] = stripe_header_ok(P, s_task[tid], s_hdr[tid]) ? 1 : 0;
@@ -581,24 +637,15 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 wi = s_heavy[v];
             } else {
                 if (v - nheavy >= pend_own - item) {
-                    if (!pool || pend != it1) break;
-                    // the pool: slot p is item k = p / grid of CTA (p % grid)'s last
-                    // sixteenth; slots past a shorter one are skipped
-                    const uint32_t max_tail = ((P.n_items / gridDim.x + 1u) >> 4) + 1u;
-                    wi = ~0u;
-                    for (;;) {
-                        uint32_t p = 0;
-                        if (lane == 0) p = atomicAdd(P.work, 1u);
-                        p = __shfl_sync(0xffffffffu, p, 0);
-                        const uint32_t b = p % gridDim.x, k = p / gridDim.x;
-                        if (k >= max_tail) break;
-                        const uint32_t a1 = uint32_t(uint64_t(b + 1) * P.n_items / gridDim.x);
-                        if (tail_of(b) + k < a1) {
-                            wi = tail_of(b) + k;
-                            break;
-                        }
+                    // own items taken: the pool being drained, or the CTA's own
+                    // pool after its last phase
+                    const int j = steal >= 0 ? steal : (pool && pend == it1 ? int(j_me) : -1);
+                    if (j < 0) break;
+                    wi = pool_grab(uint32_t(j));
+                    if (wi == ~0u) {
+                        if (lane == 0) atomicOr(&s_empty, 1u << j);
+                        break;
                     }
-                    if (wi == ~0u) break;
                 } else {
                     wi = item + (v - nheavy);
                     bool listed = false;
@@ -976,13 +1023,44 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         __syncthreads();
         if (tid == 0) {
             __threadfence();
-            if (atomicAdd(P.work + 1, 1u) == gridDim.x - 1u) {
-                atomicExch(P.work, 0u);
-                atomicExch(P.work + 1, 0u);
+            if (atomicAdd(P.work, 1u) == gridDim.x - 1u) {
+                for (uint32_t j = 0; j <= P.n_pools; ++j) atomicExch(P.work + j, 0u);
                 __threadfence();
             }
         }
     }
+}
+
+// Pools of a launch of `grid` CTAs over P's items: CTA b's pooled items are
+// the last sixteenth of its range, kept inside its last table phase (the
+// run of same-table stripes holding its last item); consecutive CTAs whose
+// last phases share a table form one pool.  False when the launch has more
+// CTAs or pools than the parameters hold.
+bool pool_setup(DecodeParams &P, uint32_t grid) {
+    if (grid > uint32_t(kMaxPoolCtas)) return false;
+    uint32_t n_pools = 0;
+    for (uint32_t b = 0; b < grid; ++b) {
+        const uint32_t a0 = uint32_t(uint64_t(b) * P.n_items / grid), a1 = uint32_t(uint64_t(b + 1) * P.n_items / grid);
+        uint32_t t = 0;
+        while (t + 1 < P.n_tasks && P.task[t + 1].item_begin <= a1 - 1) ++t;
+        const uint32_t table = P.tables ? P.task[t].table : 0u;
+        uint32_t run = t;
+        while (run > 0 && P.tables && P.task[run - 1].table == table) --run;
+        const uint32_t phase0 = std::max(a0, P.task[run].item_begin);
+        const uint32_t tail = std::max(a1 - ((a1 - a0) >> 4), phase0);
+        P.tail_begin[b] = tail;
+        if (b == 0 || P.pool_table[n_pools - 1] != table) {
+            if (n_pools == uint32_t(kMaxPools)) return false;
+            P.pool_table[n_pools] = table;
+            P.pool_cta[n_pools] = uint16_t(b);
+            P.pool_tail[n_pools] = 0;
+            ++n_pools;
+        }
+        P.pool_tail[n_pools - 1] = uint16_t(std::max<uint32_t>(P.pool_tail[n_pools - 1], a1 - tail));
+    }
+    P.pool_cta[n_pools] = uint16_t(grid);
+    P.n_pools = n_pools;
+    return true;
 }
 
 template <int kPer, bool kVec, bool kStaged, bool kGemv = false, bool kFixed = false, bool kPool = false>
@@ -1011,6 +1089,12 @@ int launch(DecodeParams &P, cudaStream_t stream) {
         attr_set[dev] = true;
     }
     const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(grid_max[dev]));
+    if constexpr (kPool) {
+        if (!pool_setup(P, grid)) {
+            P.work = nullptr;
+            return launch<kPer, kVec, kStaged, kGemv, kFixed, false>(P, stream);
+        }
+    }
     decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool><<<grid, kThreads, kSmemBytes, stream>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -1108,10 +1192,7 @@ int decode_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_l
             items += items_of(e.n_values, P.chunk_syms, P.sub_syms);
         }
         P.n_items = items;
-        // the work pool needs one code table across the launch
-        bool one_table = true;
-        for (uint32_t u = 1; u < P.n_tasks; ++u) one_table &= P.task[u].table == P.task[0].table;
-        P.work = one_table ? d_work : nullptr;
+        P.work = d_work;
         rc = launch_tasks(P, static_cast<cudaStream_t>(stream));
         if (rc) return rc;
     }

@@ -106,12 +106,14 @@ def test_long_code_pairs(variant):
 
 
 def test_work_pool_parity_and_reset():
-    """With a work area the last sixteenth of every CTA's items is shared: the
-    output is the same bytes, the area is zero again after every launch, and
-    layers over several tables (which skip the pool) decode the same way."""
+    """With a work area the last sixteenth of every CTA's items is pooled
+    (one pool per run of CTAs ending in one code table, drained by any CTA):
+    the output is the same bytes, and the area is zero again after every
+    launch, for one table and for several."""
     one = [workloads.normal_tensor((1 << 25,), 0.02, seed=21)]           # 4096 items: ~27 per CTA, one pooled
-    several = [workloads.normal_tensor((1 << 21,), 0.02, seed=22), workloads.uniform_bytes(1 << 20, seed=23)]
-    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    several = [workloads.normal_tensor((1 << 24,), 0.02, seed=22), workloads.normal_tensor((1 << 24,), 0.7, seed=24),
+               workloads.uniform_bytes(1 << 20, seed=23)]                # pools over three tables
+    work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device="cuda")
     for tensors in (one, several):
         blob = oracle.encode_layer(tensors)
         info = k3.layer_info(blob)
@@ -282,7 +284,7 @@ def test_fault_random_bitstream_pooled():
     hi = even_off - 64                                        # the stream's padding stays zero
     bad[lo:hi] = rng.integers(0, 256, hi - lo, dtype=np.uint8)
     d_blob = torch.from_numpy(bad).cuda()
-    work = torch.zeros(2, dtype=torch.int32, device="cuda")
+    work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device="cuda")
     for _ in range(2):
         buf = torch.full((info["out_bytes"] + 2 * GUARD,), SENTINEL, dtype=torch.uint8, device="cuda")
         st = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -224,12 +224,12 @@ def test_decode_argument_checks_need_no_device():
     assert st == k3.E_EMPTY
     # the work-area variant: its own checks first, then the same as above
     ws = L.k3huf_decode_layer_ws
-    assert ws(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, None, 8, None) == k3.E_ARG    # no work area
-    assert ws(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, 8192, 4, None) == k3.E_ARG    # too short
-    assert ws(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, 8194, 8, None) == k3.E_ARG    # unaligned
-    assert ws(b.ctypes.data, b.size, 4096 + 8, b.size, 4096, 1 << 20, 4096, 8192, 8, None) == k3.E_ARG
-    assert ws(bad.ctypes.data, bad.size, 4096, bad.size, 4096, 1 << 20, 4096, 8192, 8, None) == k3.E_FORMAT
-    assert k3.WORK_BYTES == 8
+    assert ws(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, None, 68, None) == k3.E_ARG    # no work area
+    assert ws(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, 8192, 64, None) == k3.E_ARG   # too short
+    assert ws(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, 8194, 68, None) == k3.E_ARG   # unaligned
+    assert ws(b.ctypes.data, b.size, 4096 + 8, b.size, 4096, 1 << 20, 4096, 8192, 68, None) == k3.E_ARG
+    assert ws(bad.ctypes.data, bad.size, 4096, bad.size, 4096, 1 << 20, 4096, 8192, 68, None) == k3.E_FORMAT
+    assert k3.WORK_BYTES == 68
     assert L.k3huf_set_decoder_variant(3) == k3.E_ARG
     assert L.k3huf_set_decoder_variant(-1) == k3.E_ARG
 
