@@ -164,6 +164,33 @@ int k3huf_decode_layer_ws(const void *h_layer_hdr, size_t hdr_bytes,
                           void *d_out, size_t out_bytes,
                           uint32_t *d_status, void *d_work, size_t work_bytes, void *stream);
 
+/* Flag of k3huf_decode_layer_ex: the launch may start early. */
+#define K3HUF_DECODE_EARLY_START 1u
+
+/* k3huf_decode_layer_ws with options; not from the article (its decoder
+ * runs one call at a time).
+ *  d_work / work_bytes: as for k3huf_decode_layer_ws, or d_work NULL (and
+ *    work_bytes ignored) to decode as k3huf_decode_layer does;
+ *  flags: 0 or K3HUF_DECODE_EARLY_START.  With that flag the kernels are
+ *    launched with programmatic stream serialisation: a kernel's CTAs may
+ *    start while the kernel before it in the stream is still running, take
+ *    the SMs it frees, and read the container and build their code tables
+ *    there; their first write to global memory (status, output, work area)
+ *    waits until that kernel has completed.  The caller guarantees that the
+ *    kernel before this call in the stream does not write the container
+ *    (d_layer); copies, event waits and kernels of other streams order the
+ *    call as usual.  Back-to-back layer decodes, or a decode after the
+ *    kernels that consume the previous layer, meet this.
+ *  Other arguments as for k3huf_decode_layer_ws; the output is the same
+ *  bytes.
+ * Errors: K3HUF_E_ARG for an unknown flag or, when d_work is not NULL, an
+ * unaligned or short work area; else as k3huf_decode_layer. */
+int k3huf_decode_layer_ex(const void *h_layer_hdr, size_t hdr_bytes,
+                          const void *d_layer, size_t layer_bytes,
+                          void *d_out, size_t out_bytes,
+                          uint32_t *d_status, void *d_work, size_t work_bytes,
+                          uint32_t flags, void *stream);
+
 /* Decode one stripe on the GPU (the article's per-stripe decode).
  *  codelen: host copy of the stripe's table (validated with k3huf_build);
  *  chunk_syms, sub_syms: values per indexed chunk and per sub-stream, as

@@ -26,6 +26,7 @@ STRIPE_VALUES = 1 << 25
 
 EXPORTS = [
     "k3huf_build", "k3huf_layer_info", "k3huf_tensor_info", "k3huf_decode_layer", "k3huf_decode_layer_ws",
+    "k3huf_decode_layer_ex",
     "k3huf_decode_stripe",
     "k3huf_set_decoder_variant", "k3huf_encode_layer", "k3huf_ring_create", "k3huf_ring_run",
     "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
@@ -90,6 +91,7 @@ def _lib():
             L.k3huf_tensor_info.argtypes = [_vp, _sz, ctypes.c_uint32, ctypes.POINTER(TensorInfo)]
             L.k3huf_decode_layer.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp, _vp]
             L.k3huf_decode_layer_ws.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]
+            L.k3huf_decode_layer_ex.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp, _vp, _sz, ctypes.c_uint32, _vp]
             L.k3huf_decode_stripe.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32, _vp, _sz, ctypes.c_uint32, _vp,
                                               _vp, _vp]
             L.k3huf_set_decoder_variant.argtypes = [ctypes.c_int]
@@ -252,18 +254,26 @@ def encode_layer_gpu(tensors, chunk_syms: int = 4096, sub_syms: int = 256, share
 
 
 WORK_BYTES = 68
+DECODE_EARLY_START = 1
 
 
 def decode_layer(hdr, d_layer, d_out, d_status, stream=None, layer_bytes: int | None = None,
-                 out_bytes: int | None = None, work=None) -> None:
+                 out_bytes: int | None = None, work=None, early_start: bool = False) -> None:
     """Launch the decode of a layer; asynchronous on ``stream``.  ``work``: a
     zeroed device buffer of at least WORK_BYTES that no other launch uses
     meanwhile (k3huf_decode_layer_ws: the end of the launch is spread over
-    all CTAs), or None."""
+    all CTAs), or None.  ``early_start`` (k3huf_decode_layer_ex): the launch
+    may begin while the kernel before it in the stream finishes; that kernel
+    must not write ``d_layer``."""
     h = _host(hdr)
     lb = _nbytes(d_layer) if layer_bytes is None else layer_bytes
     ob = _nbytes(d_out) if out_bytes is None else out_bytes
-    if work is None:
+    if early_start:
+        _check(_lib().k3huf_decode_layer_ex(h.ctypes.data, h.size, _dptr(d_layer), lb, _dptr(d_out), ob,
+                                            _dptr(d_status), None if work is None else _dptr(work),
+                                            0 if work is None else _nbytes(work), DECODE_EARLY_START,
+                                            _stream(stream)), "k3huf_decode_layer_ex")
+    elif work is None:
         _check(_lib().k3huf_decode_layer(h.ctypes.data, h.size, _dptr(d_layer), lb, _dptr(d_out), ob,
                                          _dptr(d_status), _stream(stream)), "k3huf_decode_layer")
     else:

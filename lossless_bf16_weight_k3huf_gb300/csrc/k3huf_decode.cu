@@ -186,6 +186,13 @@ __device__ __forceinline__ void cp_async_wait_all() {
 __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Programmatic dependent launch: the next grid in the stream, if launched
+// with early start, may be scheduled once every CTA of this one has passed
+// grid_dep_launch (or exited); grid_dep_wait returns once the grid before
+// this one has completed and its writes are visible.  Both are no-ops for a
+// grid launched the ordinary way.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // 64-bit MSB-first bit window over one sub-stream read straight from
 // global memory (16-byte read-only loads, one block ahead) -- used for
@@ -480,6 +487,8 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     __shared__ __align__(16) StripeTask s_task[kMaxTasks];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // (one CTA per SM: a next grid started early takes the SMs this one frees)
+    grid_dep_launch();
     uint8_t *wslot = smem + kSmemLut + kSmemL12 + size_t(warp) * kWarpSlot;
     uint32_t *bitbuf = reinterpret_cast<uint32_t *>(wslot);
     uint8_t *wrows = wslot + kBitBuf + 16;
@@ -600,9 +609,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         if (rebuild) {
             table_bad = !build_tables<kPer>(my_len, lut1, lut);
             table_built = table;
-            if (table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
         }
-        if (steal >= 0 && table_bad) break;           // (CTA-uniform) its items cannot be taken
+        if (steal >= 0 && table_bad) {                // (CTA-uniform) its items cannot be taken
+            if (tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
+            break;
+        }
         if (item == it0 && hown) {                    // published by the next barrier
             cp_async_wait_all();
             s_hok[tid] = stripe_header_ok(P, s_task[tid], s_hdr[tid]) ? 1 : 0;
@@ -627,6 +638,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         }
         __syncthreads();
         const uint32_t nheavy = s_nheavy <= uint32_t(kMaxHeavy) ? s_nheavy : 0u;   // overflow: index order only
+        // everything up to here reads only the container and the parameters;
+        // the first write to global memory (the status word, the output, the
+        // work area) waits for the grid before this one (first phase only)
+        if (item == it0) grid_dep_wait();
+        if (steal < 0 && rebuild && table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
 
         while (!table_bad && !dead) {
             uint32_t v = 0;
@@ -1064,7 +1080,7 @@ bool pool_setup(DecodeParams &P, uint32_t grid) {
 }
 
 template <int kPer, bool kVec, bool kStaged, bool kGemv = false, bool kFixed = false, bool kPool = false>
-int launch(DecodeParams &P, cudaStream_t stream) {
+int launch(DecodeParams &P, cudaStream_t stream, bool early = false) {
     static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
     static int grid_max[kMaxDevices] = {};
     int dev = 0;
@@ -1092,10 +1108,30 @@ int launch(DecodeParams &P, cudaStream_t stream) {
     if constexpr (kPool) {
         if (!pool_setup(P, grid)) {
             P.work = nullptr;
-            return launch<kPer, kVec, kStaged, kGemv, kFixed, false>(P, stream);
+            return launch<kPer, kVec, kStaged, kGemv, kFixed, false>(P, stream, early);
         }
     }
-    decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    if (early) {
+        // programmatic stream serialisation: the grid may start, reading only
+        // the container, while the previous kernel in the stream finishes
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool>, P);
+        if (e != cudaSuccess) {
+            set_cuda_error(int(e));
+            return K3HUF_E_CUDA;
+        }
+    } else {
+        decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool><<<grid, kThreads, kSmemBytes, stream>>>(P);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) {
         set_cuda_error(int(e));
@@ -1108,17 +1144,17 @@ int launch(DecodeParams &P, cudaStream_t stream) {
 int g_per = 2;
 
 template <int kPer>
-int launch_syms(DecodeParams &P, cudaStream_t stream) {
+int launch_syms(DecodeParams &P, cudaStream_t stream, bool early) {
     const bool vec = P.sub_syms % 8 == 0;
     // a sub-stream's bits (at most 12 per value) must fit the shared buffer
     const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= kBitBuf;
     if constexpr (kPer == 2)
         if (staged && P.chunk_syms == 4096 && P.sub_syms == 256)
-            return P.work ? launch<2, true, true, false, true, true>(P, stream)
-                          : launch<2, true, true, false, true>(P, stream);
+            return P.work ? launch<2, true, true, false, true, true>(P, stream, early)
+                          : launch<2, true, true, false, true>(P, stream, early);
     P.work = nullptr;                                    // (the pool has the default sizes only)
-    if (staged) return vec ? launch<kPer, true, true>(P, stream) : launch<kPer, false, true>(P, stream);
-    return vec ? launch<kPer, true, false>(P, stream) : launch<kPer, false, false>(P, stream);
+    if (staged) return vec ? launch<kPer, true, true>(P, stream, early) : launch<kPer, false, true>(P, stream, early);
+    return vec ? launch<kPer, true, false>(P, stream, early) : launch<kPer, false, false>(P, stream, early);
 }
 
 // fused GEMV launches: staged bits and the vector merge only
@@ -1131,10 +1167,10 @@ int launch_gemv(DecodeParams &P, cudaStream_t stream) {
     }
 }
 
-int launch_tasks(DecodeParams &P, cudaStream_t stream) {
+int launch_tasks(DecodeParams &P, cudaStream_t stream, bool early = false) {
     switch (g_per) {
-        case 1: return launch_syms<1>(P, stream);
-        default: return launch_syms<2>(P, stream);
+        case 1: return launch_syms<1>(P, stream, early);
+        default: return launch_syms<2>(P, stream, early);
     }
 }
 
@@ -1161,7 +1197,7 @@ extern "C" int k3huf_set_decoder_variant(int variant) {
 
 namespace {
 int decode_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes, void *d_out,
-                      size_t out_bytes, uint32_t *d_status, uint32_t *d_work, void *stream) {
+                      size_t out_bytes, uint32_t *d_status, uint32_t *d_work, bool early, void *stream) {
     if (!h_layer_hdr || !d_layer || !d_out || !d_status) return K3HUF_E_ARG;
     if (!aligned16(d_layer) || !aligned16(d_out) || (reinterpret_cast<uintptr_t>(d_status) & 3u)) return K3HUF_E_ARG;
     Layer L;
@@ -1193,7 +1229,7 @@ int decode_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_l
         }
         P.n_items = items;
         P.work = d_work;
-        rc = launch_tasks(P, static_cast<cudaStream_t>(stream));
+        rc = launch_tasks(P, static_cast<cudaStream_t>(stream), early);
         if (rc) return rc;
     }
     return K3HUF_OK;
@@ -1202,7 +1238,8 @@ int decode_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_l
 
 extern "C" int k3huf_decode_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
                                   void *d_out, size_t out_bytes, uint32_t *d_status, void *stream) {
-    return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status, nullptr, stream);
+    return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status, nullptr, false,
+                             stream);
 }
 
 extern "C" int k3huf_decode_layer_ws(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
@@ -1210,7 +1247,16 @@ extern "C" int k3huf_decode_layer_ws(const void *h_layer_hdr, size_t hdr_bytes, 
                                      void *stream) {
     if (!d_work || work_bytes < K3HUF_WORK_BYTES || (reinterpret_cast<uintptr_t>(d_work) & 3u)) return K3HUF_E_ARG;
     return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status,
-                             static_cast<uint32_t *>(d_work), stream);
+                             static_cast<uint32_t *>(d_work), false, stream);
+}
+
+extern "C" int k3huf_decode_layer_ex(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                                     void *d_out, size_t out_bytes, uint32_t *d_status, void *d_work, size_t work_bytes,
+                                     uint32_t flags, void *stream) {
+    if (flags & ~uint32_t(K3HUF_DECODE_EARLY_START)) return K3HUF_E_ARG;
+    if (d_work && (work_bytes < K3HUF_WORK_BYTES || (reinterpret_cast<uintptr_t>(d_work) & 3u))) return K3HUF_E_ARG;
+    return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status,
+                             static_cast<uint32_t *>(d_work), (flags & K3HUF_DECODE_EARLY_START) != 0, stream);
 }
 
 extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms, uint32_t sub_syms,

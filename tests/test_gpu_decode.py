@@ -129,6 +129,76 @@ def test_work_pool_parity_and_reset():
             assert int(work.abs().sum().item()) == 0
 
 
+def test_early_start_chain():
+    """Decodes launched with early start on one stream, each starting while
+    the kernel before it runs: three layers (pooled with a work area, one
+    table, and one that spans two launches), twice over.  Either every
+    output is filled and every status zeroed first and the six decodes run
+    back to back (a decode behind a decode), or each decode comes right
+    after the fill of its output and the zeroing of its status (a write
+    ahead of the previous kernel's end would be lost).  Every output equals
+    the oracle's, every status is zero and the work area is zero again."""
+    layers = [
+        [workloads.normal_tensor((1 << 24,), 0.02, seed=41), workloads.normal_tensor((1 << 23,), 0.7, seed=42)],
+        [workloads.normal_tensor((3 << 20,), 0.05, seed=43)],
+        [workloads.normal_tensor((4096 + 17 * i,), 0.02, 600 + i) for i in range(70)],
+    ]
+    work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device="cuda")
+    cases = []
+    for tensors in layers:
+        blob = oracle.encode_layer(tensors)
+        info = k3.layer_info(blob)
+        # the decode writes the tensors' bytes only: the alignment gaps
+        # between them keep the fill byte
+        ref = np.full(info["out_bytes"], SENTINEL, np.uint8)
+        dec = oracle.decode_layer(blob)[1]
+        for t in tensor_regions(blob):
+            a, b = t["out_offset"], t["out_offset"] + 2 * t["n_values"]
+            ref[a:b] = dec[a:b]
+        cases.append((blob[: info["hdr_bytes"]], torch.from_numpy(blob).cuda(), torch.from_numpy(ref).cuda(),
+                      info["out_bytes"]))
+    assert k3.layer_info(cases[2][0])["n_stripes"] > 64
+    for fill_first in (True, False, True, False):
+        outs = [torch.empty(n, dtype=torch.uint8, device="cuda") for _, _, _, n in cases * 2]
+        sts = [torch.empty(1, dtype=torch.int32, device="cuda") for _ in outs]
+        if fill_first:
+            for out, st in zip(outs, sts):
+                out.fill_(SENTINEL)
+                st.fill_(0)
+        for li, ((hdr, d_blob, ref, n), out, st) in enumerate(zip(cases * 2, outs, sts)):
+            if not fill_first:
+                out.fill_(SENTINEL)
+                st.fill_(0)
+            k3.decode_layer(hdr, d_blob, out, st, work=work if li % 3 == 0 else None, early_start=True)
+        torch.cuda.synchronize()
+        for (hdr, d_blob, ref, n), out, st in zip(cases * 2, outs, sts):
+            assert int(st.item()) == 0
+            assert torch.equal(out, ref)
+        assert int(work.abs().sum().item()) == 0
+
+
+def test_early_start_device_table_fault():
+    """Early start with a device table that does not build: the status bit
+    is written after the preceding kernel (the status fill) completes, so
+    it is not lost."""
+    blob = oracle.encode_layer([workloads.normal_tensor((1 << 22,), 0.02, 44)])
+    info = k3.layer_info(blob)
+    bad = blob.copy()
+    bad[64:64 + 256] = 1
+    d_good, d_bad = torch.from_numpy(blob).cuda(), torch.from_numpy(bad).cuda()
+    for _ in range(3):
+        out = torch.empty(info["out_bytes"], dtype=torch.uint8, device="cuda")
+        st0 = torch.empty(1, dtype=torch.int32, device="cuda")
+        st1 = torch.empty(1, dtype=torch.int32, device="cuda")
+        st0.fill_(0)
+        k3.decode_layer(blob[: info["hdr_bytes"]], d_good, out, st0, early_start=True)
+        st1.fill_(0)
+        k3.decode_layer(blob[: info["hdr_bytes"]], d_bad, out, st1, early_start=True)
+        torch.cuda.synchronize()
+        assert int(st0.item()) == 0
+        assert int(st1.item()) & k3.ST_HEADER
+
+
 def test_limiter_fired_alphabet():
     x = workloads.heavy_tail(n=1 << 22)
     blob = check_parity([x])
@@ -414,8 +484,17 @@ def _full_size(tensors):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     k3.set_decoder_variant(0)
     k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, out, st)
+    # then twice as the benchmark launches it (work-area pools, early start):
+    # the first of the two starts while the plain decode above finishes
+    work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device="cuda")
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out2 = torch.empty_like(out)
+    for _ in range(2):
+        k3.decode_layer(blob[: info["hdr_bytes"]], d_blob, out2, st2, work=work, early_start=True)
     torch.cuda.synchronize()
-    assert st.item() == 0
+    assert st.item() == 0 and st2.item() == 0
+    assert int(work.abs().sum().item()) == 0
+    assert torch.equal(out, out2)
     _sampled_parity(blob, tensors, out)
     # the oracle encoder's tables equal the product encoder's
     for t, x in zip(tensor_regions(blob), tensors):

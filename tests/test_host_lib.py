@@ -230,6 +230,16 @@ def test_decode_argument_checks_need_no_device():
     assert ws(b.ctypes.data, b.size, 4096 + 8, b.size, 4096, 1 << 20, 4096, 8192, 68, None) == k3.E_ARG
     assert ws(bad.ctypes.data, bad.size, 4096, bad.size, 4096, 1 << 20, 4096, 8192, 68, None) == k3.E_FORMAT
     assert k3.WORK_BYTES == 68
+    # the variant with options: flags and (optional) work area checked first
+    ex = L.k3huf_decode_layer_ex
+    assert ex(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, None, 0, 2, None) == k3.E_ARG    # unknown flag
+    assert ex(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, None, 0, 1 << 31, None) == k3.E_ARG
+    assert ex(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, 8192, 64, 1, None) == k3.E_ARG   # too short
+    assert ex(b.ctypes.data, b.size, 4096, b.size, 4096, 1 << 20, 4096, 8194, 68, 1, None) == k3.E_ARG   # unaligned
+    assert ex(b.ctypes.data, b.size, 4096 + 8, b.size, 4096, 1 << 20, 4096, None, 0, 1, None) == k3.E_ARG
+    assert ex(bad.ctypes.data, bad.size, 4096, bad.size, 4096, 1 << 20, 4096, None, 0, 1, None) == k3.E_FORMAT
+    assert ex(b.ctypes.data, b.size, 4096, b.size - 1, 4096, 1 << 20, 4096, 8192, 68, 0, None) == k3.E_ARG
+    assert k3.DECODE_EARLY_START == 1
     assert L.k3huf_set_decoder_variant(3) == k3.E_ARG
     assert L.k3huf_set_decoder_variant(-1) == k3.E_ARG
 
