@@ -21,6 +21,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "k3huf_oracle.c")
+_SRC_PS = os.path.join(_HERE, "k3huf_pagestyle.c")     # the article-style decoder (CPU timing only)
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libk3huf_oracle.so")
 _lock = threading.Lock()
@@ -38,9 +39,10 @@ _u32p = ctypes.POINTER(ctypes.c_uint32)
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (plain -O2, no target-specific flags)."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_PS)):
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-shared", "-fPIC", "-Wall", "-o", tmp, _SRC])
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-shared", "-fPIC", "-Wall", "-o", tmp, _SRC, _SRC_PS])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -66,6 +68,8 @@ def lib():
             L.orc_decode_stripe_range.argtypes = [_u8p, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32,
                                                   ctypes.c_uint32, _u8p]
             L.orc_decode_layer.argtypes = [_u8p, ctypes.c_uint64, _u8p]
+            L.orc_ps_build.argtypes = [_u8p, ctypes.POINTER(ctypes.c_uint16)]
+            L.orc_ps_decode_stripe.argtypes = [_u8p, ctypes.c_uint64, ctypes.c_uint32, _u8p, _u8p]
             _lib = L
     return _lib
 
@@ -191,3 +195,38 @@ def decode_chunks(blob: np.ndarray, stripe: int, first_chunk: int, n_chunks: int
     stripe into ``out`` (a layer-output-sized uint8 buffer); returns rc."""
     blob = np.ascontiguousarray(blob, dtype=np.uint8)
     return int(lib().orc_decode_stripe_range(_ptr(blob), blob.size, stripe, first_chunk, n_chunks, _ptr(out)))
+
+
+# --- the article-style decoder (k3huf_pagestyle.c): CPU timing beside the oracle ---
+
+def pagestyle_table(codelen) -> np.ndarray:
+    """The article-style decoder's 4096-entry table, (symbol << 4) | length
+    per 12-bit window, 0 where no code starts."""
+    cl = np.ascontiguousarray(codelen, dtype=np.uint8)
+    lut = np.zeros(4096, np.uint16)
+    rc = lib().orc_ps_build(_ptr(cl), lut.ctypes.data_as(ctypes.POINTER(ctypes.c_uint16)))
+    if rc:
+        raise ValueError(f"orc_ps_build: {rc}")
+    return lut
+
+
+def pagestyle_decode_stripe(blob: np.ndarray, stripe: int, out: np.ndarray, hi: np.ndarray | None = None) -> int:
+    """Decode one stripe with the article-style decoder into ``out`` (the
+    layer's output buffer); ``hi``: scratch of at least the stripe's value
+    count.  Returns 0 or E_FORMAT / E_ARG."""
+    blob = np.ascontiguousarray(blob, dtype=np.uint8)
+    if hi is None:
+        hi = np.empty(1 << 25, np.uint8)
+    return int(lib().orc_ps_decode_stripe(_ptr(blob), blob.size, stripe, _ptr(hi), _ptr(out)))
+
+
+def pagestyle_decode_layer(blob: np.ndarray):
+    """(rc, output) of the article-style decoder over every stripe."""
+    info = layer_info(blob)
+    out = np.zeros(info["out_bytes"], np.uint8)
+    hi = np.empty(1 << 25, np.uint8)
+    for s in range(info["n_stripes"]):
+        rc = pagestyle_decode_stripe(blob, s, out, hi)
+        if rc:
+            return rc, out
+    return 0, out

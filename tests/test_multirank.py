@@ -53,3 +53,20 @@ def test_cpu_baseline_parallel_fields():
     r = bench.cpu_baseline_parallel(blob, budget_s=5.0, threads=3)
     assert r["cores"] == 3 and r["kind"] == "oracle" and r["value"] > 0
     assert r["sample"].startswith("193 chunks of 4096 values")
+
+
+def test_cpu_article_style_fields():
+    """The article-style decoder's timing: one core over whole stripes,
+    then the whole layer with one thread per stripe, decoded and input
+    rates both positive, and the sample naming what ran."""
+    import numpy as np
+    import bench
+    import oracle
+    import workloads
+    blob = oracle.encode_layer([np.tile(workloads.tiny(), 17)[: (1 << 25) + 5003]])    # two stripes
+    r = bench.cpu_article_style(blob, budget_s=0.0)
+    assert r["one_core"] > 0 and r["all_cores"] > 0
+    assert r["input_gbs"]["one_core"] > 0 and r["input_gbs"]["all_cores"] > 0
+    assert r["cores"] == min(2, os.cpu_count() or 1)
+    assert "not the oracle" in r["kind"]
+    assert "(2 stripes" in r["sample"] and r["sample"].startswith("one core: 64 MiB decoded")
