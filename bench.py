@@ -461,6 +461,22 @@ def main():
     ms_per_step = dev_ms / args.steps
     value = whole_job_gbs(raw, world, args.steps, dev_ms)
 
+    # single launches, each between its own pair of events (so none starts
+    # early), after 5 more warm-ups: median and min of 20, in us per launch
+    single = []
+    with torch.cuda.stream(stream):
+        for i in range(25):
+            if flush is not None:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            k3.decode_layer(hdr, d_blob, d_out, d_st, stream=stream, work=d_work)
+            b.record(stream)
+            if i >= 5:
+                single.append((a, b))
+    stream.synchronize()
+    single_us = sorted(a.elapsed_time(b) * 1e3 / launches_per_step for a, b in single)
+
     # end to end through the C ABI with host buffers
     e2e = bench_e2e(k3, blob, hdr, info, dev, stream, max(4, min(args.steps, 20)))
 
@@ -493,6 +509,9 @@ def main():
                      "frac_of_8TBs": round(achieved / 8000.0, 4)},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
+        "single_launch_us": {"median": round(statistics.median(single_us), 2), "min": round(single_us[0], 2),
+                             "of": len(single_us), "note": "outside the timed region: launches one at a time, "
+                                                           "event pair around each, no early start"},
         "clocks": clk.summary(),
         "timed_region_ms": round(total_ms, 3),
     }
