@@ -265,13 +265,21 @@ int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_la
  *  d_scratch: device, 256-byte aligned, scratch_bytes >=
  *    k3huf_encode_scratch_bytes(...) (contents need not be initialised);
  *  d_blob: device, 256-byte aligned, blob_cap bytes; with d_blob NULL only
- *    *blob_bytes is set (the histogram pass still runs).
+ *    *blob_bytes is set (the histogram pass still runs).  A buffer of
+ *    k3huf_encode_bound(...) bytes always suffices, so one call encodes;
+ *    the container fills its first *blob_bytes bytes.
  * Synchronises `stream` twice (after the histograms and at the end) and
  * returns when the container is complete.  K3HUF_E_ARG on a bad argument
  * or a short buffer, K3HUF_E_FORMAT if the packed bits disagree with the
  * planned layout (an internal check), K3HUF_E_CUDA on a CUDA error. */
 int k3huf_encode_scratch_bytes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms,
                                uint32_t sub_syms, int shared_table, size_t *scratch_bytes);
+/* Upper bound of the container's size for any values of these sizes: the
+ * layout when every code has the limit's 12 bits (host, pure; allocates
+ * nothing on the device).  Arguments as for k3huf_encode_layer_gpu;
+ * K3HUF_E_ARG for an empty layer, a zero size or a null output. */
+int k3huf_encode_bound(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms, uint32_t sub_syms,
+                       int shared_table, size_t *blob_bytes);
 int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
                            uint32_t chunk_syms, uint32_t sub_syms, int shared_table, void *d_scratch,
                            size_t scratch_bytes, void *d_blob, size_t blob_cap, size_t *blob_bytes, void *stream);

@@ -31,7 +31,7 @@ EXPORTS = [
     "k3huf_set_decoder_variant", "k3huf_encode_layer", "k3huf_ring_create", "k3huf_ring_run",
     "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
     "k3huf_feed_read", "k3huf_feed_close", "k3huf_ring_create_staged", "k3huf_ring_run_file",
-    "k3huf_encode_scratch_bytes", "k3huf_encode_layer_gpu", "k3huf_gemv_layer",
+    "k3huf_encode_scratch_bytes", "k3huf_encode_bound", "k3huf_encode_layer_gpu", "k3huf_gemv_layer",
 ]
 FILE_ALIGN = 4096
 
@@ -104,6 +104,8 @@ def _lib():
             L.k3huf_ring_destroy.argtypes = [_vp]
             L.k3huf_encode_scratch_bytes.argtypes = [ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint64), ctypes.c_uint32,
                                                      ctypes.c_uint32, ctypes.c_int, ctypes.POINTER(_sz)]
+            L.k3huf_encode_bound.argtypes = [ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint64), ctypes.c_uint32,
+                                             ctypes.c_uint32, ctypes.c_int, ctypes.POINTER(_sz)]
             L.k3huf_encode_layer_gpu.argtypes = [ctypes.c_uint32, ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_uint64),
                                                  ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, _vp, _sz, _vp, _sz,
                                                  ctypes.POINTER(_sz), _vp]
@@ -227,11 +229,26 @@ def encode_scratch_bytes(n_values, chunk_syms: int = 4096, sub_syms: int = 256, 
     return int(out.value)
 
 
+def encode_bound(sizes, chunk_syms: int = 4096, sub_syms: int = 256, shared_table: bool = False) -> int:
+    """Bytes that hold the container of tensors of these sizes whatever their
+    values (k3huf_encode_bound)."""
+    n = len(sizes)
+    nv = (ctypes.c_uint64 * n)(*[int(x) for x in sizes])
+    out = _sz(0)
+    _check(_lib().k3huf_encode_bound(n, nv, chunk_syms, sub_syms, int(shared_table), ctypes.byref(out)),
+           "k3huf_encode_bound")
+    return int(out.value)
+
+
 def encode_layer_gpu(tensors, chunk_syms: int = 4096, sub_syms: int = 256, shared_table: bool = False,
-                     stream=None, scratch=None):
+                     stream=None, scratch=None, out=None):
     """Container of a layer of bf16 CUDA tensors (16-byte aligned), built on
     the GPU; returns a CUDA uint8 tensor.  ``scratch`` (a CUDA tensor) is
-    allocated here when not given."""
+    allocated here when not given.  ``out``: a CUDA uint8 tensor of at least
+    encode_bound(...) bytes, 256-byte aligned; the container is encoded in
+    one call into its first bytes and that prefix is returned (without
+    ``out``, a first call sizes the container and a second fills a tensor
+    of exactly that size)."""
     import torch
     n = len(tensors)
     sizes = [int(t.numel()) for t in tensors]
@@ -244,6 +261,11 @@ def encode_layer_gpu(tensors, chunk_syms: int = 4096, sub_syms: int = 256, share
     size = _sz(0)
     L = _lib()
     s = _stream(stream)
+    if out is not None:
+        _check(L.k3huf_encode_layer_gpu(n, ptrs, nv, chunk_syms, sub_syms, int(shared_table), _dptr(scratch),
+                                        _nbytes(scratch), _dptr(out), _nbytes(out), ctypes.byref(size), s),
+               "k3huf_encode_layer_gpu")
+        return out[: size.value]
     _check(L.k3huf_encode_layer_gpu(n, ptrs, nv, chunk_syms, sub_syms, int(shared_table), _dptr(scratch),
                                     _nbytes(scratch), None, 0, ctypes.byref(size), s), "k3huf_encode_layer_gpu")
     blob = torch.empty(size.value, dtype=torch.uint8, device=dev)

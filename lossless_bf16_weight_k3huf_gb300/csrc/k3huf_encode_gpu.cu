@@ -60,6 +60,7 @@ constexpr int kHistThreads = 256;
 constexpr int kScanThreads = 1024;
 constexpr int kPackThreads = 256;
 constexpr int kStageWords = 128;     // staging window of a packing warp (one step: <= 97 words)
+constexpr int kPackCtasPerSm = 4;    // packing CTAs per SM the register budget is set for
 
 ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_chunks) {
     ScratchLayout s{};
@@ -141,6 +142,41 @@ __global__ void __launch_bounds__(kPackThreads) chunk_bits_kernel(EncParams P) {
     }
 }
 
+// 3'. the same pass for the default layout (sub-streams of 256 values, a
+//    power-of-two count per chunk): one warp per chunk, each step of 256
+//    values is one sub-stream, whose bit count goes into the container's
+//    sub-stream index slot (the last one's is implied by the chunk's total);
+//    the packing pass turns those counts into the index
+__global__ void __launch_bounds__(kPackThreads) sub_bits_kernel(EncParams P) {
+    __shared__ uint8_t len[256];
+    const EncStripe &T = P.stripes[blockIdx.y];
+    for (int s = threadIdx.x; s < 256; s += kPackThreads) len[s] = uint8_t(P.codes[size_t(T.table) * 256 + s] & 15u);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const uint32_t warps = gridDim.x * (kPackThreads / 32), S = P.S;
+    uint16_t *sub_idx = reinterpret_cast<uint16_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES + 4ull * T.n_chunks);
+    for (uint32_t c = blockIdx.x * (kPackThreads / 32) + (threadIdx.x >> 5); c < T.n_chunks; c += warps) {
+        const uint32_t a = c * P.chunk_syms, b = min(T.n, a + P.chunk_syms);
+        uint32_t total = 0;
+        for (uint32_t k = 0; k < S; ++k) {
+            const uint32_t v = a + 256u * k + 8u * uint32_t(lane);
+            uint32_t bits = 0;
+            if (v + 8 <= b) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(T.src + 2 * size_t(v));
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) bits += len[(w[i] >> 8) & 0xFFu] + len[w[i] >> 24];
+            } else {
+                for (uint32_t u = v; u < b && u < v + 8; ++u) bits += len[T.src[2 * size_t(u) + 1]];
+            }
+            bits = __reduce_add_sync(0xffffffffu, bits);
+            total += bits;
+            if (lane == 0 && k + 1 < S) sub_idx[size_t(c) * (S - 1) + k] = uint16_t(bits);
+        }
+        if (lane == 0) P.chunk_bits[T.chunk_begin + c] = total;
+    }
+}
+
 // 4. one CTA per stripe: the chunk index (exclusive prefix of the chunks'
 //    bits), the stripe header, and the check of the total against the plan
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(EncParams P) {
@@ -184,13 +220,21 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(EncParams P) {
 }
 
 // 5. one warp per chunk: codes packed MSB-first, sub-stream index, low bytes
-__global__ void __launch_bounds__(kPackThreads) pack_kernel(EncParams P) {
-    __shared__ uint32_t code[256];
+__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_kernel(EncParams P) {
+    // the code table once per lane: entry s of lane l at code[s][l], so the
+    // warp's 32 lookups fall in 32 different banks whatever the symbols
+    // (a single copy put the frequent +/- pairs of one exponent, 128 apart,
+    // in one bank)
+    __shared__ uint32_t code[256][32];
     __shared__ uint32_t s_stage[kPackThreads / 32][kStageWords];
     const EncStripe &T = P.stripes[blockIdx.y];
-    for (int s = threadIdx.x; s < 256; s += kPackThreads) code[s] = P.codes[size_t(T.table) * 256 + s];
-    __syncthreads();
     const int lane = threadIdx.x & 31;
+    for (int s = threadIdx.x; s < 256; s += kPackThreads) {
+        const uint32_t e = P.codes[size_t(T.table) * 256 + s];
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) code[s][(j + lane) & 31] = e;   // lanes of a store: 32 banks
+    }
+    __syncthreads();
     uint32_t *stage = s_stage[threadIdx.x >> 5];
     uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
     const uint32_t n_words = (T.even_offset - T.bits_offset) / 4;   // the stream region, padding included
@@ -242,7 +286,7 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(EncParams P) {
             uint32_t e[8], my = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                e[i] = i < int(nv) ? code[hb[i]] : 0u;
+                e[i] = i < int(nv) ? code[hb[i]][lane] : 0u;
                 my += e[i] & 15u;
             }
             // place the lanes' bits: exclusive scan of the bit counts
@@ -368,6 +412,107 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(EncParams P) {
     }
 }
 
+// 5'. packing for the default layout: one lane per sub-stream.  A warp
+//    takes 32 consecutive sub-streams (whole chunks: S divides 32); the
+//    lanes of a chunk scan the bit counts that sub_bits_kernel left in the
+//    sub-stream index into their first bits, write the index, then each
+//    lane codes its 256 values in order into a 64-bit accumulator and
+//    writes every full word.  Words wholly inside a sub-stream's bits are
+//    its own (plain stores); its first and last words may hold a
+//    neighbour's bits too and are OR-ed atomically into the zeroed
+//    container.  The same lane writes its 256 low bytes.
+__global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(EncParams P) {
+    __shared__ uint32_t code[256][32];       // entry s of lane l at code[s][l] (as in pack_kernel)
+    const EncStripe &T = P.stripes[blockIdx.y];
+    const int lane = threadIdx.x & 31;
+    for (int s = threadIdx.x; s < 256; s += kPackThreads) {
+        const uint32_t e = P.codes[size_t(T.table) * 256 + s];
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) code[s][(j + lane) & 31] = e;
+    }
+    __syncthreads();
+    uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
+    const uint32_t n_words = (T.even_offset - T.bits_offset) / 4;   // the stream region, padding included
+    uint8_t *even = T.dst + T.even_offset;
+    uint16_t *sub_idx = reinterpret_cast<uint16_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES + 4ull * T.n_chunks);
+    const uint32_t S = P.S, n_sub = T.n_chunks * S;
+    const uint32_t k = uint32_t(lane) & (S - 1);
+    const uint32_t step = gridDim.x * kPackThreads;
+    for (uint32_t g0 = (blockIdx.x * kPackThreads + threadIdx.x) & ~31u; g0 < n_sub; g0 += step) {
+        const uint32_t g = g0 + uint32_t(lane);
+        const bool live = g < n_sub;               // (whole chunks: n_sub and g0 are multiples of S)
+        const uint32_t c = g / S;
+        uint32_t cnt = 0;
+        if (live && k + 1 < S) cnt = sub_idx[size_t(c) * (S - 1) + k];
+        uint32_t incl = cnt;
+        for (uint32_t d = 1; d < S; d <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d, int(S));
+            if (k >= d) incl += t;
+        }
+        __syncwarp();                              // every count read before any slot is overwritten
+        const uint32_t rel = incl - cnt;           // first bit, relative to the chunk's
+        if (!live) continue;
+        if (k > 0) sub_idx[size_t(c) * (S - 1) + k - 1] = uint16_t(rel);
+        const uint32_t b0 = P.chunk_start[T.chunk_begin + c] + rel;
+        const uint32_t v0 = g * 256u;
+        const uint32_t m = v0 < T.n ? min(256u, T.n - v0) : 0u;
+        // the accumulator's top na bits are pending, the first b0 % 32 of
+        // them the previous sub-stream's place (zeros here)
+        uint64_t acc = 0;
+        uint32_t na = b0 & 31u, wi = b0 >> 5;
+        bool first = true;
+        auto put = [&](uint32_t e) {
+            const uint32_t l = e & 15u;
+            if (l) acc |= uint64_t(e >> 4) << (64u - na - l);
+            na += l;
+        };
+        auto flush = [&]() {                       // at most 55 bits pending: one word at most
+            if (na >= 32u) {
+                const uint32_t w = __byte_perm(uint32_t(acc >> 32), 0, 0x0123);
+                if (wi < n_words) {
+                    if (first)
+                        atomicOr(&words[wi], w);
+                    else
+                        words[wi] = w;
+                }
+                first = false;
+                ++wi;
+                acc <<= 32;
+                na -= 32u;
+            }
+        };
+        uint32_t i = 0;
+        for (; i + 16 <= m; i += 16) {
+            const uint4 x0 = *reinterpret_cast<const uint4 *>(T.src + 2 * size_t(v0 + i));
+            const uint4 x1 = *reinterpret_cast<const uint4 *>(T.src + 2 * size_t(v0 + i) + 16);
+            const uint32_t q[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {          // two values per word, a flush per pair
+                put(code[(q[j] >> 8) & 0xFFu][lane]);
+                put(code[q[j] >> 24][lane]);
+                flush();
+            }
+            uint4 lo;
+            lo.x = __byte_perm(q[0], q[1], 0x6420);
+            lo.y = __byte_perm(q[2], q[3], 0x6420);
+            lo.z = __byte_perm(q[4], q[5], 0x6420);
+            lo.w = __byte_perm(q[6], q[7], 0x6420);
+            *reinterpret_cast<uint4 *>(even + v0 + i) = lo;
+        }
+        for (; i < m; ++i) {                       // the stripe's last sub-stream: its ragged end
+            const uint8_t *src = T.src + 2 * size_t(v0 + i);
+            put(code[src[1]][lane]);
+            flush();
+            even[v0 + i] = src[0];
+        }
+        // the last, partial word: shared with the next sub-stream
+        if (na && wi < n_words) {
+            const uint32_t w = __byte_perm(uint32_t(acc >> 32), 0, 0x0123);
+            if (w) atomicOr(&words[wi], w);
+        }
+    }
+}
+
 int cuda_fail(cudaError_t e) {
     set_cuda_error(int(e));
     return K3HUF_E_CUDA;
@@ -384,6 +529,21 @@ int check_inputs(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_sy
 }  // namespace k3huf
 
 using namespace k3huf;
+
+extern "C" int k3huf_encode_bound(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms, uint32_t sub_syms,
+                                  int shared_table, size_t *blob_bytes) {
+    int rc = check_inputs(n_tensors, n_values, chunk_syms);
+    if (rc) return rc;
+    if (!blob_bytes) return K3HUF_E_ARG;
+    try {
+        LayerPlan L;
+        plan_stripes(n_tensors, n_values, chunk_syms, effective_sub_syms(chunk_syms, sub_syms), shared_table != 0, L);
+        *blob_bytes = size_t(layout_bound(L));
+        return K3HUF_OK;
+    } catch (const std::bad_alloc &) {
+        return K3HUF_E_NOMEM;
+    }
+}
 
 extern "C" int k3huf_encode_scratch_bytes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms,
                                           uint32_t sub_syms, int shared_table, size_t *scratch_bytes) {
@@ -491,9 +651,20 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         // 3-5. chunk bits, chunk index, packing
         const uint32_t wpb = kPackThreads / 32;
         const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_chunks + wpb - 1) / wpb));
-        chunk_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
-        scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
-        pack_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+        // the default layout (256-value sub-streams, 1-16 per chunk) packs
+        // one sub-stream per lane; any other layout one chunk per warp
+        const bool per_sub = sub_syms == 256 && chunk_syms % 256 == 0 && P.S <= 16 && (P.S & (P.S - 1)) == 0;
+        if (per_sub) {
+            sub_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+            scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
+            const uint64_t max_sub = uint64_t(max_chunks) * P.S;
+            const uint32_t gs = uint32_t(std::min<uint64_t>(4096, std::max<uint64_t>(1, (max_sub + kPackThreads - 1) / kPackThreads)));
+            pack_sub_kernel<<<dim3(gs, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+        } else {
+            chunk_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+            scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
+            pack_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
+        }
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
         uint32_t flag = 0;
         e = cudaMemcpyAsync(&flag, scr + SL.flag, sizeof flag, cudaMemcpyDeviceToHost, st);

@@ -178,22 +178,35 @@ void plan_layout(const uint64_t *stripe_hist, LayerPlan &L) {
         limit_depths(cnt, depth);
         for (int s = 0; s < 256; ++s) L.codelen[256ull * tb + s] = uint8_t(depth[s]);
     }
-    L.hdr = align_up(K3HUF_LAYER_HDR_BYTES + 256ull * L.n_tables + 32ull * L.n_tensors + 32ull * L.stripes.size(), 256);
-    uint64_t pos = L.hdr;
     for (size_t i = 0; i < L.stripes.size(); ++i) {
         PlanStripe &p = L.stripes[i];
         const uint8_t *cl = &L.codelen[256ull * p.table];
         uint64_t bits = 0;
         for (int s = 0; s < 256; ++s) bits += stripe_hist[256 * i + s] * cl[s];
         p.huff_bits = bits;
+    }
+    place_stripes(L);
+}
+
+void place_stripes(LayerPlan &L) {
+    L.hdr = align_up(K3HUF_LAYER_HDR_BYTES + 256ull * L.n_tables + 32ull * L.n_tensors + 32ull * L.stripes.size(), 256);
+    uint64_t pos = L.hdr;
+    for (size_t i = 0; i < L.stripes.size(); ++i) {
+        PlanStripe &p = L.stripes[i];
         p.bits_offset = uint32_t(align_up(K3HUF_STRIPE_HDR_BYTES + index_bytes(p.n_chunks, L.chunk_syms, L.sub_syms), 16));
-        p.even_offset = uint32_t(p.bits_offset + align_up((bits + 7) / 8, 16) + kBitsSlack);
+        p.even_offset = uint32_t(p.bits_offset + align_up((p.huff_bits + 7) / 8, 16) + kBitsSlack);
         p.stripe_bytes = p.even_offset + align_up(p.n, 16);
         pos = align_up(pos, 256);
         p.blob_offset = pos;
         pos += p.stripe_bytes;
     }
     L.total = pos;
+}
+
+uint64_t layout_bound(LayerPlan L) {
+    for (PlanStripe &p : L.stripes) p.huff_bits = uint64_t(K3HUF_MAXLEN) * p.n;
+    place_stripes(L);
+    return L.total;
 }
 
 void write_layer_header(const LayerPlan &L, uint8_t *blob) {

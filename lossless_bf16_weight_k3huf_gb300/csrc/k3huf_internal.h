@@ -97,6 +97,10 @@ void plan_stripes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_s
 // Code lengths from per-stripe high-byte histograms (stripes x 256), then
 // every stripe's bit count, offsets and size.
 void plan_layout(const uint64_t *stripe_hist, LayerPlan &L);
+// Header size, then every stripe's offsets and size from its huff_bits.
+void place_stripes(LayerPlan &L);
+// Container size when every code is K3HUF_MAXLEN bits: no values give more.
+uint64_t layout_bound(LayerPlan L);
 // Bytes [0, L.hdr): layer header, code tables, tensor and stripe directories.
 void write_layer_header(const LayerPlan &L, uint8_t *blob);
 // The 32-byte stripe header.

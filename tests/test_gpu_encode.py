@@ -53,7 +53,8 @@ def test_gpu_encoder_matches_oracle(name):
 
 
 @pytest.mark.parametrize("chunk_syms,sub_syms", [(1, 256), (7, 256), (1000, 200), (4096, 0), (4096, 512),
-                                                (4096, 8), (65536, 256), (1 << 21, 256), (5000, 1000), (64, 16)])
+                                                (4096, 8), (65536, 256), (1 << 21, 256), (5000, 1000), (64, 16),
+                                                (256, 256), (1024, 256), (2048, 256), (4096, 256)])
 def test_gpu_encoder_chunk_sizes(chunk_syms, sub_syms):
     x = workloads.normal_tensor((300_001,), 0.05, 9)
     assert np.array_equal(gpu_blob([x], chunk_syms=chunk_syms, sub_syms=sub_syms),
@@ -95,3 +96,19 @@ def test_gpu_encoder_scratch_reuse_needs_no_clearing():
         got = k3.encode_layer_gpu([dev(x)], scratch=scratch)
         torch.cuda.synchronize()
         assert np.array_equal(got.cpu().numpy(), oracle.encode_layer([x]))
+
+
+@pytest.mark.parametrize("name", ["uniform", "heavy", "multi", "n4097", "single"])
+def test_gpu_encoder_one_call_into_bound_buffer(name):
+    """One call into a buffer of k3huf_encode_bound bytes filled with a
+    sentinel: the container is its prefix, equal to the oracle's, and the
+    bytes after it are not written."""
+    ts = CASES[name]() + ([workloads.dyadic_long_codes(1 << 16)] if name == "uniform" else [])
+    bound = k3.encode_bound([np.asarray(t).size for t in ts])
+    buf = torch.full((bound + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    got = k3.encode_layer_gpu([dev(x) for x in ts], out=buf[:bound])
+    torch.cuda.synchronize()
+    ref = oracle.encode_layer(ts)
+    assert got.numel() == ref.size <= bound
+    assert np.array_equal(got.cpu().numpy(), ref)
+    assert bool((buf[ref.size:] == 0xA5).all())

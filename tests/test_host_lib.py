@@ -259,6 +259,29 @@ def test_encode_scratch_bytes():
     assert e.value.code == k3.E_ARG
 
 
+def test_encode_bound_holds_every_container():
+    """The bound (every code 12 bits) is at least the CPU encoder's
+    container for these values, exceeds it by no more than the bits a
+    12-bit code adds per value (plus alignment), and grows with the sizes."""
+    cases = [
+        [workloads.tiny()],
+        [workloads.uniform_bytes(50_000)],
+        [workloads.dyadic_long_codes(1 << 16)],
+        [workloads.single_symbol(10_000)],
+        [workloads.normal_tensor((n,), 0.02, 5) for n in (1, 4095, 4097, 33)],
+    ]
+    for tensors in cases:
+        sizes = [np.asarray(t).size for t in tensors]
+        for kw in ({}, {"chunk_syms": 1024, "sub_syms": 128}, {"shared_table": True}):
+            blob = k3.encode_layer(tensors, **kw)
+            bound = k3.encode_bound(sizes, **kw)
+            assert blob.size <= bound <= blob.size + sum(12 * n // 8 + 16 + 256 for n in sizes) + 256
+    assert k3.encode_bound([1 << 26]) > k3.encode_bound([1 << 25])
+    with pytest.raises(k3.K3HufError) as e:
+        k3.encode_bound([0])
+    assert e.value.code == k3.E_ARG
+
+
 def test_encode_gpu_argument_checks_need_no_device():
     """Misaligned pointers and short scratch are refused before any CUDA call."""
     L = k3._lib()
