@@ -252,6 +252,28 @@ int k3huf_encode_layer(uint32_t n_tensors, const void *const *h_tensors, const u
 int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
                      uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status, void *stream);
 
+/* Flag of k3huf_gemv_layer_ex: y is set to zero first (y = W x). */
+#define K3HUF_GEMV_ZERO_Y 2u
+
+/* k3huf_gemv_layer with options; not from the articles.
+ *  flags: any of
+ *   K3HUF_GEMV_ZERO_Y: a kernel of the call sets the n_values / cols
+ *     floats of d_y to zero first, so the call computes y = W x;
+ *   K3HUF_DECODE_EARLY_START: the call's kernels are launched with
+ *     programmatic stream serialisation, as k3huf_decode_layer_ex does: the
+ *     GEMV's CTAs may start, read the container and build their tables on
+ *     the SMs the kernel before them frees, and their first global write
+ *     (y, status) waits until that kernel has completed.  With both flags
+ *     the zeroing kernel waits for the kernel before it and the GEMV for the
+ *     zeroing, so back-to-back calls overlap one call's table build with
+ *     the previous call's end.  The caller guarantees that the kernel
+ *     before the call in the stream writes neither the container nor x.
+ *  Other arguments, requirements and errors as for k3huf_gemv_layer;
+ *  K3HUF_E_ARG for an unknown flag. */
+int k3huf_gemv_layer_ex(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                        uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
+                        uint32_t flags, void *stream);
+
 /* GPU encoder: the same container as k3huf_encode_layer (byte for byte),
  * built from bf16 tensors already in device memory.  The article "Kimi K3
  * 纯 CPU 推理中的无损 Trunk 压缩" (section 已实现的部分) packs offline:

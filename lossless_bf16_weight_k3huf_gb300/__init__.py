@@ -32,6 +32,7 @@ EXPORTS = [
     "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
     "k3huf_feed_read", "k3huf_feed_close", "k3huf_ring_create_staged", "k3huf_ring_run_file",
     "k3huf_encode_scratch_bytes", "k3huf_encode_bound", "k3huf_encode_layer_gpu", "k3huf_gemv_layer",
+    "k3huf_gemv_layer_ex",
 ]
 FILE_ALIGN = 4096
 
@@ -110,6 +111,8 @@ def _lib():
                                                  ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, _vp, _sz, _vp, _sz,
                                                  ctypes.POINTER(_sz), _vp]
             L.k3huf_gemv_layer.argtypes = [_vp, _sz, _vp, _sz, ctypes.c_uint32, ctypes.c_uint64, _vp, _vp, _vp, _vp]
+            L.k3huf_gemv_layer_ex.argtypes = [_vp, _sz, _vp, _sz, ctypes.c_uint32, ctypes.c_uint64, _vp, _vp, _vp,
+                                              ctypes.c_uint32, _vp]
             L.k3huf_feed_open.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(_vp)]
             L.k3huf_feed_direct.argtypes = [_vp]
             L.k3huf_feed_read.argtypes = [_vp, ctypes.c_uint64, _sz, _vp, _sz]
@@ -304,12 +307,23 @@ def decode_layer(hdr, d_layer, d_out, d_status, stream=None, layer_bytes: int | 
                "k3huf_decode_layer_ws")
 
 
+GEMV_ZERO_Y = 2
+
+
 def gemv_layer(hdr, d_layer, tensor: int, cols: int, d_x, d_y, d_status, stream=None,
-               layer_bytes: int | None = None) -> None:
+               layer_bytes: int | None = None, zero_y: bool = False, early_start: bool = False) -> None:
     """y += W x with tensor ``tensor`` of the layer as a row-major matrix of
-    ``cols`` columns, decoded on chip (never written out); asynchronous."""
+    ``cols`` columns, decoded on chip (never written out); asynchronous.
+    ``zero_y``: y = W x (the call zeroes y first); ``early_start``: the
+    call's kernels may begin while the kernel before them finishes, which
+    must write neither ``d_layer`` nor ``d_x`` (k3huf_gemv_layer_ex)."""
     h = _host(hdr)
     lb = _nbytes(d_layer) if layer_bytes is None else layer_bytes
+    flags = (GEMV_ZERO_Y if zero_y else 0) | (DECODE_EARLY_START if early_start else 0)
+    if flags:
+        _check(_lib().k3huf_gemv_layer_ex(h.ctypes.data, h.size, _dptr(d_layer), lb, tensor, cols, _dptr(d_x),
+                                          _dptr(d_y), _dptr(d_status), flags, _stream(stream)), "k3huf_gemv_layer_ex")
+        return
     _check(_lib().k3huf_gemv_layer(h.ctypes.data, h.size, _dptr(d_layer), lb, tensor, cols, _dptr(d_x), _dptr(d_y),
                                    _dptr(d_status), _stream(stream)), "k3huf_gemv_layer")
 

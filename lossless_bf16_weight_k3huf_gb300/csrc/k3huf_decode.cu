@@ -1158,13 +1158,42 @@ int launch_syms(DecodeParams &P, cudaStream_t stream, bool early) {
 }
 
 // fused GEMV launches: staged bits and the vector merge only
-int launch_gemv(DecodeParams &P, cudaStream_t stream) {
+int launch_gemv(DecodeParams &P, cudaStream_t stream, bool early = false) {
     switch (g_per) {
-        case 1: return launch<1, true, true, true>(P, stream);
+        case 1: return launch<1, true, true, true>(P, stream, early);
         default:
-            if (P.chunk_syms == 4096 && P.sub_syms == 256) return launch<2, true, true, true, true>(P, stream);
-            return launch<2, true, true, true>(P, stream);
+            if (P.chunk_syms == 4096 && P.sub_syms == 256) return launch<2, true, true, true, true>(P, stream, early);
+            return launch<2, true, true, true>(P, stream, early);
     }
+}
+
+// y = 0 ahead of a GEMV that accumulates into it.  It lets the kernel behind
+// it be scheduled at once and writes only once the kernel before it (which
+// may still be adding into y) has completed.
+__global__ void __launch_bounds__(256) zero_y_kernel(float *y, uint64_t n) {
+    grid_dep_launch();
+    grid_dep_wait();
+    for (uint64_t i = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += uint64_t(gridDim.x) * blockDim.x)
+        y[i] = 0.f;
+}
+
+int launch_zero_y(float *y, uint64_t n, cudaStream_t stream, bool early) {
+    const uint32_t grid = uint32_t(std::min<uint64_t>(64, (n + 255) / 256));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = early ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, zero_y_kernel, y, n);
+    if (e != cudaSuccess) {
+        set_cuda_error(int(e));
+        return K3HUF_E_CUDA;
+    }
+    return K3HUF_OK;
 }
 
 int launch_tasks(DecodeParams &P, cudaStream_t stream, bool early = false) {
@@ -1291,9 +1320,9 @@ extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_sy
     return launch_tasks(P, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
-                                uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
-                                void *stream) {
+namespace {
+int gemv_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes, uint32_t tensor,
+                    uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status, uint32_t flags, void *stream) {
     using namespace k3huf;
     if (!h_layer_hdr || !d_layer || !d_x || !d_y || !d_status || cols == 0) return K3HUF_E_ARG;
     if (!aligned16(d_layer) || !aligned16(d_x) || (reinterpret_cast<uintptr_t>(d_y) & 3u) ||
@@ -1335,8 +1364,28 @@ extern "C" int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const
             items += items_of(e.n_values, cs, ss);
         }
         P.n_items = items;
-        rc = launch_gemv(P, static_cast<cudaStream_t>(stream));
+        if (s0 == 0 && (flags & K3HUF_GEMV_ZERO_Y)) {
+            rc = launch_zero_y(d_y, te.n_values / cols, static_cast<cudaStream_t>(stream),
+                               (flags & K3HUF_DECODE_EARLY_START) != 0);
+            if (rc) return rc;
+        }
+        rc = launch_gemv(P, static_cast<cudaStream_t>(stream), (flags & K3HUF_DECODE_EARLY_START) != 0);
         if (rc) return rc;
     }
     return K3HUF_OK;
+}
+}  // namespace
+
+extern "C" int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                                uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
+                                void *stream) {
+    return gemv_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, tensor, cols, d_x, d_y, d_status, 0u, stream);
+}
+
+extern "C" int k3huf_gemv_layer_ex(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                                   uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
+                                   uint32_t flags, void *stream) {
+    if (flags & ~uint32_t(K3HUF_DECODE_EARLY_START | K3HUF_GEMV_ZERO_Y)) return K3HUF_E_ARG;
+    return gemv_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, tensor, cols, d_x, d_y, d_status, flags,
+                           stream);
 }

@@ -96,3 +96,44 @@ def test_gemv_refuses_unsupported_shapes():
         with pytest.raises(k3.K3HufError) as e:
             k3.gemv_layer(blob[: info["hdr_bytes"]], d_blob, tensor, cols, x, y, st)
         assert e.value.code == k3.E_ARG
+
+
+def test_gemv_ex_zero_y_and_early_start_back_to_back():
+    """k3huf_gemv_layer_ex with both flags, calls back to back on one
+    stream: every call gives y = W x for its own x although y starts as
+    garbage and the call before it is still adding into y (its zeroing
+    waits for that call, its GEMV for the zeroing), interleaved with an
+    early-start decode; a multi-stripe heavy-tail matrix and a two-table
+    layer."""
+    rows, cols = 4097, 8192
+    heavy = workloads.heavy_tail(n=rows * cols).reshape(rows, cols)
+    blob_a = oracle.encode_layer([heavy])
+    blob_b = oracle.encode_layer([workloads.normal_tensor((5, 8192), 0.1, 1), workloads.normal_tensor((96, 16384), 0.03, 2)])
+    cases = [(blob_a, 0, cols), (blob_b, 1, 16384)]
+    xs = {(i, s): x_vector(c, 20 + s + 7 * i) for i, (_, _, c) in enumerate(cases) for s in range(3)}
+    refs = {key: reference(cases[key[0]][0], cases[key[0]][1], cases[key[0]][2], x) for key, x in xs.items()}
+    dev = [(torch.from_numpy(b).cuda(), b[: k3.layer_info(b)["hdr_bytes"]]) for b, _, _ in cases]
+    dec_out = torch.empty(k3.layer_info(blob_b)["out_bytes"], dtype=torch.uint8, device="cuda")
+    dec_ref = torch.from_numpy(oracle.decode_layer(blob_b)[1]).cuda()
+    for _ in range(2):
+        ys, sts = {}, []
+        for s in range(3):
+            for i, (b, t, c) in enumerate(cases):
+                d_blob, hdr = dev[i]
+                y = torch.full((k3.tensor_info(b, t)["n_values"] // c,), float("nan"), dtype=torch.float32, device="cuda")
+                st = torch.zeros(1, dtype=torch.int32, device="cuda")
+                x = torch.from_numpy(xs[(i, s)].view(np.int16)).cuda()
+                k3.gemv_layer(hdr, d_blob, t, c, x, y, st, zero_y=True, early_start=True)
+                ys[(i, s)] = y
+                sts.append(st)
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            k3.decode_layer(dev[1][1], dev[1][0], dec_out, st, early_start=True)
+            sts.append(st)
+        torch.cuda.synchronize()
+        assert all(int(st.item()) == 0 for st in sts)
+        for t in (k3.tensor_info(blob_b, j) for j in range(2)):      # (the gaps between tensors are not written)
+            a0, a1 = t["out_offset"], t["out_offset"] + 2 * t["n_values"]
+            assert torch.equal(dec_out[a0:a1], dec_ref[a0:a1])
+        for key, y in ys.items():
+            ref, mag = refs[key]
+            assert np.all(np.abs(y.cpu().numpy().astype(np.float64) - ref) <= 1e-4 * mag + 1e-30), key

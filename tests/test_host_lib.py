@@ -240,6 +240,13 @@ def test_decode_argument_checks_need_no_device():
     assert ex(bad.ctypes.data, bad.size, 4096, bad.size, 4096, 1 << 20, 4096, None, 0, 1, None) == k3.E_FORMAT
     assert ex(b.ctypes.data, b.size, 4096, b.size - 1, 4096, 1 << 20, 4096, 8192, 68, 0, None) == k3.E_ARG
     assert k3.DECODE_EARLY_START == 1
+    # the GEMV with options: an unknown flag is refused first
+    gx = L.k3huf_gemv_layer_ex
+    assert gx(b.ctypes.data, b.size, 4096, b.size, 0, 8192, 4096, 4096, 4096, 4, None) == k3.E_ARG
+    assert gx(b.ctypes.data, b.size, 4096, b.size, 0, 8192, 4096, 4096, 4096, 1 << 31, None) == k3.E_ARG
+    assert gx(b.ctypes.data, b.size, 4096, b.size, 0, 0, 4096, 4096, 4096, 3, None) == k3.E_ARG   # cols 0
+    assert gx(b.ctypes.data, b.size, 4096, b.size, 0, 8192, 4096, 4098, 4096, 3, None) == k3.E_ARG   # y unaligned
+    assert k3.GEMV_ZERO_Y == 2
     assert L.k3huf_set_decoder_variant(3) == k3.E_ARG
     assert L.k3huf_set_decoder_variant(-1) == k3.E_ARG
 
