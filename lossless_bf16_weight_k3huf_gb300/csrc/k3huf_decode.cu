@@ -509,10 +509,22 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     uint32_t j_me = 0;
     if (pool)
         while (j_me + 1 < P.n_pools && P.pool_cta[j_me + 1] <= blockIdx.x) ++j_me;
+    // everything before a thread's first write to global memory (the status
+    // word, the output, the work area) reads only the container and the
+    // parameters; that write waits for the grid before this one (a no-op
+    // for a grid launched the ordinary way)
+    bool dep_done = false;
+    auto dep = [&]() {
+        if (!dep_done) {
+            grid_dep_wait();
+            dep_done = true;
+        }
+    };
     // the next item of pool j for this warp, or ~0u once the pool is empty
     // (slot p: item p / n of CTA pool_cta[j] + p % n's share)
     auto pool_grab = [&](uint32_t j) -> uint32_t {
         const uint32_t c0 = P.pool_cta[j], nb = uint32_t(P.pool_cta[j + 1]) - c0, max_tail = P.pool_tail[j];
+        dep();
         for (;;) {
             uint32_t p = 0;
             if (lane == 0) p = atomicAdd(P.work + 1 + j, 1u);
@@ -575,6 +587,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             // a pool with items left, the CTA's own first; none once a warp of
             // the CTA has stopped
             if (dead && lane == 0) atomicOr(&s_dead, 1u);
+            dep();
             __syncthreads();
             if (tid == 0) {
                 int pick = -1;
@@ -611,6 +624,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             table_built = table;
         }
         if (steal >= 0 && table_bad) {                // (CTA-uniform) its items cannot be taken
+            dep();
             if (tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
             break;
         }
@@ -638,11 +652,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         }
         __syncthreads();
         const uint32_t nheavy = s_nheavy <= uint32_t(kMaxHeavy) ? s_nheavy : 0u;   // overflow: index order only
-        // everything up to here reads only the container and the parameters;
-        // the first write to global memory (the status word, the output, the
-        // work area) waits for the grid before this one (first phase only)
-        if (item == it0) grid_dep_wait();
-        if (steal < 0 && rebuild && table_bad && tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
+        if (steal < 0 && rebuild && table_bad) {
+            dep();
+            if (tid == 0) atomicOr(P.status, K3HUF_ST_HEADER);
+        }
 
         while (!table_bad && !dead) {
             uint32_t v = 0;
@@ -674,6 +687,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             uint32_t hdr[8];
             for (int i = 0; i < 8; ++i) hdr[i] = s_hdr[ti][i];
             if (!s_hok[ti]) {
+                dep();
                 if (lane == 0 && wi == T.item_begin) atomicOr(P.status, K3HUF_ST_HEADER);
                 continue;
             }
@@ -768,6 +782,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     while (!(landed = mbar_try_wait(&s_bar[warp], phase)) && ++polls < kWaitLimit) {
                     }
                     phase ^= 1u;
+                    dep();                                   // (the first copy went out before it)
                     if (!__all_sync(0xffffffffu, landed)) {
                         if (lane == 0) atomicOr(P.status, K3HUF_ST_TIMEOUT);
                         // let the copy in flight land (again bounded), then stop this warp's work
@@ -784,6 +799,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     __syncwarp();
                 }
 
+                if (!kStaged) dep();
                 const bool in_pass = uint32_t(lane) >= pa && uint32_t(lane) < pb;
                 const uint32_t len = in_pass ? my_len : 0u;
                 uint32_t bp = in_pass ? c_off - byte_lo * 8u : 0u;
@@ -1035,6 +1051,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         item = pend;
     }
     // the last CTA to finish returns the work area to zero for the next launch
+    dep();
     if (pool) {
         __syncthreads();
         if (tid == 0) {
