@@ -174,9 +174,10 @@ int k3huf_decode_layer_ws(const void *h_layer_hdr, size_t hdr_bytes,
  *  flags: 0 or K3HUF_DECODE_EARLY_START.  With that flag the kernels are
  *    launched with programmatic stream serialisation: a kernel's CTAs may
  *    start while the kernel before it in the stream is still running, take
- *    the SMs it frees, and read the container and build their code tables
- *    there; their first write to global memory (status, output, work area)
- *    waits until that kernel has completed.  The caller guarantees that the
+ *    the SMs it frees, read the container, build their code tables and
+ *    decode their first values into shared memory there; their first write
+ *    to global memory (status, output) and their first access to the work
+ *    area wait until that kernel has completed.  The caller guarantees that the
  *    kernel before this call in the stream does not write the container
  *    (d_layer); copies, event waits and kernels of other streams order the
  *    call as usual.  Back-to-back layer decodes, or a decode after the
@@ -267,7 +268,8 @@ int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_la
  *     the zeroing kernel waits for the kernel before it and the GEMV for the
  *     zeroing, so back-to-back calls overlap one call's table build with
  *     the previous call's end.  The caller guarantees that the kernel
- *     before the call in the stream writes neither the container nor x.
+ *     before the call in the stream does not write the container (x is
+ *     read only after that kernel has completed).
  *  Other arguments, requirements and errors as for k3huf_gemv_layer;
  *  K3HUF_E_ARG for an unknown flag. */
 int k3huf_gemv_layer_ex(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,

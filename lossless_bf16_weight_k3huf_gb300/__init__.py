@@ -316,7 +316,7 @@ def gemv_layer(hdr, d_layer, tensor: int, cols: int, d_x, d_y, d_status, stream=
     ``cols`` columns, decoded on chip (never written out); asynchronous.
     ``zero_y``: y = W x (the call zeroes y first); ``early_start``: the
     call's kernels may begin while the kernel before them finishes, which
-    must write neither ``d_layer`` nor ``d_x`` (k3huf_gemv_layer_ex)."""
+    must not write ``d_layer`` (k3huf_gemv_layer_ex)."""
     h = _host(hdr)
     lb = _nbytes(d_layer) if layer_bytes is None else layer_bytes
     flags = (GEMV_ZERO_Y if zero_y else 0) | (DECODE_EARLY_START if early_start else 0)

@@ -782,8 +782,8 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     while (!(landed = mbar_try_wait(&s_bar[warp], phase)) && ++polls < kWaitLimit) {
                     }
                     phase ^= 1u;
-                    dep();                                   // (the first copy went out before it)
                     if (!__all_sync(0xffffffffu, landed)) {
+                        dep();
                         if (lane == 0) atomicOr(P.status, K3HUF_ST_TIMEOUT);
                         // let the copy in flight land (again bounded), then stop this warp's work
                         polls = 0;
@@ -799,7 +799,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     __syncwarp();
                 }
 
-                if (!kStaged) dep();
                 const bool in_pass = uint32_t(lane) >= pa && uint32_t(lane) < pb;
                 const uint32_t len = in_pass ? my_len : 0u;
                 uint32_t bp = in_pass ? c_off - byte_lo * 8u : 0u;
@@ -954,6 +953,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         }
                     }
                     __syncwarp();
+                    // decoding wrote only shared memory: a launch started early
+                    // decodes its first round before the grid ahead of it ends;
+                    // the output stores (the GEMV's reads of x) wait for it
+                    dep();
                     if (kVec && full) {
                         const uint32_t rv = r * kRound;
 #pragma unroll
@@ -1038,6 +1041,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     if (pos != my_end) st |= K3HUF_ST_INDEX;
                 }
                 st = __reduce_or_sync(0xffffffffu, st);
+                if (st) dep();
                 if (lane == 0 && st) atomicOr(P.status, st);
                 __syncwarp();                            // slot free for the next pass / item
                 pa = pb;
@@ -1045,6 +1049,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             if (kGemv) {
 #pragma unroll
                 for (int d = 16; d; d >>= 1) gacc += __shfl_xor_sync(0xffffffffu, gacc, d);
+                dep();
                 if (lane == 0 && gacc != 0.f) atomicAdd(P.gemv_y + grow, gacc);
             }
         }
