@@ -177,6 +177,29 @@ def test_early_start_chain():
         assert int(work.abs().sum().item()) == 0
 
 
+def test_early_start_waits_for_a_reader_of_its_output():
+    """A kernel reads a decode's output right before an early-start decode
+    of another layer overwrites that buffer: the reader sees the first
+    layer's bytes (the decode writes only after the reader has completed)."""
+    a = oracle.encode_layer([workloads.normal_tensor((1 << 23,), 0.02, 51)])
+    b = oracle.encode_layer([workloads.normal_tensor((1 << 23,), 0.7, 52)])
+    ia, ib = k3.layer_info(a), k3.layer_info(b)
+    assert ia["out_bytes"] == ib["out_bytes"]
+    da, db = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    ref_a = torch.from_numpy(oracle.decode_layer(a)[1]).cuda()
+    ref_b = torch.from_numpy(oracle.decode_layer(b)[1]).cuda()
+    out = torch.empty(ia["out_bytes"], dtype=torch.uint8, device="cuda")
+    work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        st = torch.zeros(2, dtype=torch.int32, device="cuda")
+        k3.decode_layer(a[: ia["hdr_bytes"]], da, out, st[0:1], work=work, early_start=True)
+        seen = out.clone()                                # the reader of layer a's output
+        k3.decode_layer(b[: ib["hdr_bytes"]], db, out, st[1:2], work=work, early_start=True)
+        torch.cuda.synchronize()
+        assert int(st.abs().sum().item()) == 0
+        assert torch.equal(seen, ref_a) and torch.equal(out, ref_b)
+
+
 def test_early_start_device_table_fault():
     """Early start with a device table that does not build: the status bit
     is written after the preceding kernel (the status fill) completes, so

@@ -137,3 +137,29 @@ def test_gemv_ex_zero_y_and_early_start_back_to_back():
         for key, y in ys.items():
             ref, mag = refs[key]
             assert np.all(np.abs(y.cpu().numpy().astype(np.float64) - ref) <= 1e-4 * mag + 1e-30), key
+
+
+def test_gemv_ex_reads_x_after_the_kernel_that_writes_it():
+    """x is written by the kernel right before an early-start call (with and
+    without the zeroing kernel between them): every result uses the new x,
+    since the GEMV reads x only after the kernel before it has completed."""
+    rows, cols = 512, 16384
+    w = workloads.normal_tensor((rows, cols), 0.02, 31)
+    blob = oracle.encode_layer([w])
+    info = k3.layer_info(blob)
+    d_blob, hdr = torch.from_numpy(blob).cuda(), blob[: info["hdr_bytes"]]
+    srcs = [torch.from_numpy(x_vector(cols, 40 + i).view(np.int16)).cuda() for i in range(4)]
+    x = torch.zeros(cols, dtype=torch.int16, device="cuda")
+    for zero_y in (True, False):
+        ys = []
+        for i, src in enumerate(srcs):
+            y = torch.zeros(rows, dtype=torch.float32, device="cuda")
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            x.copy_(src)                                  # the kernel before the call writes x
+            k3.gemv_layer(hdr, d_blob, 0, cols, x, y, st, zero_y=zero_y, early_start=True)
+            ys.append((y, st))
+        torch.cuda.synchronize()
+        for i, (y, st) in enumerate(ys):
+            assert int(st.item()) == 0
+            ref, mag = reference(blob, 0, cols, x_vector(cols, 40 + i))
+            assert np.all(np.abs(y.cpu().numpy().astype(np.float64) - ref) <= 1e-4 * mag + 1e-30), (zero_y, i)
