@@ -466,16 +466,38 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
             if (l) acc |= uint64_t(e >> 4) << (64u - na - l);
             na += l;
         };
+        // the lane's own words (after its first) wait in q0..q3, the last
+        // four in order, and leave as one 16-byte store per aligned group of
+        // four (one L1 wavefront instead of four); q_j holds word wi - 4 + j
+        // once wi has moved past the newest
+        uint32_t q0 = 0, q1 = 0, q2 = 0, q3 = 0, pend = 0;
+        auto store_tail = [&](uint32_t last) {    // the pend newest words, the newest at index last
+#pragma unroll
+            for (uint32_t j = 0; j < 4; ++j) {
+                const uint32_t idx = last - 3u + j;
+                if (j + pend >= 4u && idx < n_words) words[idx] = j == 0 ? q0 : j == 1 ? q1 : j == 2 ? q2 : q3;
+            }
+        };
         auto flush = [&]() {                       // at most 55 bits pending: one word at most
             if (na >= 32u) {
                 const uint32_t w = __byte_perm(uint32_t(acc >> 32), 0, 0x0123);
-                if (wi < n_words) {
-                    if (first)
-                        atomicOr(&words[wi], w);
-                    else
-                        words[wi] = w;
+                if (first) {
+                    if (wi < n_words) atomicOr(&words[wi], w);
+                    first = false;
+                } else {
+                    q0 = q1;
+                    q1 = q2;
+                    q2 = q3;
+                    q3 = w;
+                    ++pend;
+                    if ((wi & 3u) == 3u) {         // a group of four ends here
+                        if (pend == 4u && wi < n_words)
+                            *reinterpret_cast<uint4 *>(words + wi - 3u) = make_uint4(q0, q1, q2, q3);
+                        else
+                            store_tail(wi);
+                        pend = 0;
+                    }
                 }
-                first = false;
                 ++wi;
                 acc <<= 32;
                 na -= 32u;
@@ -505,6 +527,7 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
             flush();
             even[v0 + i] = src[0];
         }
+        if (pend) store_tail(wi - 1u);             // words of a group the lane did not finish
         // the last, partial word: shared with the next sub-stream
         if (na && wi < n_words) {
             const uint32_t w = __byte_perm(uint32_t(acc >> 32), 0, 0x0123);
