@@ -37,10 +37,16 @@
 //    per-lane row in shared memory; every 64 values the warp merges its 32
 //    sub-streams' high bytes with their raw low bytes (loads issued one round
 //    early) into coalesced 16-byte bf16 stores;
+//  - launched with early start, a grid's CTAs take the SMs the grid before
+//    it frees, build their tables, copy their first items' bits and decode
+//    their first round there; each thread's first global write and first
+//    access to the work area wait (griddepcontrol.wait) until that grid has
+//    completed;
 //  - a sub-stream that ends away from the next recorded bit offset, or an
 //    undecodable window, sets a status bit; every loop is bounded by value
-//    counts, every shared/global read index is clamped, and the only wait
-//    (the bulk copy's mbarrier) has an iteration limit.
+//    counts, every shared/global read index is clamped, and the one spin
+//    wait (the bulk copy's mbarrier) has an iteration limit (the early-start
+//    wait ends when the grid before, itself bounded, completes).
 #include <cuda_runtime.h>
 
 #include <algorithm>
