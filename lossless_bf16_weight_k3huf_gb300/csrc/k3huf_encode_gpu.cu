@@ -40,6 +40,7 @@ struct EncStripe {
     uint32_t n, n_chunks;
     uint32_t table, bits_offset;
     uint32_t even_offset, chunk_begin;   // first chunk of the stripe in the per-chunk arrays
+    uint32_t span;         // bytes from dst to the next stripe (or the container's end)
 };
 
 struct EncParams {
@@ -175,6 +176,21 @@ __global__ void __launch_bounds__(kPackThreads) sub_bits_kernel(EncParams P) {
         }
         if (lane == 0) P.chunk_bits[T.chunk_begin + c] = total;
     }
+}
+
+// 2'. zeroing for the per-sub-stream packer, in place of clearing the whole
+//     container: every byte of a stripe up to its low bytes (header and
+//     index, written later anyway; the bit stream, whose shared words take
+//     atomic ORs, and its padding) and from the low bytes' last whole 16 to
+//     the next stripe (padding); the low bytes themselves the packer writes
+__global__ void __launch_bounds__(256) zero_gaps_kernel(EncParams P) {
+    const EncStripe &T = P.stripes[blockIdx.y];
+    const uint32_t n1 = T.even_offset / 16u;                       // 16-byte units [0, n1)
+    const uint32_t b0 = (T.even_offset + (T.n & ~15u)) / 16u, b1 = T.span / 16u;
+    const uint32_t total = n1 + (b1 - b0);
+    uint4 *d = reinterpret_cast<uint4 *>(T.dst);
+    for (uint32_t u = blockIdx.x * 256u + threadIdx.x; u < total; u += gridDim.x * 256u)
+        d[u < n1 ? u : b0 + (u - n1)] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // 4. one CTA per stripe: the chunk index (exclusive prefix of the chunks'
@@ -661,22 +677,30 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
             desc[i].huff_bits = p.huff_bits;
             desc[i].bits_offset = p.bits_offset;
             desc[i].even_offset = p.even_offset;
+            desc[i].span = uint32_t((i + 1 < ns ? L.stripes[i + 1].blob_offset : L.total) - p.blob_offset);
         }
+        // the default layout (256-value sub-streams, 1-16 per chunk) packs
+        // one sub-stream per lane; any other layout one chunk per warp
+        const bool per_sub = sub_syms == 256 && chunk_syms % 256 == 0 && P.S <= 16 && (P.S & (P.S - 1)) == 0;
         std::vector<uint8_t> head(size_t(L.hdr));
         write_layer_header(L, head.data());
         e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(scr + SL.codes, codes.data(), codes.size() * sizeof(uint32_t), cudaMemcpyHostToDevice, st);
         if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.flag, 0, sizeof(uint32_t), st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(blob, 0, size_t(L.total), st);
+        if (e == cudaSuccess && !per_sub) e = cudaMemsetAsync(blob, 0, size_t(L.total), st);
         if (e == cudaSuccess) e = cudaMemcpyAsync(blob, head.data(), head.size(), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return cuda_fail(e);
+        if (per_sub) {
+            uint64_t max_units = 1;
+            for (size_t i = 0; i < ns; ++i)
+                max_units = std::max<uint64_t>(max_units, (desc[i].span - (desc[i].n & ~15u)) / 16u);
+            const uint32_t gz = uint32_t(std::min<uint64_t>(1024, (max_units + 255) / 256));
+            zero_gaps_kernel<<<dim3(gz, uint32_t(ns)), 256, 0, st>>>(P);
+        }
         // 3-5. chunk bits, chunk index, packing
         const uint32_t wpb = kPackThreads / 32;
         const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_chunks + wpb - 1) / wpb));
-        // the default layout (256-value sub-streams, 1-16 per chunk) packs
-        // one sub-stream per lane; any other layout one chunk per warp
-        const bool per_sub = sub_syms == 256 && chunk_syms % 256 == 0 && P.S <= 16 && (P.S & (P.S - 1)) == 0;
         if (per_sub) {
             sub_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
             scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
