@@ -788,7 +788,7 @@ def bench_gemv(args, rank, world, local, dev):
                    "l2": "inputs larger than L2"},
         "roofline": {"bound": "hbm", "achieved": round(alg / t_f / 1e9, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(alg / t_f / 1e9 / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": None, "algorithmic_bytes_per_call": alg},
+                     "traffic": ncu_traffic("gemv"), "algorithmic_bytes_per_call": alg},
         "e2e": {"value": round(raw / t_f / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
                 "note": "weights resident compressed in HBM; no host traffic per call"},
         "gpu_launches": 2 * args.steps,                 # zeroing kernel + fused GEMV
