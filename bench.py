@@ -89,8 +89,8 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_src_sha():
-    p = os.path.join(ROOT, "lossless_bf16_weight_k3huf_gb300", "csrc", "k3huf_decode.cu")
+def kernel_src_sha(src="k3huf_decode.cu"):
+    p = os.path.join(ROOT, "lossless_bf16_weight_k3huf_gb300", "csrc", src)
     return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
 
 
@@ -101,7 +101,7 @@ def ncu_traffic(workload):
     try:
         with open(p) as f:
             t = json.load(f).get(workload)
-        if t and t.get("kernel_src_sha") == kernel_src_sha():
+        if t and t.get("kernel_src_sha") == kernel_src_sha(t.get("kernel_src", "k3huf_decode.cu")):
             return float(t["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -696,7 +696,7 @@ def bench_encode(args, rank, world, local, dev):
                    "cpu_encoder_threads": os.cpu_count(), "l2": "inputs larger than L2"},
         "roofline": {"bound": "hbm", "achieved": round(alg / t / 1e9, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(alg / t / 1e9 / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": None, "algorithmic_bytes_per_call": alg},
+                     "traffic": ncu_traffic("encode"), "algorithmic_bytes_per_call": alg},
         "e2e": {"value": round(raw / te / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": raw,
                 "d2h_bytes_per_step": int(blob.numel())},
         "gpu_launches": 5 * args.steps,                 # histogram, gap zeroing, bit counts, scan, packing
