@@ -538,3 +538,43 @@ def test_full_heavy_tail():
 @pytest.mark.slow
 def test_full_trunk_layer():
     _full_size(workloads.trunk_layer())
+
+
+def test_random_layers_every_launch_path():
+    """24 seeded random layers (alphabet size and skew, 1-4 tensors of
+    1-300,000 values, chunk and sub-stream sizes, shared or per-tensor
+    tables) decoded three ways on the GPU: plain, with a work area, and
+    with a work area and early start back to back.  Every tensor's bytes
+    equal the input's."""
+    rng = np.random.default_rng(2026)
+    work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device="cuda")
+    for case in range(24):
+        tensors = []
+        for _ in range(int(rng.integers(1, 5))):
+            n = int(rng.integers(1, 300_001))
+            n_sym = int(rng.integers(1, 257))
+            syms = rng.choice(256, size=n_sym, replace=False)
+            w = float(rng.uniform(0.05, 1.0)) ** np.arange(n_sym, dtype=np.float64)
+            hi = rng.choice(syms, size=n, p=w / w.sum()).astype(np.uint16)
+            tensors.append((hi << 8) | rng.integers(0, 256, size=n, dtype=np.uint16))
+        chunk_syms = int(rng.choice([64, 256, 1000, 4096, 8192]))
+        sub_syms = int(rng.choice([0, 8, 64, 256, 512]))
+        blob = oracle.encode_layer(tensors, chunk_syms=chunk_syms, sub_syms=sub_syms,
+                                   shared_table=bool(rng.integers(0, 2)))
+        info = k3.layer_info(blob)
+        hdr = blob[: info["hdr_bytes"]]
+        d_blob = torch.from_numpy(blob).cuda()
+        outs = [torch.empty(info["out_bytes"], dtype=torch.uint8, device="cuda") for _ in range(3)]
+        st = torch.zeros(3, dtype=torch.int32, device="cuda")
+        k3.decode_layer(hdr, d_blob, outs[0], st[0:1])
+        k3.decode_layer(hdr, d_blob, outs[1], st[1:2], work=work)
+        k3.decode_layer(hdr, d_blob, outs[2], st[2:3], work=work, early_start=True)
+        torch.cuda.synchronize()
+        assert int(st.abs().sum().item()) == 0, case
+        assert int(work.abs().sum().item()) == 0, case
+        for t, x in enumerate(tensors):
+            ti = k3.tensor_info(hdr, t)
+            a, b = ti["out_offset"], ti["out_offset"] + 2 * ti["n_values"]
+            ref = torch.from_numpy(x.view(np.uint8)).cuda()
+            for o in outs:
+                assert torch.equal(o[a:b], ref), (case, t)
