@@ -5,12 +5,15 @@ roofline fraction, and the compression ratio of the workload.
 A step is one pass of the whole decode path over one layer container that
 is already resident in HBM: host-side header validation and launch, the
 per-CTA table build, chunk seek, Huffman decode of the high bytes, merge
-with the raw low bytes, integrity check.  ``e2e`` repeats the step through
+with the raw low bytes, integrity check.  The K timed steps run back to
+back with early start (each launch's table build overlaps the previous
+launch's end) between one pair of CUDA events; ``single_launch_us`` gives
+launches timed one at a time beside it.  ``e2e`` repeats the step through
 the same C ABI with host buffers: pinned host container -> HBM, decode,
 decoded weights -> pinned host, all inside the timed region.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W]
-                       [--workload projection|tiny|heavy_tail|trunk_layer|ring]
+                       [--workload projection|tiny|heavy_tail|trunk_layer|ring|ring_file|gemv|encode]
                        [--impl reference]
 For N > 1 run under torchrun: every rank decodes its own replica (the path
 has no exchange step), timing is the max over ranks and ``value`` counts
