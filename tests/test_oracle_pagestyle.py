@@ -1,8 +1,9 @@
 """Pins of the article-style CPU decoder (oracle/k3huf_pagestyle.c), the
 like-for-like CPU timing beside the bit-serial oracle.
 
-Its table is checked window by window against the oracle's bit-serial code
-walk, its stripe decode byte for byte against the oracle's decode of the
+Its table is checked window by window against the hand-worked examples
+in tests/golden/canonical_examples.txt and against the oracle's bit-serial
+code walk, its stripe decode byte for byte against the oracle's decode of the
 same containers (and both against the original tensors), and its error
 paths on streams the oracle rejects."""
 import numpy as np
@@ -10,6 +11,7 @@ import pytest
 
 import oracle
 import workloads
+from conftest import golden_lines
 
 
 def _stripe0(blob):
@@ -41,6 +43,28 @@ def test_table_matches_bit_serial_walk(name, codelen):
         sym, used = oracle.decode_window(cl, w)
         want = 0 if sym < 0 else (sym << 4) | used
         assert int(lut[w]) == want, (name, w)
+
+
+@pytest.mark.parametrize("row", list(golden_lines("canonical_examples.txt")), ids=lambda r: r[0])
+def test_table_matches_hand_worked_ranges(row):
+    """The hand-worked examples E1-E6 (canonical codes worked out by hand and
+    the 12-bit window ranges they imply): every window of the article-style
+    table holds the symbol and length its range says, 0 where no code
+    starts."""
+    name, maxlen, lens_s, _codes, ranges_s = row
+    cl = np.zeros(256, np.uint8)
+    for tok in lens_s.split():
+        sym, ln = tok.split(":")
+        cl[int(sym)] = int(ln)
+    lut = oracle.pagestyle_table(cl)
+    covered = 0
+    for tok in ranges_s.split():
+        sym, rng = tok.split(":")
+        lo, hi = (int(x) for x in rng.strip("[)").split(","))
+        want = 0 if sym == "x" else (int(sym) << 4) | int(cl[int(sym)])
+        assert (lut[lo:hi] == want).all(), (name, sym, lo, hi)
+        covered += hi - lo
+    assert covered == 4096, name
 
 
 def test_table_rejects_long_lengths():
