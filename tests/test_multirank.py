@@ -70,3 +70,25 @@ def test_cpu_article_style_fields():
     assert r["cores"] == min(2, os.cpu_count() or 1)
     assert "not the oracle" in r["kind"]
     assert "(2 stripes" in r["sample"] and r["sample"].startswith("one core: 64 MiB decoded")
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one
+    JSON line with the contract's keys: impl, metric, value, unit, timing,
+    the cpu_baseline describing the run and an e2e with no host traffic."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["steps"] == 1 and d["n_gpus"] == 1
+    assert d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
