@@ -320,17 +320,22 @@ int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, con
  * 4096-value chunks) is refused with K3HUF_E_ARG.  Arguments, output and
  * errors otherwise as k3huf_encode_layer_gpu; nothing is allocated on the
  * device.  The first call on a device looks up the array's address on that
- * device (make that first call before any stream capture).  All calls share
- * the one array: calls whose work overlaps on the GPU (other streams, other
- * host threads) race and must be serialised by the caller. */
+ * device (make that first call before any stream capture).  The array used
+ * is the current device's copy, so every tensor, the output and the stream
+ * must belong to the current device: a host pointer, another device's
+ * pointer or another device's stream is refused with K3HUF_E_ARG before
+ * any work is issued.  All calls share the one array: calls whose work
+ * overlaps on the GPU (other streams, other host threads) race and must be
+ * serialised by the caller. */
 int k3huf_encode_layer_gpu_noalloc(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
                                    uint32_t chunk_syms, uint32_t sub_syms, int shared_table, void *d_blob,
                                    size_t blob_cap, size_t *blob_bytes, void *stream);
 
 /* Streaming ring: layers held in pinned host memory are copied to device
  * slots with cudaMemcpyAsync on a copy stream while the previous layer is
- * decoded on a compute stream, double buffered (the article's trunk ring,
- * "a second slot is what overlaps reads with compute").
+ * decoded on a compute stream, double buffered.  The kimi-k3-in-c tuning
+ * article (section 2.2) gives its trunk ring a second slot so that reading
+ * the next layer overlaps computing on the current one.
  * k3huf_ring_create allocates n_slots device slots of slot_bytes each and
  * the streams/events it needs. */
 typedef struct k3huf_ring k3huf_ring;

@@ -767,6 +767,28 @@ extern "C" int k3huf_encode_layer_gpu_noalloc(uint32_t n_tensors, const void *co
         }
         scratch = g_fixed_addr[dev];
     }
+    // the address above is the current device's copy of the array, so the
+    // tensors, the output and the stream must belong to that device too
+    if (!d_tensors) return K3HUF_E_ARG;
+    auto on_device = [dev](const void *p) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        return (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) && a.device == dev;
+    };
+    for (uint32_t t = 0; t < n_tensors; ++t)
+        if (!d_tensors[t] || !on_device(d_tensors[t])) return K3HUF_E_ARG;
+    if (d_blob && !on_device(d_blob)) return K3HUF_E_ARG;
+    if (stream) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return K3HUF_E_ARG;
+        }
+        if (sdev != dev) return K3HUF_E_ARG;
+    }
     return k3huf_encode_layer_gpu(n_tensors, d_tensors, n_values, chunk_syms, sub_syms, shared_table, scratch,
                                   kFixedScratchBytes, d_blob, blob_cap, blob_bytes, stream);
 }

@@ -171,6 +171,23 @@ def encode_layer(tensors, chunk_syms: int = 4096, shared_table: bool = False, ma
     return out
 
 
+def container_bytes(tensors, chunk_syms: int = 4096, shared_table: bool = False, maxlen: int = MAXLEN,
+                    sub_syms: int = 256) -> int:
+    """Size in bytes of the container encode_layer would write for these
+    tensors: the encoder's sizing pass alone (histograms, code lengths and
+    the layout's arithmetic), without packing any bits."""
+    ts = [np.ascontiguousarray(t, dtype=np.uint16).reshape(-1) for t in tensors]
+    n = len(ts)
+    ptrs = (_u8p * n)(*[_ptr(t.view(np.uint8)) for t in ts])
+    nv = np.array([t.size for t in ts], dtype=np.uint64)
+    size = ctypes.c_uint64(0)
+    rc = lib().orc_encode_layer(n, ptrs, _ptr(nv, _u64p), chunk_syms, sub_syms, int(shared_table), maxlen,
+                                None, 0, ctypes.byref(size))
+    if rc:
+        raise ValueError(f"oracle encode failed: {rc}")
+    return int(size.value)
+
+
 def layer_info(blob: np.ndarray) -> dict:
     info = np.zeros(10, dtype=np.uint64)
     rc = lib().orc_layer_info(_ptr(blob), blob.size, _ptr(info, _u64p))

@@ -540,6 +540,31 @@ def test_full_trunk_layer():
     _full_size(workloads.trunk_layer())
 
 
+@pytest.mark.slow
+def test_full_ring_trunk_layers():
+    """Three trunk layers (9 tensors, 9 code tables and 28 stripes each,
+    seeds 10-12 of the streaming ring) go from pinned host memory through
+    the ring's two device slots, more layers than slots: every byte of every
+    layer equals its input tensors (checked on the GPU) and sampled chunks of
+    every stripe equal the oracle's bit-serial decode of those chunks."""
+    seeds = workloads.ring_layers(n_layers=3)
+    layers = [workloads.trunk_layer(seed=s) for s in seeds]
+    blobs = [k3.encode_layer(ts) for ts in layers]
+    h = [torch.from_numpy(b).pin_memory() for b in blobs]
+    outs = [torch.full((k3.layer_info(b)["out_bytes"],), SENTINEL, dtype=torch.uint8, device="cuda") for b in blobs]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ring = k3.Ring(max(b.size for b in blobs), 2)
+    stats = ring.run(h, outs, st)
+    ring.close()
+    assert st.item() == 0
+    assert stats["h2d_bytes"] == sum(b.size for b in blobs)
+    assert stats["out_bytes"] == sum(2 * sum(t.size for t in ts) for ts in layers)
+    for i, (ts, b, o) in enumerate(zip(layers, blobs, outs)):
+        info = k3.layer_info(b)
+        assert info["n_tables"] == 9 and info["n_tensors"] == 9 and info["n_stripes"] == 28
+        _sampled_parity(b, ts, o, n_sample=6, seed=i)
+
+
 def test_random_layers_every_launch_path():
     """24 seeded random layers (alphabet size and skew, 1-4 tensors of
     1-300,000 values, chunk and sub-stream sizes, shared or per-tensor

@@ -325,3 +325,25 @@ def test_incomplete_code_invalid_window_is_rejected():
     bad = blob.copy()
     bad[o + st["bits_offset"]] = 0b01011000            # starts with 01: no code
     assert oracle.decode_layer(bad)[0] == oracle.E_FORMAT
+
+
+@pytest.mark.parametrize("case", ["ragged", "chunks", "multi", "shared", "two_stripes"])
+def test_container_bytes_is_the_written_size(case):
+    """The oracle's sizing pass (no bits packed) gives the size of the
+    container its writer produces, whose layout check_layout walks field by
+    field against the closed forms."""
+    kw = {}
+    if case == "ragged":
+        ts = [workloads.normal_tensor((12289,), 0.02, seed=21)]
+    elif case == "chunks":
+        ts = [workloads.normal_tensor((50_001,), 0.05, seed=22)]
+        kw = {"chunk_syms": 1000}
+    elif case in ("multi", "shared"):
+        ts = [workloads.normal_tensor((700, 33), 0.02, seed=23), workloads.single_symbol(5),
+              workloads.dyadic_long_codes(40_000)]
+        kw = {"shared_table": case == "shared"}
+    else:
+        ts = [np.tile(workloads.tiny(), 17)[: STRIPE_VALUES + 4097]]
+    blob = oracle.encode_layer(ts, **kw)
+    check_layout(blob, ts, chunk_syms=kw.get("chunk_syms", 4096), shared=kw.get("shared_table", False))
+    assert oracle.container_bytes(ts, **kw) == blob.size
