@@ -798,10 +798,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                         dead = true;
                         break;
                     }
-                    // stream words MSB-first in each 32-bit word
-                    const uint32_t nw = nbytes / 4;
-#pragma unroll 4
-                    for (uint32_t w = uint32_t(lane); w < nw; w += 32) bitbuf[w] = bswap32(bitbuf[w]);
                     __syncwarp();
                 }
 
@@ -819,10 +815,13 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 const uint32_t wlen = __reduce_max_sync(0xffffffffu, len);
                 const uint32_t n_rounds = (wlen + kRound - 1) / kRound;
 
-                // 64-bit window at bit position `cur` of the staged stream
+                // 64-bit window at bit position `cur` of the staged stream.  The
+                // slot keeps the stream's byte order; each word is put MSB-first
+                // (one byte permute) as a window loads it, which costs fewer
+                // instructions than a pass that swaps the whole slot in place
                 auto window = [&](uint32_t cur, uint32_t &hi, uint32_t &lo) {
                     const uint32_t i = min(cur >> 5, max_word);
-                    const uint32_t w0 = bitbuf[i], w1 = bitbuf[i + 1], w2 = bitbuf[i + 2];
+                    const uint32_t w0 = bswap32(bitbuf[i]), w1 = bswap32(bitbuf[i + 1]), w2 = bswap32(bitbuf[i + 2]);
                     hi = __funnelshift_l(w1, w0, cur);
                     lo = __funnelshift_l(w2, w1, cur);
                 };
@@ -865,10 +864,10 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             } else {
                                 const uint32_t i = min(cur >> 5, max_word);
                                 const uint32_t d = i - rw_i;        // words moved since the last group
-                                const uint32_t n2 = bitbuf[i + 2];
+                                const uint32_t n2 = bswap32(bitbuf[i + 2]);
                                 uint32_t n1 = rw2, n0 = rw1;
-                                if (d >= 2) n1 = bitbuf[i + 1];
-                                if (d >= 3) n0 = bitbuf[i];
+                                if (d >= 2) n1 = bswap32(bitbuf[i + 1]);
+                                if (d >= 3) n0 = bswap32(bitbuf[i]);
                                 if (d == 2) n0 = rw2;
                                 if (d == 0) {
                                     n0 = rw0;
@@ -949,7 +948,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             uint32_t win;
                             if (kStaged) {
                                 const uint32_t i = min(bp >> 5, max_word);
-                                win = __funnelshift_l(bitbuf[i + 1], bitbuf[i], bp);
+                                win = __funnelshift_l(bswap32(bitbuf[i + 1]), bswap32(bitbuf[i]), bp);
                             } else {
                                 win = gb.window();
                             }

@@ -66,3 +66,25 @@ def test_noalloc_encoder_refuses_layers_beyond_its_scratch(noalloc):
     ptrs = (ctypes.c_void_p * 1)(1 << 20)
     size = ctypes.c_size_t(0)
     assert noalloc(1, ptrs, nv, 4096, 256, 0, None, 0, ctypes.byref(size), None) == k3.E_ARG
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")
+def test_noalloc_encoder_refuses_host_pointers(noalloc):
+    """The fixed array used is the current device's copy, so every pointer
+    must be device memory of the current device: a host pointer given as
+    the tensor, or as the output, is refused before any work is issued."""
+    x = np.ascontiguousarray(workloads.normal_tensor((4096,), 0.02, 13)).view(np.int16)
+    d = torch.from_numpy(x).cuda()
+    size = ctypes.c_size_t(0)
+    nv = (ctypes.c_uint64 * 1)(x.size)
+    stream = torch.cuda.current_stream().cuda_stream
+    host = np.zeros(1 << 16, dtype=np.uint8)
+    host_addr = host.ctypes.data + (-host.ctypes.data) % 256
+    ptrs = (ctypes.c_void_p * 1)(host.ctypes.data + (-host.ctypes.data) % 16)
+    assert noalloc(1, ptrs, nv, 4096, 256, 0, None, 0, ctypes.byref(size), stream) == k3.E_ARG
+    ptrs = (ctypes.c_void_p * 1)(d.data_ptr())
+    assert noalloc(1, ptrs, nv, 4096, 256, 0, None, 0, ctypes.byref(size), stream) == k3.OK
+    assert 0 < size.value <= host.size - 256
+    assert noalloc(1, ptrs, nv, 4096, 256, 0, host_addr, size.value, ctypes.byref(size), stream) == k3.E_ARG
+    torch.cuda.synchronize()
