@@ -46,8 +46,9 @@ struct EncStripe {
 struct EncParams {
     const EncStripe *stripes;
     const uint32_t *codes;     // n_tables x 256: (code << 4) | length
-    uint32_t *counts;          // n_stripes x 256
-    uint32_t *chunk_bits;      // bits of every chunk
+    uint32_t *counts;          // n_stripes x 256 (after the histogram pass: the one-pass
+                               // packer's per-stripe chunk counters)
+    uint32_t *chunk_bits;      // bits of every chunk (or, one-pass packer: 64-bit records)
     uint32_t *chunk_start;     // first bit of every chunk within its stripe's stream
     uint32_t *flag;            // nonzero: the packed bits disagree with the plan
     uint32_t chunk_syms, sub_syms, S;
@@ -74,8 +75,10 @@ ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_chunk
     s.stripes = take(n_stripes * sizeof(EncStripe));
     s.counts = take(n_stripes * 256 * sizeof(uint32_t));
     s.codes = take(n_tables * 256 * sizeof(uint32_t));
-    s.chunk_bits = take(size_t(n_chunks) * sizeof(uint32_t));
-    s.chunk_start = take(size_t(n_chunks) * sizeof(uint32_t));
+    // two words per chunk: the bit count and first bit of each chunk, or,
+    // for the one-pass packer, one 64-bit look-back record per chunk
+    s.chunk_bits = take(size_t(n_chunks) * 2 * sizeof(uint32_t));
+    s.chunk_start = s.chunk_bits + size_t(n_chunks) * sizeof(uint32_t);
     s.flag = take(sizeof(uint32_t));
     s.total = at;
     return s;
@@ -552,6 +555,249 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
     }
 }
 
+// 3''-5''. the default layout with 4096-value chunks (16 sub-streams of 256
+//    values) in one pass, in place of 3'-5': bit counts, chunk index,
+//    sub-stream index and packing.  The chunks' first bits form a prefix
+//    sum along each stripe, taken here by decoupled look-back: each warp
+//    takes the stripe's next chunk from a counter, so every chunk before it
+//    is already held by a running warp, publishes the chunk's bit count,
+//    then sums its predecessors' published counts back to the nearest one
+//    whose first bit is known, and publishes its own first bit and end.
+//    Per chunk and warp:
+//  - its 8 KB of values are copied into shared memory (cp.async, coalesced
+//    16-byte pieces) as 32 rows of 128 values, one per lane, rows padded to
+//    272 bytes so that the lanes' reads of their rows never conflict;
+//  - lane l owns values [128 l, 128 l + 128): half of sub-stream l / 2.  It
+//    codes them in order into a private run of words (rows of 49 words, so
+//    the lanes' stores fall in different banks), two codes at a time (at
+//    most 24 bits, so 32-bit shifts suffice); its bit count comes out of
+//    the same pass;
+//  - a warp scan of the lanes' counts and the look-back give every lane its
+//    first bit; the low bytes leave from the staged rows (coalesced 8-byte
+//    stores), and the rows then take the chunk's stream words: each lane
+//    shifts its run into place (funnel shifts; only its first and last
+//    words, which neighbouring lanes share, by shared atomic OR);
+//  - the stream words leave with coalesced stores; only the chunk's first
+//    and last words, which the neighbouring chunks may share, are OR-ed
+//    atomically into the zeroed container.
+//    The input is read from DRAM once, here, after the histogram pass.
+constexpr int kLbWarps = 12;
+constexpr int kLbThreads = 32 * kLbWarps;
+constexpr uint32_t kLbRow = 272;                          // a lane's 128 values (256 bytes) + 16 of padding
+constexpr uint32_t kLbIn = 32 * kLbRow;                   // one chunk's values, then its stream words
+constexpr uint32_t kLbRun = 49;                           // words of a lane's private run (128 x 12 bits + 1)
+constexpr uint32_t kLbWarpBytes = kLbIn + 4 * 32 * kLbRun;
+constexpr size_t kLbSmem = size_t(256) * 32 * 4 + size_t(kLbWarps) * kLbWarpBytes;
+static_assert(kLbWarpBytes % 16 == 0, "per-warp staging must stay 16-byte aligned");
+static_assert(4096 * K3HUF_MAXLEN / 32 + 2 <= kLbIn / 4, "a chunk's stream words fit the staged rows");
+constexpr uint32_t kLbSpin = 1u << 22;                    // look-back polls before giving up
+constexpr uint64_t kLbAgg = 1ull << 62, kLbIncl = 2ull << 62;  // record: status | 32-bit value
+
+__device__ __forceinline__ uint32_t lb_smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// 16-byte global -> shared copy of src_bytes (0-16) bytes, the rest zero
+__device__ __forceinline__ void lb_cp16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(lb_smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void lb_cp_wait() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// A lane's private run of stream words, written MSB-first from bit 0: whole
+// words go to the run, the partial one waits in `pend` (np bits at its top).
+// Codes arrive in pairs: two codes of at most 12 bits are one string of at
+// most 24, so 32-bit shifts do all the work.
+struct LbRun {
+    uint32_t pend, np, wi;
+    // append the len low bits of v (1 <= len <= 24)
+    __device__ __forceinline__ void append(uint32_t v, uint32_t len, uint32_t *run) {
+        const uint32_t pl = v << (32u - len);                 // left-aligned
+        const uint32_t w = pend | (pl >> np), t = np + len;
+        if (t >= 32u) {                                       // (then np >= 8: pl << (32 - np) is defined)
+            run[wi++] = w;
+            pend = pl << (32u - np);
+            np = t - 32u;
+        } else {
+            pend = w;
+            np = t;
+        }
+    }
+    // the pair of entries (code << 4) | length, the first code first
+    __device__ __forceinline__ void pair(uint32_t e0, uint32_t e1, uint32_t *run) {
+        const uint32_t l1 = e1 & 15u;
+        append(((e0 >> 4) << l1) | (e1 >> 4), (e0 & 15u) + l1, run);
+    }
+};
+
+__global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
+    extern __shared__ __align__(16) uint8_t lb_smem[];
+    uint32_t(*code)[32] = reinterpret_cast<uint32_t(*)[32]>(lb_smem);   // entry s of lane l at code[s][l]
+    const EncStripe &T = P.stripes[blockIdx.y];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int s = threadIdx.x; s < 256; s += kLbThreads) {
+        const uint32_t e = P.codes[size_t(T.table) * 256 + s];
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) code[s][(j + lane) & 31] = e;
+    }
+    __syncthreads();
+    uint8_t *const in = lb_smem + size_t(256) * 32 * 4 + size_t(warp) * kLbWarpBytes;
+    uint32_t *const sw = reinterpret_cast<uint32_t *>(in);           // the chunk's stream words, after the rows
+    uint32_t *const run = reinterpret_cast<uint32_t *>(in + kLbIn) + lane * kLbRun;
+    uint32_t *chunk_idx = reinterpret_cast<uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
+    uint16_t *sub_idx = reinterpret_cast<uint16_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES + 4ull * T.n_chunks);
+    uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
+    const uint32_t n_words = (T.even_offset - T.bits_offset) / 4;    // the stream region, padding included
+    uint8_t *even = T.dst + T.even_offset;
+    unsigned long long *rec = reinterpret_cast<unsigned long long *>(P.chunk_bits) + T.chunk_begin;
+    const uint8_t *row = in + lane * kLbRow;
+    for (;;) {
+        uint32_t c = 0;
+        if (lane == 0) c = atomicAdd(P.counts + blockIdx.y, 1u);
+        c = __shfl_sync(0xffffffffu, c, 0);
+        if (c >= T.n_chunks) break;
+        const uint32_t a = c * 4096u, nv = min(4096u, T.n - a);
+        {
+            // 1. the chunk's values: 16-byte piece u to row u / 16, column u % 16
+            const uint32_t nbytes = 2 * nv;
+            const uint8_t *src = T.src + 2 * size_t(a);
+#pragma unroll 4
+            for (uint32_t k = 0; k < 16; ++k) {
+                const uint32_t u = k * 32 + uint32_t(lane), off = u * 16;
+                const uint32_t sb = off < nbytes ? min(16u, nbytes - off) : 0u;
+                lb_cp16(in + (u >> 4) * kLbRow + (u & 15) * 16, sb ? src + off : src, sb);
+            }
+            lb_cp_wait();
+            __syncwarp();
+        }
+        // 2. this lane's values [128 lane, 128 lane + m) of the chunk, coded
+        //    in order into its run, two at a time
+        const uint32_t v0 = 128u * uint32_t(lane);
+        const uint32_t m = v0 < nv ? min(128u, nv - v0) : 0u;
+        LbRun R{0u, 0u, 0u};
+        if (m == 128u) {
+#pragma unroll 2
+            for (uint32_t j = 0; j < 16; ++j) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(row + 16 * j);
+                const uint32_t q[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) R.pair(code[(q[i] >> 8) & 0xFFu][lane], code[q[i] >> 24][lane], run);
+            }
+        } else {
+            // a stripe's ragged end: one code at a time
+            for (uint32_t v = 0; v < m; ++v) {
+                const uint32_t e = code[row[2 * v + 1]][lane];
+                R.append(e >> 4, e & 15u, run);
+            }
+        }
+        if (R.np) run[R.wi] = R.pend;
+        const uint32_t bits = 32u * R.wi + R.np;
+        // 3. the lane's first bit within the chunk, and the chunk's bits
+        uint32_t incl = bits;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += t;
+        }
+        const uint32_t lo = incl - bits, total = __shfl_sync(0xffffffffu, incl, 31);
+        // 4. the chunk's first bit within the stripe's stream: look-back
+        uint32_t start = 0;
+        if (c == 0) {
+            if (lane == 0) atomicExch(rec, kLbIncl | total);
+        } else {
+            if (lane == 0) atomicExch(rec + c, kLbAgg | total);
+            int64_t j = int64_t(c) - 1;
+            uint32_t polls = 0;
+            for (;;) {
+                const int64_t idx = j - lane;
+                const unsigned long long r =
+                    idx >= 0 ? *reinterpret_cast<volatile unsigned long long *>(rec + idx) : kLbIncl;
+                if (__any_sync(0xffffffffu, (r >> 62) == 0)) {
+                    if (++polls >= kLbSpin) {              // (a predecessor never published: give up)
+                        if (lane == 0) atomicOr(P.flag, 1u);
+                        break;
+                    }
+                    __nanosleep(32);
+                    continue;
+                }
+                const uint32_t incl_mask = __ballot_sync(0xffffffffu, (r >> 62) == 2);
+                const uint32_t upto = incl_mask ? uint32_t(__ffs(incl_mask)) - 1 : 31u;
+                start += __reduce_add_sync(0xffffffffu, uint32_t(lane) <= upto ? uint32_t(r) : 0u);
+                if (incl_mask) break;
+                j -= 32;
+            }
+            if (lane == 0) atomicExch(rec + c, kLbIncl | (start + total));
+        }
+        // 5. chunk index, sub-stream index (sub-stream k starts at lane 2k's
+        //    first bit; one that starts at or past the chunk's end, at its
+        //    end), the stripe header with the first chunk, the plan's total
+        //    checked with the last
+        if (lane == 0) chunk_idx[c] = start;
+        if ((lane & 1) == 0 && lane > 0) sub_idx[size_t(c) * 15 + (lane >> 1) - 1] = uint16_t(lo);
+        if (lane == 0 && c == 0) {
+            uint32_t *h = reinterpret_cast<uint32_t *>(T.dst);
+            h[0] = kStripeMagic;
+            h[1] = T.table;
+            h[2] = T.n;
+            h[3] = T.n_chunks;
+            h[4] = uint32_t(T.huff_bits);
+            h[5] = uint32_t(T.huff_bits >> 32);
+            h[6] = T.bits_offset;
+            h[7] = T.even_offset;
+        }
+        if (lane == 0 && c + 1 == T.n_chunks && uint64_t(start) + total != T.huff_bits) atomicOr(P.flag, 1u);
+        // 6. low bytes of the chunk, 8 per lane and step
+#pragma unroll 4
+        for (uint32_t k = 0; k < 16; ++k) {
+            const uint32_t u = k * 32 + uint32_t(lane), vv = 8 * u;
+            if (vv >= nv) continue;
+            const uint4 x = *reinterpret_cast<const uint4 *>(in + (u >> 4) * kLbRow + (u & 15) * 16);
+            const uint32_t l0 = __byte_perm(x.x, x.y, 0x6420), l1 = __byte_perm(x.z, x.w, 0x6420);
+            if (vv + 8 <= nv) {
+                *reinterpret_cast<uint2 *>(even + a + vv) = make_uint2(l0, l1);
+            } else {
+                for (uint32_t i = 0; vv + i < nv; ++i) even[a + vv + i] = uint8_t((i < 4 ? l0 : l1) >> (8 * (i & 3)));
+            }
+        }
+        __syncwarp();
+        // 7. the rows take the chunk's stream words (staging bit b is stream
+        //    bit (start & ~31) + b): each lane shifts its run into place
+        const uint32_t sh = start & 31u, n_sw = (sh + total + 31u) >> 5;
+        for (uint32_t k = lane; k < n_sw; k += 32) sw[k] = 0u;
+        __syncwarp();
+        if (bits) {
+            const uint32_t o = sh + lo, d0 = o >> 5, r = o & 31u, kw = (bits + 31u) >> 5;
+            uint32_t prev = 0;
+            for (uint32_t i = 0; i <= kw; ++i) {
+                const uint32_t cur = i < kw ? run[i] : 0u;
+                const uint32_t w = __funnelshift_r(cur, prev, r);   // (prev:cur) >> r, low word
+                prev = cur;
+                // (the word after the run's last one holds bits only when they spill over)
+                if (i == kw && (r == 0u || ((bits & 31u) != 0u && (bits & 31u) + r <= 32u))) break;
+                if (i == 0 || i + 1 >= kw) atomicOr(&sw[d0 + i], w);
+                else sw[d0 + i] = w;
+            }
+        }
+        __syncwarp();
+        // 8. the stream words out, in the stream's byte order (the staging
+        //    words hold their first bit at the top); the first and the last
+        //    may hold the neighbouring chunks' bits too
+        const uint32_t w0 = start >> 5;
+        for (uint32_t k = lane; k < n_sw; k += 32) {
+            const uint32_t gw = w0 + k;
+            if (gw >= n_words) continue;
+            const uint32_t w = __byte_perm(sw[k], 0, 0x0123);
+            if (k == 0 || k + 1 == n_sw) {
+                if (w) atomicOr(&words[gw], w);
+            } else {
+                words[gw] = w;
+            }
+        }
+        __syncwarp();                                 // the rows and the runs free again
+    }
+}
+
 int cuda_fail(cudaError_t e) {
     set_cuda_error(int(e));
     return K3HUF_E_CUDA;
@@ -701,7 +947,22 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         // 3-5. chunk bits, chunk index, packing
         const uint32_t wpb = kPackThreads / 32;
         const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_chunks + wpb - 1) / wpb));
-        if (per_sub) {
+        const bool one_pass = per_sub && chunk_syms == 4096;
+        if (one_pass) {
+            // per-stripe chunk counters (the histograms' place) and look-back records start at zero
+            e = cudaMemsetAsync(scr + SL.counts, 0, ns * sizeof(uint32_t), st);
+            if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.chunk_bits, 0, size_t(n_chunks) * 8, st);
+            if (e != cudaSuccess) return cuda_fail(e);
+            int dev = 0, sms = 0;
+            e = cudaGetDevice(&dev);
+            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(pack_lb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kLbSmem));
+            if (e != cudaSuccess) return cuda_fail(e);
+            const uint32_t per = std::max<uint32_t>(1, (2u * uint32_t(std::max(1, sms)) + uint32_t(ns) - 1) / uint32_t(ns));
+            const uint32_t gl = std::min<uint32_t>(per, std::max<uint32_t>(1, (max_chunks + kLbWarps - 1) / kLbWarps));
+            pack_lb_kernel<<<dim3(gl, uint32_t(ns)), kLbThreads, kLbSmem, st>>>(P);
+        } else if (per_sub) {
             sub_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
             scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
             const uint64_t max_sub = uint64_t(max_chunks) * P.S;
