@@ -1010,6 +1010,33 @@ def bench_gemv(args, rank, world, local, dev):
         t_f = timed(fused, args.steps)
     t_u = timed(unfused, args.steps)
     t_mv = timed(lambda: torch.mv(W, x_bf), args.steps)
+
+    # several vectors at once: one decode of W for all of them (k3huf_gemv_layer_batch)
+    # against decode into HBM + cuBLAS GEMM, and cuBLAS on the uncompressed weights
+    curve = []
+    for n_vec in (2, 4, 8):
+        xs = np.concatenate([workloads.normal_tensor((cols,), 1.0, 4 + b).reshape(-1) for b in range(n_vec)])
+        X = torch.from_numpy(xs.view(np.int16)).to(dev).view(n_vec, cols)
+        Xb = X.view(torch.bfloat16)
+        Y = torch.zeros((n_vec, rows), dtype=torch.float32, device=dev)
+        k3.gemv_layer_batch(hdr, d_blob, 0, cols, X, Y, st, zero_y=True)
+        refB = (W.float() @ Xb.float().t()).t()
+        magB = (W.float().abs() @ Xb.float().abs().t()).t()
+        torch.cuda.synchronize()
+        if st.item() != 0 or not bool(((Y - refB).abs() <= 1e-4 * magB + 1e-30).all()):
+            raise SystemExit(f"batched fused GEMV ({n_vec} vectors) disagrees with decode + matmul")
+        del refB, magB
+        tb_f = timed(lambda: k3.gemv_layer_batch(hdr, d_blob, 0, cols, X, Y, st, zero_y=True, early_start=True),
+                     args.steps)
+
+        def unfused_b():
+            k3.decode_layer(hdr, d_blob, d_out, st)
+            torch.mm(W, Xb.t())
+
+        tb_u = timed(unfused_b, args.steps)
+        tb_c = timed(lambda: torch.mm(W, Xb.t()), args.steps)
+        curve.append({"n_vec": n_vec, "fused_ms": round(tb_f * 1e3, 4), "decode_then_cublas_ms": round(tb_u * 1e3, 4),
+                      "cublas_uncompressed_ms": round(tb_c * 1e3, 4)})
     raw = 2 * rows * cols
     peak, peak_kind = measured_peak()
     alg = info["blob_bytes"] + 2 * cols + 4 * rows * 2          # container, x, y read and written
@@ -1024,6 +1051,9 @@ def bench_gemv(args, rank, world, local, dev):
                    "cublas_gemv_bf16_ms": round(t_mv * 1e3, 4),
                    "call": "k3huf_gemv_layer_ex (y zeroed by the call, early start)",
                    "note": "unfused = k3huf_decode_layer into HBM, then torch.mv (cuBLAS) on the bf16 weights",
+                   "batch_curve": [{"n_vec": 1, "fused_ms": round(t_f * 1e3, 4),
+                                    "decode_then_cublas_ms": round(t_u * 1e3, 4),
+                                    "cublas_uncompressed_ms": round(t_mv * 1e3, 4)}] + curve,
                    "l2": "inputs larger than L2"},
         "roofline": {"bound": "hbm", "achieved": round(alg / t_f / 1e9, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(alg / t_f / 1e9 / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",

@@ -276,6 +276,21 @@ int k3huf_gemv_layer_ex(const void *h_layer_hdr, size_t hdr_bytes, const void *d
                         uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
                         uint32_t flags, void *stream);
 
+/* Y += W X for n_vec vectors at once, W decoded on chip once for all of
+ * them; not from the articles (their consumer copies decoded weights into
+ * a framework tensor).  d_x: n_vec bf16 vectors of cols values, back to back
+ * (vector b at d_x + 2 * b * cols bytes, 16-byte aligned); d_y: n_vec fp32
+ * vectors of rows = n_values / cols entries, back to back (vector b at
+ * d_y + b * rows).  n_vec is 1, 2, 4 or 8; above 1 the layer must use the
+ * default chunk and sub-stream sizes (4096 / 256) and the default decoder
+ * (two codes per lookup).  Flags as for k3huf_gemv_layer_ex
+ * (K3HUF_GEMV_ZERO_Y zeroes all n_vec vectors of Y first).  Other arguments,
+ * requirements and errors as for k3huf_gemv_layer; K3HUF_E_ARG for another
+ * n_vec or layout. */
+int k3huf_gemv_layer_batch(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                           uint32_t tensor, uint64_t cols, const void *d_x, uint32_t n_vec, float *d_y,
+                           uint32_t *d_status, uint32_t flags, void *stream);
+
 /* GPU encoder: the same container as k3huf_encode_layer (byte for byte),
  * built from bf16 tensors already in device memory.  The article "Kimi K3
  * 纯 CPU 推理中的无损 Trunk 压缩" (section 已实现的部分) packs offline:

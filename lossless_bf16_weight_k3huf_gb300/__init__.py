@@ -32,7 +32,7 @@ EXPORTS = [
     "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
     "k3huf_feed_read", "k3huf_feed_close", "k3huf_ring_create_staged", "k3huf_ring_run_file",
     "k3huf_encode_scratch_bytes", "k3huf_encode_bound", "k3huf_encode_layer_gpu", "k3huf_gemv_layer",
-    "k3huf_gemv_layer_ex",
+    "k3huf_gemv_layer_ex", "k3huf_gemv_layer_batch",
 ]
 FILE_ALIGN = 4096
 
@@ -113,6 +113,8 @@ def _lib():
             L.k3huf_gemv_layer.argtypes = [_vp, _sz, _vp, _sz, ctypes.c_uint32, ctypes.c_uint64, _vp, _vp, _vp, _vp]
             L.k3huf_gemv_layer_ex.argtypes = [_vp, _sz, _vp, _sz, ctypes.c_uint32, ctypes.c_uint64, _vp, _vp, _vp,
                                               ctypes.c_uint32, _vp]
+            L.k3huf_gemv_layer_batch.argtypes = [_vp, _sz, _vp, _sz, ctypes.c_uint32, ctypes.c_uint64, _vp,
+                                                 ctypes.c_uint32, _vp, _vp, ctypes.c_uint32, _vp]
             L.k3huf_feed_open.argtypes = [ctypes.c_char_p, ctypes.c_int, ctypes.POINTER(_vp)]
             L.k3huf_feed_direct.argtypes = [_vp]
             L.k3huf_feed_read.argtypes = [_vp, ctypes.c_uint64, _sz, _vp, _sz]
@@ -326,6 +328,20 @@ def gemv_layer(hdr, d_layer, tensor: int, cols: int, d_x, d_y, d_status, stream=
         return
     _check(_lib().k3huf_gemv_layer(h.ctypes.data, h.size, _dptr(d_layer), lb, tensor, cols, _dptr(d_x), _dptr(d_y),
                                    _dptr(d_status), _stream(stream)), "k3huf_gemv_layer")
+
+
+def gemv_layer_batch(hdr, d_layer, tensor: int, cols: int, d_x, d_y, d_status, stream=None,
+                     layer_bytes: int | None = None, zero_y: bool = False, early_start: bool = False) -> None:
+    """Y += W X for several vectors with one decode of W (k3huf_gemv_layer_batch):
+    ``d_x`` a CUDA bf16 tensor of n_vec x cols (n_vec 1, 2, 4 or 8), ``d_y`` a
+    CUDA float32 tensor of n_vec x rows; ``zero_y``: Y = W X."""
+    h = _host(hdr)
+    lb = _nbytes(d_layer) if layer_bytes is None else layer_bytes
+    n_vec = _nbytes(d_x) // (2 * cols)
+    flags = (GEMV_ZERO_Y if zero_y else 0) | (DECODE_EARLY_START if early_start else 0)
+    _check(_lib().k3huf_gemv_layer_batch(h.ctypes.data, h.size, _dptr(d_layer), lb, tensor, cols, _dptr(d_x), n_vec,
+                                         _dptr(d_y), _dptr(d_status), flags, _stream(stream)),
+           "k3huf_gemv_layer_batch")
 
 
 def decode_stripe(codelen, chunk_syms: int, sub_syms: int, d_stripe, stripe_bytes: int, n_values: int, d_out,

@@ -112,9 +112,11 @@ struct DecodeParams {
     uint32_t sub_syms;
     uint32_t n_items;
     uint8_t inline_table[256];
-    const uint8_t *gemv_x;      // fused GEMV: device bf16 x[cols], or null
-    float *gemv_y;              // fused GEMV: device y[rows], accumulated
+    const uint8_t *gemv_x;      // fused GEMV: device bf16 x[cols] (vector b at gemv_x + b * gemv_ldx), or null
+    float *gemv_y;              // fused GEMV: device y[rows] (vector b at gemv_y + b * gemv_ldy), accumulated
     uint64_t gemv_cols;
+    uint64_t gemv_ldx;          // bytes from one x vector to the next
+    uint64_t gemv_ldy;          // floats from one y vector to the next
     uint32_t *work;             // work area: [0] CTAs finished, [1 + j] next slot of pool j
                                 // (all left zero), or null
     uint32_t n_pools;
@@ -476,7 +478,7 @@ __device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, con
 // kFixed: the container's default sizes (chunks of 4096 values, sub-streams
 // of 256) as compile-time constants, so that sub-stream and piece offsets
 // fold into immediates and divisions by them into shifts
-template <int kPer, bool kVec, bool kStaged, bool kGemv, bool kFixed = false, bool kPool = false>
+template <int kPer, bool kVec, bool kStaged, int kGemv, bool kFixed = false, bool kPool = false>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -710,7 +712,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             const uint32_t g0 = (wi - T.item_begin) * kItem;
             // fused GEMV: the item lies inside one row of the matrix (the row
             // length is a multiple of the item's span)
-            float gacc = 0.f;
+            float gacc[kGemv > 0 ? kGemv : 1] = {};
             uint64_t grow = 0, gcol0 = 0;
             if (kGemv) {
                 const uint64_t f0 = uint64_t(T.tensor_stripe) * K3HUF_STRIPE_VALUES + uint64_t(g0) * ss;
@@ -973,9 +975,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             o.y = interleave_hi(ev[i].x, h.x);
                             o.z = interleave_lo(ev[i].y, h.y);
                             o.w = interleave_hi(ev[i].y, h.y);
-                            if (kGemv)
-                                gacc = dot8(o, __ldg(reinterpret_cast<const uint4 *>(x_p0 + 2 * (size_t(i) * pstride + rv))), gacc);
-                            else
+                            if (kGemv) {
+#pragma unroll
+                                for (int b = 0; b < kGemv; ++b)
+                                    gacc[b] = dot8(o, __ldg(reinterpret_cast<const uint4 *>(x_p0 + b * P.gemv_ldx + 2 * (size_t(i) * pstride + rv))), gacc[b]);
+                            } else
                                 *reinterpret_cast<uint4 *>(out_p0 + 2 * (size_t(i) * pstride + rv)) = o;
                         }
                         if (__all_sync(0xffffffffu, rem >= uint32_t(2 * kRound))) {
@@ -1000,7 +1004,6 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                             o.z = interleave_lo(ev[i].y, hy);
                             o.w = interleave_hi(ev[i].y, hy);
                             if (kGemv) {
-                                const uint4 xv = __ldg(reinterpret_cast<const uint4 *>(P.gemv_x + 2 * (gcol0 + size_t(gw) * ss + v)));
                                 uint4 wv = o;
                                 if (v + 8 > m_len) {          // weights past the sub-stream's end count zero
                                     const uint32_t kk = m_len - v;
@@ -1009,7 +1012,9 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                                     wv.z = kk >= 6 ? wv.z : kk == 5 ? (wv.z & 0xFFFFu) : 0u;
                                     wv.w = kk >= 8 ? wv.w : kk == 7 ? (wv.w & 0xFFFFu) : 0u;
                                 }
-                                gacc = dot8(wv, xv, gacc);
+#pragma unroll
+                                for (int b = 0; b < kGemv; ++b)
+                                    gacc[b] = dot8(wv, __ldg(reinterpret_cast<const uint4 *>(P.gemv_x + b * P.gemv_ldx + 2 * (gcol0 + size_t(gw) * ss + v))), gacc[b]);
                                 continue;
                             }
                             uint8_t *dst = out + 2 * (size_t(g0 + gw) * ss + v);
@@ -1053,9 +1058,14 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
             }
             if (kGemv) {
 #pragma unroll
-                for (int d = 16; d; d >>= 1) gacc += __shfl_xor_sync(0xffffffffu, gacc, d);
+                for (int b = 0; b < kGemv; ++b)
+#pragma unroll
+                    for (int d = 16; d; d >>= 1) gacc[b] += __shfl_xor_sync(0xffffffffu, gacc[b], d);
                 dep();
-                if (lane == 0 && gacc != 0.f) atomicAdd(P.gemv_y + grow, gacc);
+                if (lane == 0)
+#pragma unroll
+                    for (int b = 0; b < kGemv; ++b)
+                        if (gacc[b] != 0.f) atomicAdd(P.gemv_y + b * P.gemv_ldy + grow, gacc[b]);
             }
         }
         item = pend;
@@ -1106,7 +1116,7 @@ bool pool_setup(DecodeParams &P, uint32_t grid) {
     return true;
 }
 
-template <int kPer, bool kVec, bool kStaged, bool kGemv = false, bool kFixed = false, bool kPool = false>
+template <int kPer, bool kVec, bool kStaged, int kGemv = 0, bool kFixed = false, bool kPool = false>
 int launch(DecodeParams &P, cudaStream_t stream, bool early = false) {
     static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
     static int grid_max[kMaxDevices] = {};
@@ -1185,12 +1195,23 @@ int launch_syms(DecodeParams &P, cudaStream_t stream, bool early) {
 }
 
 // fused GEMV launches: staged bits and the vector merge only
-int launch_gemv(DecodeParams &P, cudaStream_t stream, bool early = false) {
+int launch_gemv(DecodeParams &P, uint32_t n_vec, cudaStream_t stream, bool early = false) {
+    const bool fixed = P.chunk_syms == 4096 && P.sub_syms == 256;
+    if (n_vec > 1) {
+        // several vectors: the default layout and two codes per lookup only
+        if (!fixed || g_per == 1) return K3HUF_E_ARG;
+        switch (n_vec) {
+            case 2: return launch<2, true, true, 2, true>(P, stream, early);
+            case 4: return launch<2, true, true, 4, true>(P, stream, early);
+            case 8: return launch<2, true, true, 8, true>(P, stream, early);
+            default: return K3HUF_E_ARG;
+        }
+    }
     switch (g_per) {
-        case 1: return launch<1, true, true, true>(P, stream, early);
+        case 1: return launch<1, true, true, 1>(P, stream, early);
         default:
-            if (P.chunk_syms == 4096 && P.sub_syms == 256) return launch<2, true, true, true, true>(P, stream, early);
-            return launch<2, true, true, true>(P, stream, early);
+            if (fixed) return launch<2, true, true, 1, true>(P, stream, early);
+            return launch<2, true, true, 1>(P, stream, early);
     }
 }
 
@@ -1349,9 +1370,11 @@ extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_sy
 
 namespace {
 int gemv_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes, uint32_t tensor,
-                    uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status, uint32_t flags, void *stream) {
+                    uint64_t cols, const void *d_x, uint32_t n_vec, float *d_y, uint32_t *d_status, uint32_t flags,
+                    void *stream) {
     using namespace k3huf;
     if (!h_layer_hdr || !d_layer || !d_x || !d_y || !d_status || cols == 0) return K3HUF_E_ARG;
+    if (n_vec != 1 && n_vec != 2 && n_vec != 4 && n_vec != 8) return K3HUF_E_ARG;
     if (!aligned16(d_layer) || !aligned16(d_x) || (reinterpret_cast<uintptr_t>(d_y) & 3u) ||
         (reinterpret_cast<uintptr_t>(d_status) & 3u))
         return K3HUF_E_ARG;
@@ -1374,6 +1397,8 @@ int gemv_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_lay
     P.gemv_x = static_cast<const uint8_t *>(d_x);
     P.gemv_y = d_y;
     P.gemv_cols = cols;
+    P.gemv_ldx = 2 * cols;                     // X: n_vec rows of cols bf16
+    P.gemv_ldy = te.n_values / cols;           // Y: n_vec rows of `rows` floats
     for (uint32_t s0 = 0; s0 < te.n_stripes; s0 += kMaxTasks) {
         const uint32_t s1 = std::min<uint32_t>(te.n_stripes, s0 + kMaxTasks);
         uint32_t items = 0;
@@ -1392,11 +1417,11 @@ int gemv_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_lay
         }
         P.n_items = items;
         if (s0 == 0 && (flags & K3HUF_GEMV_ZERO_Y)) {
-            rc = launch_zero_y(d_y, te.n_values / cols, static_cast<cudaStream_t>(stream),
+            rc = launch_zero_y(d_y, uint64_t(n_vec) * (te.n_values / cols), static_cast<cudaStream_t>(stream),
                                (flags & K3HUF_DECODE_EARLY_START) != 0);
             if (rc) return rc;
         }
-        rc = launch_gemv(P, static_cast<cudaStream_t>(stream), (flags & K3HUF_DECODE_EARLY_START) != 0);
+        rc = launch_gemv(P, n_vec, static_cast<cudaStream_t>(stream), (flags & K3HUF_DECODE_EARLY_START) != 0);
         if (rc) return rc;
     }
     return K3HUF_OK;
@@ -1406,13 +1431,22 @@ int gemv_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_lay
 extern "C" int k3huf_gemv_layer(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
                                 uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
                                 void *stream) {
-    return gemv_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, tensor, cols, d_x, d_y, d_status, 0u, stream);
+    return gemv_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, tensor, cols, d_x, 1u, d_y, d_status, 0u,
+                           stream);
 }
 
 extern "C" int k3huf_gemv_layer_ex(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
                                    uint32_t tensor, uint64_t cols, const void *d_x, float *d_y, uint32_t *d_status,
                                    uint32_t flags, void *stream) {
     if (flags & ~uint32_t(K3HUF_DECODE_EARLY_START | K3HUF_GEMV_ZERO_Y)) return K3HUF_E_ARG;
-    return gemv_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, tensor, cols, d_x, d_y, d_status, flags,
+    return gemv_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, tensor, cols, d_x, 1u, d_y, d_status, flags,
                            stream);
+}
+
+extern "C" int k3huf_gemv_layer_batch(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer,
+                                      size_t layer_bytes, uint32_t tensor, uint64_t cols, const void *d_x,
+                                      uint32_t n_vec, float *d_y, uint32_t *d_status, uint32_t flags, void *stream) {
+    if (flags & ~uint32_t(K3HUF_DECODE_EARLY_START | K3HUF_GEMV_ZERO_Y)) return K3HUF_E_ARG;
+    return gemv_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, tensor, cols, d_x, n_vec, d_y, d_status,
+                           flags, stream);
 }

@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    and last words, which the neighbouring chunks may share, are OR-ed
 //    atomically into the zeroed container.
 //    The input is read from DRAM once, here, after the histogram pass.
-constexpr int kLbWarps = 12;
+constexpr int kLbWarps = 13;
 constexpr int kLbThreads = 32 * kLbWarps;
 constexpr uint32_t kLbRow = 272;                          // a lane's 128 values (256 bytes) + 16 of padding
 constexpr uint32_t kLbIn = 32 * kLbRow;                   // one chunk's values, then its stream words

@@ -163,3 +163,38 @@ def test_gemv_ex_reads_x_after_the_kernel_that_writes_it():
             assert int(st.item()) == 0
             ref, mag = reference(blob, 0, cols, x_vector(cols, 40 + i))
             assert np.all(np.abs(y.cpu().numpy().astype(np.float64) - ref) <= 1e-4 * mag + 1e-30), (zero_y, i)
+
+
+@pytest.mark.parametrize("n_vec", [2, 4, 8])
+def test_gemv_batch_matches_oracle(n_vec):
+    """Y = W X for several vectors with one decode of W, each vector's y
+    against the oracle's decode of W times that vector in float64."""
+    rows, cols = 48, 16384
+    w = workloads.normal_tensor((rows, cols), 0.02, 40 + n_vec)
+    blob = oracle.encode_layer([w])
+    info = k3.layer_info(blob)
+    xs = [x_vector(cols, 50 + b) for b in range(n_vec)]
+    X = torch.from_numpy(np.concatenate(xs).view(np.int16)).cuda()
+    Y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    d_blob = torch.from_numpy(blob).cuda()
+    k3.gemv_layer_batch(blob[: info["hdr_bytes"]], d_blob, 0, cols, X, Y, st, zero_y=True)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    got = Y.cpu().numpy().astype(np.float64)
+    for b in range(n_vec):
+        ref, mag = reference(blob, 0, cols, xs[b])
+        assert np.all(np.abs(got[b] - ref) <= 1e-4 * mag + 1e-30), b
+
+
+def test_gemv_batch_refuses_other_counts():
+    rows, cols = 8, 8192
+    blob = oracle.encode_layer([workloads.normal_tensor((rows, cols), 0.02, 77)])
+    info = k3.layer_info(blob)
+    d_blob = torch.from_numpy(blob).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    X = torch.zeros((3, cols), dtype=torch.int16, device="cuda")
+    Y = torch.zeros((3, rows), dtype=torch.float32, device="cuda")
+    with pytest.raises(k3.K3HufError) as e:
+        k3.gemv_layer_batch(blob[: info["hdr_bytes"]], d_blob, 0, cols, X, Y, st)
+    assert e.value.code == k3.E_ARG
