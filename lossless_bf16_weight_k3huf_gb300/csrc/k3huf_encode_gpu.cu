@@ -9,16 +9,18 @@
 //  1. per-stripe histograms of the high bytes (per-warp shared-memory bins);
 //  2. host: code lengths, codes and the container layout, with the same
 //     functions as the CPU encoder (k3huf_host.cpp), so both write the same
-//     bytes; the blob is zeroed and the header copied in;
-//  3. bits of every chunk (one warp per chunk, coalesced 16-byte loads);
-//  4. per stripe, one CTA scans them into the chunk index, writes the stripe
-//     header and checks the total against the planned bit count;
-//  5. one warp per chunk packs its codes MSB-first: each step of 256 values
-//     gives every lane 8 codes, a warp scan of the lanes' bit counts places
-//     them, the codes are OR-ed into a shared staging window, whole words go
-//     out with plain coalesced stores and only the words a chunk shares with
-//     its neighbours with atomic ORs; the same pass writes the sub-stream
-//     index and the low bytes.
+//     bytes; the header is copied in and the gaps no pass writes whole are
+//     zeroed;
+//  3. the default layout (chunks of 4096 values, sub-streams of 256): one
+//     pass per chunk that counts, indexes and packs, the chunks' first bits
+//     found by decoupled look-back along each stripe (pack_lb_kernel), so
+//     the values are read from DRAM only here after the histogram;
+//  3'-5'. any other layout: bits of every chunk (one warp per chunk,
+//     coalesced 16-byte loads); per stripe, one CTA scans them into the
+//     chunk index, writes the stripe header and checks the total against
+//     the planned bit count; then packing MSB-first (one warp per chunk or
+//     one lane per sub-stream), writing the sub-stream index and the low
+//     bytes in the same pass.
 // Scratch (caller-owned device memory, k3huf_encode_scratch_bytes) holds
 // the stripe descriptors, histograms, code tables, and two words per chunk.
 #include <cuda_runtime.h>
