@@ -112,3 +112,26 @@ def test_gpu_encoder_one_call_into_bound_buffer(name):
     assert got.numel() == ref.size <= bound
     assert np.array_equal(got.cpu().numpy(), ref)
     assert bool((buf[ref.size:] == 0xA5).all())
+
+
+def test_gpu_encoder_random_layers():
+    """40 seeded random layers (alphabet size and skew, 1-4 tensors of
+    1-600,000 values, the default layout or another, shared or per-tensor
+    tables): the GPU container equals the oracle's byte for byte.  The
+    default layout goes through the one-pass packer, whose look-back spans
+    up to 147 chunks per stripe here, with ragged last chunks and lanes."""
+    rng = np.random.default_rng(4242)
+    for case in range(40):
+        tensors = []
+        for _ in range(int(rng.integers(1, 5))):
+            n = int(rng.integers(1, 600_001))
+            n_sym = int(rng.integers(1, 257))
+            syms = rng.choice(256, size=n_sym, replace=False)
+            w = float(rng.uniform(0.05, 1.0)) ** np.arange(n_sym, dtype=np.float64)
+            hi = rng.choice(syms, size=n, p=w / w.sum()).astype(np.uint16)
+            tensors.append((hi << 8) | rng.integers(0, 256, size=n, dtype=np.uint16))
+        kw = {"shared_table": bool(rng.integers(0, 2))}
+        if case % 4 == 3:
+            kw["chunk_syms"] = int(rng.choice([1024, 2048, 8192]))
+        got = gpu_blob(tensors, **kw)
+        assert np.array_equal(got, oracle.encode_layer(tensors, **kw)), case
