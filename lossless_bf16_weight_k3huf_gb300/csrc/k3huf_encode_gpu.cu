@@ -565,6 +565,9 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    is already held by a running warp, publishes the chunk's bit count,
 //    then sums its predecessors' published counts back to the nearest one
 //    whose first bit is known, and publishes its own first bit and end.
+//    14 warps per SM; the code table is held in 16 copies (lanes l and
+//    l + 16 read copy l % 16: they conflict only on different symbols of
+//    the same parity), which leaves room for the 14th warp.
 //    Per chunk and warp:
 //  - its 8 KB of values are copied into shared memory (cp.async, coalesced
 //    16-byte pieces) as 32 rows of 128 values, one per lane, rows padded to
@@ -572,8 +575,9 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //  - lane l owns values [128 l, 128 l + 128): half of sub-stream l / 2.  It
 //    codes them in order into a private run of words (rows of 49 words, so
 //    the lanes' stores fall in different banks), two codes at a time (at
-//    most 24 bits, so 32-bit shifts suffice); its bit count comes out of
-//    the same pass;
+//    most 24 bits, so 32-bit shifts suffice; codes sit left-aligned in the
+//    table, and the append has no branch); its bit count comes out of the
+//    same pass;
 //  - a warp scan of the lanes' counts and the look-back give every lane its
 //    first bit; the low bytes leave from the staged rows (coalesced 8-byte
 //    stores), and the rows then take the chunk's stream words: each lane
@@ -583,13 +587,13 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    and last words, which the neighbouring chunks may share, are OR-ed
 //    atomically into the zeroed container.
 //    The input is read from DRAM once, here, after the histogram pass.
-constexpr int kLbWarps = 13;
+constexpr int kLbWarps = 14;
 constexpr int kLbThreads = 32 * kLbWarps;
 constexpr uint32_t kLbRow = 272;                          // a lane's 128 values (256 bytes) + 16 of padding
 constexpr uint32_t kLbIn = 32 * kLbRow;                   // one chunk's values, then its stream words
 constexpr uint32_t kLbRun = 49;                           // words of a lane's private run (128 x 12 bits + 1)
 constexpr uint32_t kLbWarpBytes = kLbIn + 4 * 32 * kLbRun;
-constexpr size_t kLbSmem = size_t(256) * 32 * 4 + size_t(kLbWarps) * kLbWarpBytes;
+constexpr size_t kLbSmem = size_t(256) * 16 * 4 + size_t(kLbWarps) * kLbWarpBytes;
 static_assert(kLbWarpBytes % 16 == 0, "per-warp staging must stay 16-byte aligned");
 static_assert(4096 * K3HUF_MAXLEN / 32 + 2 <= kLbIn / 4, "a chunk's stream words fit the staged rows");
 constexpr uint32_t kLbSpin = 1u << 22;                    // look-back polls before giving up
@@ -612,39 +616,43 @@ __device__ __forceinline__ void lb_cp_wait() {
 // Codes arrive in pairs: two codes of at most 12 bits are one string of at
 // most 24, so 32-bit shifts do all the work.
 struct LbRun {
-    uint32_t pend, np, wi;
-    // append the len low bits of v (1 <= len <= 24)
-    __device__ __forceinline__ void append(uint32_t v, uint32_t len, uint32_t *run) {
-        const uint32_t pl = v << (32u - len);                 // left-aligned
-        const uint32_t w = pend | (pl >> np), t = np + len;
-        if (t >= 32u) {                                       // (then np >= 8: pl << (32 - np) is defined)
-            run[wi++] = w;
-            pend = pl << (32u - np);
-            np = t - 32u;
-        } else {
-            pend = w;
-            np = t;
-        }
+    uint32_t pend, np;
+    uint32_t *rp;                                             // the word `pend` goes to
+    // append the left-aligned string v of len bits (1 <= len <= 24).  No
+    // branch: the word is stored every time (a partial one is stored again
+    // later) and the pointer moves on when it is full
+    __device__ __forceinline__ void append(uint32_t v, uint32_t len) {
+        const uint32_t w = pend | (v >> np);
+        const uint32_t spill = __funnelshift_r(0u, v, np);   // v's bits past this word (0 when np = 0)
+        const uint32_t t = np + len;
+        *rp = w;
+        const bool full = t >= 32u;
+        pend = full ? spill : w;
+        rp += full ? 1 : 0;
+        np = t & 31u;
     }
-    // the pair of entries (code << 4) | length, the first code first
-    __device__ __forceinline__ void pair(uint32_t e0, uint32_t e1, uint32_t *run) {
-        const uint32_t l1 = e1 & 15u;
-        append(((e0 >> 4) << l1) | (e1 >> 4), (e0 & 15u) + l1, run);
+    // two table entries (code << (32 - len)) | len (codes of at most 12
+    // bits), the first code first
+    __device__ __forceinline__ void pair(uint32_t e0, uint32_t e1) {
+        const uint32_t l0 = e0 & 31u;
+        append((e0 & 0xFFF00000u) | ((e1 & 0xFFF00000u) >> l0), l0 + (e1 & 31u));
     }
 };
 
 __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
     extern __shared__ __align__(16) uint8_t lb_smem[];
-    uint32_t(*code)[32] = reinterpret_cast<uint32_t(*)[32]>(lb_smem);   // entry s of lane l at code[s][l]
+    uint32_t(*code)[16] = reinterpret_cast<uint32_t(*)[16]>(lb_smem);   // entry s for lanes l, l + 16 at code[s][l % 16]
     const EncStripe &T = P.stripes[blockIdx.y];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int s = threadIdx.x; s < 256; s += kLbThreads) {
-        const uint32_t e = P.codes[size_t(T.table) * 256 + s];
+        // (code << 4) | length becomes the code left-aligned above its length
+        const uint32_t e0 = P.codes[size_t(T.table) * 256 + s], l0 = e0 & 15u;
+        const uint32_t e = l0 ? ((e0 >> 4) << (32u - l0)) | l0 : 0u;
 #pragma unroll 8
-        for (int j = 0; j < 32; ++j) code[s][(j + lane) & 31] = e;
+        for (int j = 0; j < 16; ++j) code[s][(j + lane) & 15] = e;
     }
     __syncthreads();
-    uint8_t *const in = lb_smem + size_t(256) * 32 * 4 + size_t(warp) * kLbWarpBytes;
+    uint8_t *const in = lb_smem + size_t(256) * 16 * 4 + size_t(warp) * kLbWarpBytes;
     uint32_t *const sw = reinterpret_cast<uint32_t *>(in);           // the chunk's stream words, after the rows
     uint32_t *const run = reinterpret_cast<uint32_t *>(in + kLbIn) + lane * kLbRun;
     uint32_t *chunk_idx = reinterpret_cast<uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
@@ -677,24 +685,24 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         //    in order into its run, two at a time
         const uint32_t v0 = 128u * uint32_t(lane);
         const uint32_t m = v0 < nv ? min(128u, nv - v0) : 0u;
-        LbRun R{0u, 0u, 0u};
+        LbRun R{0u, 0u, run};
         if (m == 128u) {
 #pragma unroll 2
             for (uint32_t j = 0; j < 16; ++j) {
                 const uint4 x = *reinterpret_cast<const uint4 *>(row + 16 * j);
                 const uint32_t q[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) R.pair(code[(q[i] >> 8) & 0xFFu][lane], code[q[i] >> 24][lane], run);
+                for (int i = 0; i < 4; ++i) R.pair(code[(q[i] >> 8) & 0xFFu][lane & 15], code[q[i] >> 24][lane & 15]);
             }
         } else {
             // a stripe's ragged end: one code at a time
             for (uint32_t v = 0; v < m; ++v) {
-                const uint32_t e = code[row[2 * v + 1]][lane];
-                R.append(e >> 4, e & 15u, run);
+                const uint32_t e = code[row[2 * v + 1]][lane & 15];
+                R.append(e & 0xFFF00000u, e & 31u);
             }
         }
-        if (R.np) run[R.wi] = R.pend;
-        const uint32_t bits = 32u * R.wi + R.np;
+        if (R.np) *R.rp = R.pend;
+        const uint32_t bits = 32u * uint32_t(R.rp - run) + R.np;
         // 3. the lane's first bit within the chunk, and the chunk's bits
         uint32_t incl = bits;
 #pragma unroll
