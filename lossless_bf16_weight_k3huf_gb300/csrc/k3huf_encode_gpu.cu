@@ -22,10 +22,12 @@
 //     one lane per sub-stream), writing the sub-stream index and the low
 //     bytes in the same pass.
 // Scratch (caller-owned device memory, k3huf_encode_scratch_bytes) holds
-// the stripe descriptors, histograms, code tables, and two words per chunk.
+// the stripe descriptors, code tables, histograms, per-stripe chunk tickets,
+// two words per chunk and an error flag.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -48,8 +50,8 @@ struct EncStripe {
 struct EncParams {
     const EncStripe *stripes;
     const uint32_t *codes;     // n_tables x 256: (code << 4) | length
-    uint32_t *counts;          // n_stripes x 256 (after the histogram pass: the one-pass
-                               // packer's per-stripe chunk counters)
+    uint32_t *counts;          // n_stripes x 256 histogram bins
+    uint32_t *tickets;         // n_stripes: the one-pass packer's per-stripe chunk counters
     uint32_t *chunk_bits;      // bits of every chunk (or, one-pass packer: 64-bit records)
     uint32_t *chunk_start;     // first bit of every chunk within its stripe's stream
     uint32_t *flag;            // nonzero: the packed bits disagree with the plan
@@ -57,7 +59,7 @@ struct EncParams {
 };
 
 struct ScratchLayout {
-    size_t stripes, counts, codes, chunk_bits, chunk_start, flag, total;
+    size_t stripes, codes, counts, tickets, chunk_bits, chunk_start, flag, total;
 };
 
 constexpr int kHistThreads = 256;
@@ -74,9 +76,12 @@ ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_chunk
         at = size_t(align_up(at + bytes, 256));
         return here;
     };
+    // the descriptors and code tables go up in one copy, and everything from
+    // the histograms on is zeroed in one memset
     s.stripes = take(n_stripes * sizeof(EncStripe));
-    s.counts = take(n_stripes * 256 * sizeof(uint32_t));
     s.codes = take(n_tables * 256 * sizeof(uint32_t));
+    s.counts = take(n_stripes * 256 * sizeof(uint32_t));
+    s.tickets = take(n_stripes * sizeof(uint32_t));
     // two words per chunk: the bit count and first bit of each chunk, or,
     // for the one-pass packer, one 64-bit look-back record per chunk
     s.chunk_bits = take(size_t(n_chunks) * 2 * sizeof(uint32_t));
@@ -569,6 +574,8 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    l + 16 read copy l % 16: they conflict only on different symbols of
 //    the same parity), which leaves room for the 14th warp.
 //    Per chunk and warp:
+//  - when it takes the chunk, lane 0 starts an L2 prefetch of the chunk
+//    one round of the stripe's warps ahead;
 //  - its 8 KB of values are copied into shared memory (cp.async, coalesced
 //    16-byte pieces) as 32 rows of 128 values, one per lane, rows padded to
 //    272 bytes so that the lanes' reads of their rows never conflict;
@@ -664,7 +671,15 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
     const uint8_t *row = in + lane * kLbRow;
     for (;;) {
         uint32_t c = 0;
-        if (lane == 0) c = atomicAdd(P.counts + blockIdx.y, 1u);
+        if (lane == 0) {
+            c = atomicAdd(P.tickets + blockIdx.y, 1u);
+            // the chunk one round of the stripe's warps ahead, which a warp
+            // takes about one chunk time from now, is fetched into L2 (a
+            // whole chunk: only a stripe's last chunk can be short)
+            const uint32_t cp = c + gridDim.x * uint32_t(kLbWarps);
+            if (cp + 1 < T.n_chunks)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], 8192;" ::"l"(T.src + size_t(cp) * 8192u) : "memory");
+        }
         c = __shfl_sync(0xffffffffu, c, 0);
         if (c >= T.n_chunks) break;
         const uint32_t a = c * 4096u, nv = min(4096u, T.n - a);
@@ -808,6 +823,20 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
     }
 }
 
+// The packer's shared-memory opt-in and the SM count, once per device
+cudaError_t pack_lb_setup(int *sms) {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> s_sms[kMaxDev];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDev && (*sms = s_sms[dev].load(std::memory_order_acquire)) > 0) return cudaSuccess;
+    e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(pack_lb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kLbSmem));
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) s_sms[dev].store(*sms, std::memory_order_release);
+    return e;
+}
+
 int cuda_fail(cudaError_t e) {
     set_cuda_error(int(e));
     return K3HUF_E_CUDA;
@@ -879,6 +908,7 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         EncParams P{};
         P.stripes = reinterpret_cast<const EncStripe *>(scr + SL.stripes);
         P.counts = reinterpret_cast<uint32_t *>(scr + SL.counts);
+        P.tickets = reinterpret_cast<uint32_t *>(scr + SL.tickets);
         P.codes = reinterpret_cast<const uint32_t *>(scr + SL.codes);
         P.chunk_bits = reinterpret_cast<uint32_t *>(scr + SL.chunk_bits);
         P.chunk_start = reinterpret_cast<uint32_t *>(scr + SL.chunk_start);
@@ -904,7 +934,8 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         }
         // 1. histograms
         cudaError_t e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.counts, 0, ns * 256 * sizeof(uint32_t), st);
+        // histograms, tickets, look-back records and the flag start at zero
+        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.counts, 0, SL.total - SL.counts, st);
         if (e != cudaSuccess) return cuda_fail(e);
         const uint32_t gx = std::min<uint32_t>(512, std::max<uint32_t>(1, (max_n + 65535) / 65536));
         hist_kernel<<<dim3(gx, uint32_t(ns)), kHistThreads, 0, st>>>(P);
@@ -940,10 +971,10 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         const bool per_sub = sub_syms == 256 && chunk_syms % 256 == 0 && P.S <= 16 && (P.S & (P.S - 1)) == 0;
         std::vector<uint8_t> head(size_t(L.hdr));
         write_layer_header(L, head.data());
-        e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(scr + SL.codes, codes.data(), codes.size() * sizeof(uint32_t), cudaMemcpyHostToDevice, st);
-        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.flag, 0, sizeof(uint32_t), st);
+        std::vector<uint8_t> up(SL.codes - SL.stripes + codes.size() * sizeof(uint32_t));
+        std::memcpy(up.data(), desc.data(), ns * sizeof(EncStripe));
+        std::memcpy(up.data() + (SL.codes - SL.stripes), codes.data(), codes.size() * sizeof(uint32_t));
+        e = cudaMemcpyAsync(scr + SL.stripes, up.data(), up.size(), cudaMemcpyHostToDevice, st);
         if (e == cudaSuccess && !per_sub) e = cudaMemsetAsync(blob, 0, size_t(L.total), st);
         if (e == cudaSuccess) e = cudaMemcpyAsync(blob, head.data(), head.size(), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -959,16 +990,9 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_chunks + wpb - 1) / wpb));
         const bool one_pass = per_sub && chunk_syms == 4096;
         if (one_pass) {
-            // per-stripe chunk counters (the histograms' place) and look-back records start at zero
-            e = cudaMemsetAsync(scr + SL.counts, 0, ns * sizeof(uint32_t), st);
-            if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.chunk_bits, 0, size_t(n_chunks) * 8, st);
-            if (e != cudaSuccess) return cuda_fail(e);
-            int dev = 0, sms = 0;
-            e = cudaGetDevice(&dev);
-            if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(pack_lb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kLbSmem));
-            if (e != cudaSuccess) return cuda_fail(e);
+            // (tickets and look-back records were zeroed before the histogram)
+            int sms = 0;
+            if ((e = pack_lb_setup(&sms)) != cudaSuccess) return cuda_fail(e);
             const uint32_t per = std::max<uint32_t>(1, (2u * uint32_t(std::max(1, sms)) + uint32_t(ns) - 1) / uint32_t(ns));
             const uint32_t gl = std::min<uint32_t>(per, std::max<uint32_t>(1, (max_chunks + kLbWarps - 1) / kLbWarps));
             pack_lb_kernel<<<dim3(gl, uint32_t(ns)), kLbThreads, kLbSmem, st>>>(P);
