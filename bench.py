@@ -929,8 +929,9 @@ def bench_encode(args, rank, world, local, dev):
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {**describe("encode"), "values": n, "raw_bytes": raw, "blob_bytes": int(blob.numel()),
                    "compression_ratio": round(raw / blob.numel(), 4),
-                   "passes": ("histogram; the container's gaps zeroed; one pass per 4096-value chunk: bit counts, "
-                              "chunk and sub-stream index (decoupled look-back), packing, low bytes (2 reads of the input)"),
+                   "passes": ("histogram; one pass per 4096-value chunk: bit counts, chunk and sub-stream index "
+                              "(decoupled look-back), packing, low bytes (2 reads of the input); the words "
+                              "neighbouring chunks share joined and the padding zeroed"),
                    "call": "one k3huf_encode_layer_gpu per step into a buffer of k3huf_encode_bound bytes",
                    "cpu_encoder_gbs": round(raw / cpu_enc_s / 1e9, 3),
                    "cpu_encoder_threads": os.cpu_count(), "l2": "inputs larger than L2"},
@@ -939,7 +940,7 @@ def bench_encode(args, rank, world, local, dev):
                      "traffic": ncu_traffic("encode"), "algorithmic_bytes_per_call": alg},
         "e2e": {"value": round(raw / te / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": raw,
                 "d2h_bytes_per_step": int(blob.numel())},
-        "gpu_launches": 3 * args.steps,                 # histogram, gap zeroing, one-pass packing
+        "gpu_launches": 3 * args.steps,                 # histogram, one-pass packing, seams
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

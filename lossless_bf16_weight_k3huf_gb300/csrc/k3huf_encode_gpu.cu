@@ -22,8 +22,9 @@
 //     one lane per sub-stream), writing the sub-stream index and the low
 //     bytes in the same pass.
 // Scratch (caller-owned device memory, k3huf_encode_scratch_bytes) holds
-// the stripe descriptors, code tables, histograms, per-stripe chunk tickets,
-// two words per chunk and an error flag.
+// the stripe descriptors, code tables, two shared stream words per chunk,
+// histograms, per-stripe chunk tickets, two words per chunk and an error
+// flag.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -52,6 +53,8 @@ struct EncParams {
     const uint32_t *codes;     // n_tables x 256: (code << 4) | length
     uint32_t *counts;          // n_stripes x 256 histogram bins
     uint32_t *tickets;         // n_stripes: the one-pass packer's per-stripe chunk counters
+    uint32_t *edges;           // the one-pass packer: per chunk, its first and last stream
+                               // words when a neighbouring chunk shares them
     uint32_t *chunk_bits;      // bits of every chunk (or, one-pass packer: 64-bit records)
     uint32_t *chunk_start;     // first bit of every chunk within its stripe's stream
     uint32_t *flag;            // nonzero: the packed bits disagree with the plan
@@ -59,7 +62,7 @@ struct EncParams {
 };
 
 struct ScratchLayout {
-    size_t stripes, codes, counts, tickets, chunk_bits, chunk_start, flag, total;
+    size_t stripes, codes, edges, counts, tickets, chunk_bits, chunk_start, flag, total;
 };
 
 constexpr int kHistThreads = 256;
@@ -80,6 +83,7 @@ ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_chunk
     // the histograms on is zeroed in one memset
     s.stripes = take(n_stripes * sizeof(EncStripe));
     s.codes = take(n_tables * 256 * sizeof(uint32_t));
+    s.edges = take(size_t(n_chunks) * 2 * sizeof(uint32_t));
     s.counts = take(n_stripes * 256 * sizeof(uint32_t));
     s.tickets = take(n_stripes * sizeof(uint32_t));
     // two words per chunk: the bit count and first bit of each chunk, or,
@@ -585,14 +589,17 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    most 24 bits, so 32-bit shifts suffice; codes sit left-aligned in the
 //    table, and the append has no branch); its bit count comes out of the
 //    same pass;
-//  - a warp scan of the lanes' counts and the look-back give every lane its
-//    first bit; the low bytes leave from the staged rows (coalesced 8-byte
-//    stores), and the rows then take the chunk's stream words: each lane
+//  - a warp scan of the lanes' counts gives the chunk's count, which is
+//    published at once; the low bytes then leave from the staged rows
+//    (coalesced 8-byte stores), which takes the time predecessors need to
+//    publish theirs, and the look-back follows.  It gives every lane its
+//    first bit, and the rows take the chunk's stream words: each lane
 //    shifts its run into place (funnel shifts; only its first and last
 //    words, which neighbouring lanes share, by shared atomic OR);
-//  - the stream words leave with coalesced stores; only the chunk's first
-//    and last words, which the neighbouring chunks may share, are OR-ed
-//    atomically into the zeroed container.
+//  - the stream words leave with coalesced stores; the chunk's first and
+//    last words, when a neighbouring chunk shares them, go to a per-chunk
+//    edge pair, and seam_kernel writes each shared word whole and zeroes
+//    the stripe's padding, so that no pass zeroes the stream beforehand.
 //    The input is read from DRAM once, here, after the histogram pass.
 constexpr int kLbWarps = 14;
 constexpr int kLbThreads = 32 * kLbWarps;
@@ -726,12 +733,32 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             if (lane >= d) incl += t;
         }
         const uint32_t lo = incl - bits, total = __shfl_sync(0xffffffffu, incl, 31);
-        // 4. the chunk's first bit within the stripe's stream: look-back
+        // 4. the chunk's bit count published (with its first bit, for the
+        //    stripe's first chunk); the work that does not need the first
+        //    bit comes before the look-back, while predecessors publish:
+        //    the low bytes of the chunk, 8 per lane and step, ...
         uint32_t start = 0;
-        if (c == 0) {
-            if (lane == 0) atomicExch(rec, kLbIncl | total);
-        } else {
-            if (lane == 0) atomicExch(rec + c, kLbAgg | total);
+        if (lane == 0) atomicExch(rec + c, (c == 0 ? kLbIncl : kLbAgg) | total);
+#pragma unroll 4
+        for (uint32_t k = 0; k < 16; ++k) {
+            const uint32_t u = k * 32 + uint32_t(lane), vv = 8 * u;
+            if (vv >= nv) continue;
+            const uint4 x = *reinterpret_cast<const uint4 *>(in + (u >> 4) * kLbRow + (u & 15) * 16);
+            const uint32_t l0 = __byte_perm(x.x, x.y, 0x6420), l1 = __byte_perm(x.z, x.w, 0x6420);
+            if (vv + 8 <= nv) {
+                *reinterpret_cast<uint2 *>(even + a + vv) = make_uint2(l0, l1);
+            } else {
+                for (uint32_t i = 0; vv + i < nv; ++i) even[a + vv + i] = uint8_t((i < 4 ? l0 : l1) >> (8 * (i & 3)));
+            }
+        }
+        __syncwarp();
+        //    ... and the staging words zeroed (as many as any first bit needs)
+        {
+            const uint32_t n_z = (total + 62u) >> 5;
+            for (uint32_t k = lane; k < n_z; k += 32) sw[k] = 0u;
+        }
+        // 5. the chunk's first bit within the stripe's stream: look-back
+        if (c != 0) {
             int64_t j = int64_t(c) - 1;
             uint32_t polls = 0;
             for (;;) {
@@ -754,7 +781,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             }
             if (lane == 0) atomicExch(rec + c, kLbIncl | (start + total));
         }
-        // 5. chunk index, sub-stream index (sub-stream k starts at lane 2k's
+        // 6. chunk index, sub-stream index (sub-stream k starts at lane 2k's
         //    first bit; one that starts at or past the chunk's end, at its
         //    end), the stripe header with the first chunk, the plan's total
         //    checked with the last
@@ -772,24 +799,9 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             h[7] = T.even_offset;
         }
         if (lane == 0 && c + 1 == T.n_chunks && uint64_t(start) + total != T.huff_bits) atomicOr(P.flag, 1u);
-        // 6. low bytes of the chunk, 8 per lane and step
-#pragma unroll 4
-        for (uint32_t k = 0; k < 16; ++k) {
-            const uint32_t u = k * 32 + uint32_t(lane), vv = 8 * u;
-            if (vv >= nv) continue;
-            const uint4 x = *reinterpret_cast<const uint4 *>(in + (u >> 4) * kLbRow + (u & 15) * 16);
-            const uint32_t l0 = __byte_perm(x.x, x.y, 0x6420), l1 = __byte_perm(x.z, x.w, 0x6420);
-            if (vv + 8 <= nv) {
-                *reinterpret_cast<uint2 *>(even + a + vv) = make_uint2(l0, l1);
-            } else {
-                for (uint32_t i = 0; vv + i < nv; ++i) even[a + vv + i] = uint8_t((i < 4 ? l0 : l1) >> (8 * (i & 3)));
-            }
-        }
-        __syncwarp();
         // 7. the rows take the chunk's stream words (staging bit b is stream
         //    bit (start & ~31) + b): each lane shifts its run into place
         const uint32_t sh = start & 31u, n_sw = (sh + total + 31u) >> 5;
-        for (uint32_t k = lane; k < n_sw; k += 32) sw[k] = 0u;
         __syncwarp();
         if (bits) {
             const uint32_t o = sh + lo, d0 = o >> 5, r = o & 31u, kw = (bits + 31u) >> 5;
@@ -808,18 +820,49 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         // 8. the stream words out, in the stream's byte order (the staging
         //    words hold their first bit at the top); the first and the last
         //    may hold the neighbouring chunks' bits too
+        //    A word shared with a neighbouring chunk goes to the chunk's
+        //    edge pair instead; seam_kernel joins the two halves.  (Every
+        //    chunk but a stripe's last holds 4096 codes, so it spans more
+        //    than one word.)
         const uint32_t w0 = start >> 5;
+        const bool shared_head = sh != 0u;
+        const bool shared_tail = ((start + total) & 31u) != 0u && c + 1 < T.n_chunks;
+        if (lane == 0 && n_sw == 1 && shared_head && shared_tail) atomicOr(P.flag, 1u);
+        uint32_t *const edge = P.edges + 2 * (size_t(T.chunk_begin) + c);
         for (uint32_t k = lane; k < n_sw; k += 32) {
             const uint32_t gw = w0 + k;
             if (gw >= n_words) continue;
             const uint32_t w = __byte_perm(sw[k], 0, 0x0123);
-            if (k == 0 || k + 1 == n_sw) {
-                if (w) atomicOr(&words[gw], w);
-            } else {
-                words[gw] = w;
-            }
+            if (k == 0 && shared_head) edge[0] = w;
+            else if (k + 1 == n_sw && shared_tail) edge[1] = w;
+            else words[gw] = w;
         }
         __syncwarp();                                 // the rows and the runs free again
+    }
+}
+
+// After the one-pass packer: each stream word that two chunks share is the
+// OR of the earlier chunk's last word and the later chunk's first (written
+// whole here), and the stripe's padding is zeroed: the index's alignment,
+// the stream region after its last word, and the low bytes' tail up to the
+// next stripe (a few hundred bytes per stripe).
+__global__ void __launch_bounds__(256) seam_kernel(EncParams P) {
+    const EncStripe &T = P.stripes[blockIdx.y];
+    const uint32_t *chunk_idx = reinterpret_cast<const uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
+    uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
+    const uint32_t *edge = P.edges + 2 * size_t(T.chunk_begin);
+    for (uint32_t c = 1 + blockIdx.x * 256u + threadIdx.x; c < T.n_chunks; c += gridDim.x * 256u) {
+        const uint32_t st = chunk_idx[c];
+        if (st & 31u) words[st >> 5] = edge[2 * (c - 1) + 1] | edge[2 * c];
+    }
+    if (blockIdx.x == 0) {
+        const uint32_t p1a = K3HUF_STRIPE_HDR_BYTES + T.n_chunks * (4u + 2u * (P.S - 1u)), p1b = T.bits_offset;
+        const uint32_t p2a = T.bits_offset + 4u * uint32_t((T.huff_bits + 31u) / 32u), p2b = T.even_offset;
+        const uint32_t p3a = T.even_offset + T.n, p3b = T.span;
+        const uint32_t n1 = p1b > p1a ? p1b - p1a : 0u, n2 = p2b > p2a ? p2b - p2a : 0u;
+        const uint32_t n3 = p3b > p3a ? p3b - p3a : 0u;
+        for (uint32_t i = threadIdx.x; i < n1 + n2 + n3; i += 256u)
+            T.dst[i < n1 ? p1a + i : i < n1 + n2 ? p2a + (i - n1) : p3a + (i - n1 - n2)] = 0u;
     }
 }
 
@@ -909,6 +952,7 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         P.stripes = reinterpret_cast<const EncStripe *>(scr + SL.stripes);
         P.counts = reinterpret_cast<uint32_t *>(scr + SL.counts);
         P.tickets = reinterpret_cast<uint32_t *>(scr + SL.tickets);
+        P.edges = reinterpret_cast<uint32_t *>(scr + SL.edges);
         P.codes = reinterpret_cast<const uint32_t *>(scr + SL.codes);
         P.chunk_bits = reinterpret_cast<uint32_t *>(scr + SL.chunk_bits);
         P.chunk_start = reinterpret_cast<uint32_t *>(scr + SL.chunk_start);
@@ -978,7 +1022,8 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         if (e == cudaSuccess && !per_sub) e = cudaMemsetAsync(blob, 0, size_t(L.total), st);
         if (e == cudaSuccess) e = cudaMemcpyAsync(blob, head.data(), head.size(), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return cuda_fail(e);
-        if (per_sub) {
+        const bool one_pass = per_sub && chunk_syms == 4096;
+        if (per_sub && !one_pass) {
             uint64_t max_units = 1;
             for (size_t i = 0; i < ns; ++i)
                 max_units = std::max<uint64_t>(max_units, (desc[i].span - (desc[i].n & ~15u)) / 16u);
@@ -988,7 +1033,6 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         // 3-5. chunk bits, chunk index, packing
         const uint32_t wpb = kPackThreads / 32;
         const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_chunks + wpb - 1) / wpb));
-        const bool one_pass = per_sub && chunk_syms == 4096;
         if (one_pass) {
             // (tickets and look-back records were zeroed before the histogram)
             int sms = 0;
@@ -996,6 +1040,8 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
             const uint32_t per = std::max<uint32_t>(1, (2u * uint32_t(std::max(1, sms)) + uint32_t(ns) - 1) / uint32_t(ns));
             const uint32_t gl = std::min<uint32_t>(per, std::max<uint32_t>(1, (max_chunks + kLbWarps - 1) / kLbWarps));
             pack_lb_kernel<<<dim3(gl, uint32_t(ns)), kLbThreads, kLbSmem, st>>>(P);
+            const uint32_t gsm = std::min<uint32_t>(64, std::max<uint32_t>(1, (max_chunks + 255) / 256));
+            seam_kernel<<<dim3(gsm, uint32_t(ns)), 256, 0, st>>>(P);
         } else if (per_sub) {
             sub_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
             scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
