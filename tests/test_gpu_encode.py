@@ -117,7 +117,8 @@ def test_gpu_encoder_one_call_into_bound_buffer(name):
 def test_gpu_encoder_random_layers():
     """40 seeded random layers (alphabet size and skew, 1-4 tensors of
     1-600,000 values, the default layout or another, shared or per-tensor
-    tables): the GPU container equals the oracle's byte for byte.  The
+    tables), each encoded into a buffer filled with garbage: the GPU
+    container equals the oracle's byte for byte.  The
     default layout goes through the one-pass packer, whose look-back spans
     up to 147 chunks per stripe here, with ragged last chunks and lanes."""
     rng = np.random.default_rng(4242)
@@ -133,5 +134,10 @@ def test_gpu_encoder_random_layers():
         kw = {"shared_table": bool(rng.integers(0, 2))}
         if case % 4 == 3:
             kw["chunk_syms"] = int(rng.choice([1024, 2048, 8192]))
-        got = gpu_blob(tensors, **kw)
-        assert np.array_equal(got, oracle.encode_layer(tensors, **kw)), case
+        # into a buffer of garbage: every byte of the container is written
+        # (no pass zeroes it first on the default layout)
+        bound = k3.encode_bound([t.size for t in tensors], **kw)
+        buf = torch.full((bound,), 0xA5, dtype=torch.uint8, device="cuda")
+        got = k3.encode_layer_gpu([dev(x) for x in tensors], out=buf, **kw)
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy(), oracle.encode_layer(tensors, **kw)), case
