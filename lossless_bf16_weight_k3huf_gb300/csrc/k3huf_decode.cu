@@ -20,7 +20,7 @@
 //    stripe's stream, staged into the warp's shared-memory slot by one bulk
 //    copy (cp.async.bulk + the warp's mbarrier, bounded wait).  An item too
 //    long for the slot is decoded in passes over prefixes of its lanes;
-//  - one persistent CTA of 16 warps per SM takes a contiguous item range and
+//  - one persistent CTA per SM (18 warps; 16 for the fused GEMV) takes a contiguous item range and
 //    rebuilds the code table only when it changes; inside a table phase the
 //    warps take items from a shared counter, multi-pass items first (with a
 //    work area, the last sixteenth of every range is pooled across CTAs);
@@ -62,12 +62,9 @@ void set_cuda_error(int code) { g_last_cuda_error = code; }
 
 namespace {
 
-constexpr int kWarps = 16;                    // one CTA per SM
-constexpr int kThreads = 32 * kWarps;
 constexpr int kItem = 32;                     // sub-streams per work item (one warp)
 constexpr int kRound = 64;                    // values per lane between merges
 constexpr int kRowBytes = 64;                 // per-lane row: one round of high bytes (8-byte units, swizzled)
-constexpr uint32_t kBitBuf = 5056;            // bytes of staged bit stream per warp and pass
 constexpr int kMaxTasks = 64;                 // stripes per launch (kernel parameter space)
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kWaitLimit = 1u << 24;     // mbarrier polls before giving up
@@ -91,8 +88,23 @@ constexpr uint32_t kBadCode = 1u << 12;
 template <int kPer> __host__ __device__ constexpr int lock_bits() { return kPer == 2 ? 14 : 12; }
 constexpr size_t kSmemLut = (size_t(1) << 14) * sizeof(uint32_t);
 constexpr size_t kSmemL12 = 4096 * sizeof(uint16_t);
-constexpr size_t kWarpSlot = kBitBuf + 16 + size_t(32) * kRowBytes;   // bits + rows of one warp
-constexpr size_t kSmemBytes = kSmemLut + kSmemL12 + size_t(kWarps) * kWarpSlot;
+// The CTA's shape (one CTA per SM): warps, and each warp's slot of staged
+// bit stream per pass.  Shared memory stays just under the 196 KB carve-out
+// step, which leaves 60 KB of L1 for the low-byte loads in flight.  The
+// decode takes 18 warps, which the register file allows at 96 registers per
+// thread, with 4560-byte slots (a smaller slot splits more items into two
+// passes); the fused GEMV keeps 16 warps and 5056-byte slots, its
+// per-vector accumulators needing the registers.
+template <int kGemv> struct Shape {
+    static constexpr int warps = kGemv ? 16 : 18;
+    static constexpr int threads = 32 * warps;
+    static constexpr uint32_t bitbuf = kGemv ? 5056 : 4560;
+    static constexpr size_t slot = bitbuf + 16 + size_t(32) * kRowBytes;   // bits + rows of one warp
+    static constexpr size_t smem = kSmemLut + kSmemL12 + size_t(warps) * slot;
+};
+static_assert(Shape<0>::bitbuf % 16 == 0 && Shape<1>::bitbuf % 16 == 0, "16-byte bulk copies");
+static_assert(Shape<0>::smem + 6528 + 1024 <= 200704 && Shape<1>::smem + 6528 + 1024 <= 200704,
+              "shared memory (with the static arrays and the reserved 1 KB) under the 196 KB carve-out step");
 
 struct StripeTask {
     const uint8_t *stripe;      // device: stripe header
@@ -286,7 +298,7 @@ struct GlobalBits {
 //  - a lockstep entry reads the single-code table for each of its two codes
 //    (a block of four entries shares the first read, and fills all four
 //    from one pair of at most 12 bits).
-template <int kPer>
+template <int kPer, int kThreads>
 __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
     constexpr int L = K3HUF_MAXLEN;
     __shared__ uint32_t s_wcnt[8][L + 1];          // per warp: symbols of each length
@@ -441,6 +453,7 @@ __device__ __forceinline__ uint32_t find_task(const StripeTask *task, uint32_t n
 // chunk offsets) overflow one staging pass.  Such items take two or more
 // passes and are started first.  Deterministic in the container bytes, so
 // every warp classifies an item the same way; reads stay inside the stripe.
+template <uint32_t kBitBuf>
 __device__ bool item_heavy(const DecodeParams &P, const StripeTask *task, uint32_t wi) {
     const StripeTask &T = task[find_task(task, P.n_tasks, wi)];
     const uint32_t cs = P.chunk_syms, S = cs / P.sub_syms;
@@ -479,8 +492,11 @@ __device__ bool stripe_header_ok(const DecodeParams &P, const StripeTask &T, con
 // of 256) as compile-time constants, so that sub-stream and piece offsets
 // fold into immediates and divisions by them into shifts
 template <int kPer, bool kVec, bool kStaged, int kGemv, bool kFixed = false, bool kPool = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Shape<kGemv>::threads, 1)
 decode_kernel(const __grid_constant__ DecodeParams P) {
+    constexpr int kWarps = Shape<kGemv>::warps, kThreads = Shape<kGemv>::threads;
+    constexpr uint32_t kBitBuf = Shape<kGemv>::bitbuf;
+    constexpr size_t kWarpSlot = Shape<kGemv>::slot;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
     uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemLut);
@@ -624,11 +640,11 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
         for (uint32_t k = 0; k < 32u; ++k) {
             const uint32_t i = item + uint32_t(tid) + k * kThreads;
             if (i >= pend_own) break;
-            if (item_heavy(P, s_task, i)) hmask |= 1u << k;
+            if (item_heavy<kBitBuf>(P, s_task, i)) hmask |= 1u << k;
         }
         __syncthreads();                              // every warp done with the previous table
         if (rebuild) {
-            table_bad = !build_tables<kPer>(my_len, lut1, lut);
+            table_bad = !build_tables<kPer, kThreads>(my_len, lut1, lut);
             table_built = table;
         }
         if (steal >= 0 && table_bad) {                // (CTA-uniform) its items cannot be taken
@@ -653,7 +669,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                 if (k < kMaxHeavy) s_heavy[k] = item + uint32_t(tid) + uint32_t(__ffs(hmask) - 1) * kThreads;
             }
             for (uint32_t i = item + uint32_t(tid) + 32u * kThreads; i < pend_own; i += kThreads)
-                if (item_heavy(P, s_task, i)) {
+                if (item_heavy<kBitBuf>(P, s_task, i)) {
                     const uint32_t k = atomicAdd(&s_nheavy, 1u);
                     if (k < kMaxHeavy) s_heavy[k] = i;
                 }
@@ -1128,12 +1144,12 @@ int launch(DecodeParams &P, cudaStream_t stream, bool early = false) {
     }
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(kSmemBytes));
+                                 int(Shape<kGemv>::smem));
         int sms = 0, per_sm = 0;
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e == cudaSuccess)
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool>, kThreads,
-                                                              kSmemBytes);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool>,
+                                                              Shape<kGemv>::threads, Shape<kGemv>::smem);
         if (e != cudaSuccess) {
             set_cuda_error(int(e));
             return K3HUF_E_CUDA;
@@ -1153,8 +1169,8 @@ int launch(DecodeParams &P, cudaStream_t stream, bool early = false) {
         // the container, while the previous kernel in the stream finishes
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.blockDim = dim3(Shape<kGemv>::threads);
+        cfg.dynamicSmemBytes = Shape<kGemv>::smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1167,7 +1183,7 @@ int launch(DecodeParams &P, cudaStream_t stream, bool early = false) {
             return K3HUF_E_CUDA;
         }
     } else {
-        decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool><<<grid, kThreads, kSmemBytes, stream>>>(P);
+        decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool><<<grid, Shape<kGemv>::threads, Shape<kGemv>::smem, stream>>>(P);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -1184,7 +1200,7 @@ template <int kPer>
 int launch_syms(DecodeParams &P, cudaStream_t stream, bool early) {
     const bool vec = P.sub_syms % 8 == 0;
     // a sub-stream's bits (at most 12 per value) must fit the shared buffer
-    const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= kBitBuf;
+    const bool staged = uint64_t(P.sub_syms) * K3HUF_MAXLEN / 8 + 64 <= Shape<0>::bitbuf;
     if constexpr (kPer == 2)
         if (staged && P.chunk_syms == 4096 && P.sub_syms == 256)
             return P.work ? launch<2, true, true, false, true, true>(P, stream, early)
@@ -1386,7 +1402,7 @@ int gemv_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_lay
     const uint32_t ss = L.info.sub_syms, cs = L.info.chunk_syms;
     // every work item (32 sub-streams of ss values, whole chunks) must lie in one row
     if (te.n_values % cols != 0 || cols % (uint64_t(kItem) * ss) != 0 || ss % 8 != 0 || kItem % (cs / ss) != 0 ||
-        uint64_t(ss) * K3HUF_MAXLEN / 8 + 64 > kBitBuf)
+        uint64_t(ss) * K3HUF_MAXLEN / 8 + 64 > Shape<1>::bitbuf)
         return K3HUF_E_ARG;
     const uint8_t *blob = static_cast<const uint8_t *>(d_layer);
     DecodeParams P{};
