@@ -574,18 +574,20 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    is already held by a running warp, publishes the chunk's bit count,
 //    then sums its predecessors' published counts back to the nearest one
 //    whose first bit is known, and publishes its own first bit and end.
-//    14 warps per SM; the code table is held in 16 copies (lanes l and
+//    15 warps per SM: the code table is held in 16 copies (lanes l and
 //    l + 16 read copy l % 16: they conflict only on different symbols of
-//    the same parity), which leaves room for the 14th warp.
+//    the same parity), the rows carry no padding (XOR-swizzled pieces
+//    instead) and the runs no spare word (offset starts instead).
 //    Per chunk and warp:
 //  - when it takes the chunk, lane 0 starts an L2 prefetch of the chunk
 //    one round of the stripe's warps ahead;
 //  - its 8 KB of values are copied into shared memory (cp.async, coalesced
-//    16-byte pieces) as 32 rows of 128 values, one per lane, rows padded to
-//    272 bytes so that the lanes' reads of their rows never conflict;
+//    16-byte pieces) as 32 rows of 128 values, one per lane; piece j of
+//    row r sits at column j ^ (r % 16), so that the lanes' reads of their
+//    rows never conflict;
 //  - lane l owns values [128 l, 128 l + 128): half of sub-stream l / 2.  It
-//    codes them in order into a private run of words (rows of 49 words, so
-//    the lanes' stores fall in different banks), two codes at a time (at
+//    codes them in order into a private run of 48 words (lane l's starts at
+//    word 48 l + l / 2, so the lanes' stores fall in different banks), two codes at a time (at
 //    most 24 bits, so 32-bit shifts suffice; codes sit left-aligned in the
 //    table, and the append has no branch); its bit count comes out of the
 //    same pass;
@@ -601,12 +603,12 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    edge pair, and seam_kernel writes each shared word whole and zeroes
 //    the stripe's padding, so that no pass zeroes the stream beforehand.
 //    The input is read from DRAM once, here, after the histogram pass.
-constexpr int kLbWarps = 14;
+constexpr int kLbWarps = 15;
 constexpr int kLbThreads = 32 * kLbWarps;
-constexpr uint32_t kLbRow = 272;                          // a lane's 128 values (256 bytes) + 16 of padding
+constexpr uint32_t kLbRow = 256;                          // a lane's 128 values; piece j of row r at column j ^ (r % 16)
 constexpr uint32_t kLbIn = 32 * kLbRow;                   // one chunk's values, then its stream words
-constexpr uint32_t kLbRun = 49;                           // words of a lane's private run (128 x 12 bits + 1)
-constexpr uint32_t kLbWarpBytes = kLbIn + 4 * 32 * kLbRun;
+constexpr uint32_t kLbRun = 48;                           // words of a lane's private run (128 x 12 bits)
+constexpr uint32_t kLbWarpBytes = kLbIn + 4 * (32 * kLbRun + 16);   // lane l's run at word 48 l + l / 2
 constexpr size_t kLbSmem = size_t(256) * 16 * 4 + size_t(kLbWarps) * kLbWarpBytes;
 static_assert(kLbWarpBytes % 16 == 0, "per-warp staging must stay 16-byte aligned");
 static_assert(4096 * K3HUF_MAXLEN / 32 + 2 <= kLbIn / 4, "a chunk's stream words fit the staged rows");
@@ -668,7 +670,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
     __syncthreads();
     uint8_t *const in = lb_smem + size_t(256) * 16 * 4 + size_t(warp) * kLbWarpBytes;
     uint32_t *const sw = reinterpret_cast<uint32_t *>(in);           // the chunk's stream words, after the rows
-    uint32_t *const run = reinterpret_cast<uint32_t *>(in + kLbIn) + lane * kLbRun;
+    uint32_t *const run = reinterpret_cast<uint32_t *>(in + kLbIn) + lane * kLbRun + (lane >> 1);
     uint32_t *chunk_idx = reinterpret_cast<uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
     uint16_t *sub_idx = reinterpret_cast<uint16_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES + 4ull * T.n_chunks);
     uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
@@ -698,7 +700,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             for (uint32_t k = 0; k < 16; ++k) {
                 const uint32_t u = k * 32 + uint32_t(lane), off = u * 16;
                 const uint32_t sb = off < nbytes ? min(16u, nbytes - off) : 0u;
-                lb_cp16(in + (u >> 4) * kLbRow + (u & 15) * 16, sb ? src + off : src, sb);
+                lb_cp16(in + (u >> 4) * kLbRow + ((u ^ (u >> 4)) & 15) * 16, sb ? src + off : src, sb);
             }
             lb_cp_wait();
             __syncwarp();
@@ -711,7 +713,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         if (m == 128u) {
 #pragma unroll 2
             for (uint32_t j = 0; j < 16; ++j) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(row + 16 * j);
+                const uint4 x = *reinterpret_cast<const uint4 *>(row + 16 * ((j ^ uint32_t(lane)) & 15));
                 const uint32_t q[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) R.pair(code[(q[i] >> 8) & 0xFFu][lane & 15], code[q[i] >> 24][lane & 15]);
@@ -719,7 +721,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         } else {
             // a stripe's ragged end: one code at a time
             for (uint32_t v = 0; v < m; ++v) {
-                const uint32_t e = code[row[2 * v + 1]][lane & 15];
+                const uint32_t e = code[row[16 * (((v >> 3) ^ uint32_t(lane)) & 15) + ((2 * v + 1) & 15)]][lane & 15];
                 R.append(e & 0xFFF00000u, e & 31u);
             }
         }
@@ -743,7 +745,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         for (uint32_t k = 0; k < 16; ++k) {
             const uint32_t u = k * 32 + uint32_t(lane), vv = 8 * u;
             if (vv >= nv) continue;
-            const uint4 x = *reinterpret_cast<const uint4 *>(in + (u >> 4) * kLbRow + (u & 15) * 16);
+            const uint4 x = *reinterpret_cast<const uint4 *>(in + (u >> 4) * kLbRow + ((u ^ (u >> 4)) & 15) * 16);
             const uint32_t l0 = __byte_perm(x.x, x.y, 0x6420), l1 = __byte_perm(x.z, x.w, 0x6420);
             if (vv + 8 <= nv) {
                 *reinterpret_cast<uint2 *>(even + a + vv) = make_uint2(l0, l1);
