@@ -50,6 +50,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <vector>
 
@@ -1134,15 +1135,18 @@ bool pool_setup(DecodeParams &P, uint32_t grid) {
 
 template <int kPer, bool kVec, bool kStaged, int kGemv = 0, bool kFixed = false, bool kPool = false>
 int launch(DecodeParams &P, cudaStream_t stream, bool early = false) {
-    static bool attr_set[kMaxDevices] = {};      // per device; setting it twice is harmless
-    static int grid_max[kMaxDevices] = {};
+    // per device and instantiation: the grid size, 0 until the first launch
+    // has set the shared-memory opt-in (two threads doing it at once both set
+    // the same values, which is harmless)
+    static std::atomic<int> grid_max[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         set_cuda_error(int(e));
         return K3HUF_E_CUDA;
     }
-    if (!attr_set[dev]) {
+    int gmax = grid_max[dev].load(std::memory_order_acquire);
+    if (gmax == 0) {
         e = cudaFuncSetAttribute(decode_kernel<kPer, kVec, kStaged, kGemv, kFixed, kPool>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(Shape<kGemv>::smem));
         int sms = 0, per_sm = 0;
@@ -1154,10 +1158,10 @@ int launch(DecodeParams &P, cudaStream_t stream, bool early = false) {
             set_cuda_error(int(e));
             return K3HUF_E_CUDA;
         }
-        grid_max[dev] = std::max(1, sms * std::max(1, per_sm));
-        attr_set[dev] = true;
+        gmax = std::max(1, sms * std::max(1, per_sm));
+        grid_max[dev].store(gmax, std::memory_order_release);
     }
-    const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(grid_max[dev]));
+    const uint32_t grid = std::min<uint32_t>(P.n_items, uint32_t(gmax));
     if constexpr (kPool) {
         if (!pool_setup(P, grid)) {
             P.work = nullptr;
