@@ -587,21 +587,22 @@ __global__ void __launch_bounds__(kPackThreads, kPackCtasPerSm) pack_sub_kernel(
 //    rows never conflict;
 //  - lane l owns values [128 l, 128 l + 128): half of sub-stream l / 2.  It
 //    codes them in order into a private run of 48 words (lane l's starts at
-//    word 48 l + l / 2, so the lanes' stores fall in different banks), two codes at a time (at
-//    most 24 bits, so 32-bit shifts suffice; codes sit left-aligned in the
-//    table, and the append has no branch); its bit count comes out of the
-//    same pass;
+//    word 48 l + l / 2, so the lanes' stores fall in different banks), two
+//    codes at a time (at most 24 bits, so 32-bit shifts suffice; codes sit
+//    left-aligned in the table, and the append has no branch), and writes
+//    their low bytes back into its row (16 into each piece already read);
+//    its bit count comes out of the same pass;
 //  - a warp scan of the lanes' counts gives the chunk's count, which is
-//    published at once; the low bytes then leave from the staged rows
-//    (coalesced 8-byte stores), which takes the time predecessors need to
-//    publish theirs, and the look-back follows.  It gives every lane its
-//    first bit, and the rows take the chunk's stream words: each lane
-//    shifts its run into place (funnel shifts; only its first and last
-//    words, which neighbouring lanes share, by shared atomic OR);
-//  - the stream words leave with coalesced stores; the chunk's first and
-//    last words, when a neighbouring chunk shares them, go to a per-chunk
-//    edge pair, and seam_kernel writes each shared word whole and zeroes
-//    the stripe's padding, so that no pass zeroes the stream beforehand.
+//    published at once.  While predecessors publish theirs, the low bytes
+//    leave the rows with coalesced 16-byte stores, and the rows take
+//    the chunk's stream words relative to the chunk's first bit: each lane
+//    shifts its run into place (funnel shifts; its first and last words,
+//    which neighbouring lanes share, by shared atomic OR);
+//  - the look-back gives the chunk's first bit, and the stream words leave
+//    with coalesced stores, shifted to it.  The chunk's first and last
+//    words, when a neighbouring chunk shares them, go to a per-chunk edge
+//    pair, and seam_kernel writes each shared word whole and zeroes the
+//    stripe's padding, so that no pass zeroes the container beforehand.
 //    The input is read from DRAM once, here, after the histogram pass.
 constexpr int kLbWarps = 15;
 constexpr int kLbThreads = 32 * kLbWarps;
@@ -636,16 +637,18 @@ struct LbRun {
     uint32_t *rp;                                             // the word `pend` goes to
     // append the left-aligned string v of len bits (1 <= len <= 24).  No
     // branch: the word is stored every time (a partial one is stored again
-    // later) and the pointer moves on when it is full
+    // later) and the pointer moves on when it is full; the carry is written
+    // as arithmetic (multiply-adds), which leaves the shift and logic pipe
+    // to the shifts
     __device__ __forceinline__ void append(uint32_t v, uint32_t len) {
         const uint32_t w = pend | (v >> np);
         const uint32_t spill = __funnelshift_r(0u, v, np);   // v's bits past this word (0 when np = 0)
         const uint32_t t = np + len;
         *rp = w;
-        const bool full = t >= 32u;
-        pend = full ? spill : w;
-        rp += full ? 1 : 0;
-        np = t & 31u;
+        const uint32_t full = t >> 5;
+        pend = w + full * (spill - w);
+        rp += full;
+        np = t - 32u * full;
     }
     // two table entries (code << (32 - len)) | len (codes of at most 12
     // bits), the first code first
@@ -678,6 +681,9 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
     uint8_t *even = T.dst + T.even_offset;
     unsigned long long *rec = reinterpret_cast<unsigned long long *>(P.chunk_bits) + T.chunk_begin;
     const uint8_t *row = in + lane * kLbRow;
+    // code[s][lane % 16] at cbase + 64 s: table addresses by one byte
+    // permute and one multiply-add each
+    const uint8_t *const cbase = lb_smem + 4 * (lane & 15);
     for (;;) {
         uint32_t c = 0;
         if (lane == 0) {
@@ -706,22 +712,33 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             __syncwarp();
         }
         // 2. this lane's values [128 lane, 128 lane + m) of the chunk, coded
-        //    in order into its run, two at a time
+        //    in order into its run, two at a time; their low bytes go back
+        //    into the row, 16 at a time into a piece already read
         const uint32_t v0 = 128u * uint32_t(lane);
         const uint32_t m = v0 < nv ? min(128u, nv - v0) : 0u;
+        uint8_t *const ev = even + a + v0;
         LbRun R{0u, 0u, run};
         if (m == 128u) {
 #pragma unroll 2
-            for (uint32_t j = 0; j < 16; ++j) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(row + 16 * ((j ^ uint32_t(lane)) & 15));
-                const uint32_t q[4] = {x.x, x.y, x.z, x.w};
+            for (uint32_t j2 = 0; j2 < 8; ++j2) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(row + 16 * (((2 * j2) ^ uint32_t(lane)) & 15));
+                const uint4 y = *reinterpret_cast<const uint4 *>(row + 16 * (((2 * j2 + 1) ^ uint32_t(lane)) & 15));
+                const uint32_t q[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) R.pair(code[(q[i] >> 8) & 0xFFu][lane & 15], code[q[i] >> 24][lane & 15]);
+                for (int i = 0; i < 8; ++i)
+                    R.pair(*reinterpret_cast<const uint32_t *>(cbase + __byte_perm(q[i], 0, 0x4441) * 64u),
+                           *reinterpret_cast<const uint32_t *>(cbase + (q[i] >> 24) * 64u));
+                // (piece j2 of the row, already read: pieces 2 j2 and 2 j2 + 1 are)
+                *reinterpret_cast<uint4 *>(in + lane * kLbRow + 16 * ((j2 ^ uint32_t(lane)) & 15)) =
+                    make_uint4(__byte_perm(x.x, x.y, 0x6420), __byte_perm(x.z, x.w, 0x6420),
+                               __byte_perm(y.x, y.y, 0x6420), __byte_perm(y.z, y.w, 0x6420));
             }
         } else {
-            // a stripe's ragged end: one code at a time
+            // a stripe's ragged end: one value at a time
             for (uint32_t v = 0; v < m; ++v) {
-                const uint32_t e = code[row[16 * (((v >> 3) ^ uint32_t(lane)) & 15) + ((2 * v + 1) & 15)]][lane & 15];
+                const uint8_t *pv = row + 16 * (((v >> 3) ^ uint32_t(lane)) & 15) + ((2 * v) & 15);
+                ev[v] = pv[0];
+                const uint32_t e = code[pv[1]][lane & 15];
                 R.append(e & 0xFFF00000u, e & 31u);
             }
         }
@@ -736,30 +753,50 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         }
         const uint32_t lo = incl - bits, total = __shfl_sync(0xffffffffu, incl, 31);
         // 4. the chunk's bit count published (with its first bit, for the
-        //    stripe's first chunk); the work that does not need the first
-        //    bit comes before the look-back, while predecessors publish:
-        //    the low bytes of the chunk, 8 per lane and step, ...
-        uint32_t start = 0;
+        //    stripe's first chunk)
         if (lane == 0) atomicExch(rec + c, (c == 0 ? kLbIncl : kLbAgg) | total);
+        // the full lanes' low bytes, left in the first half of their rows,
+        // leave with coalesced 16-byte stores (piece u: lane u / 8's piece u % 8)
+        __syncwarp();
 #pragma unroll 4
-        for (uint32_t k = 0; k < 16; ++k) {
-            const uint32_t u = k * 32 + uint32_t(lane), vv = 8 * u;
-            if (vv >= nv) continue;
-            const uint4 x = *reinterpret_cast<const uint4 *>(in + (u >> 4) * kLbRow + ((u ^ (u >> 4)) & 15) * 16);
-            const uint32_t l0 = __byte_perm(x.x, x.y, 0x6420), l1 = __byte_perm(x.z, x.w, 0x6420);
-            if (vv + 8 <= nv) {
-                *reinterpret_cast<uint2 *>(even + a + vv) = make_uint2(l0, l1);
-            } else {
-                for (uint32_t i = 0; vv + i < nv; ++i) even[a + vv + i] = uint8_t((i < 4 ? l0 : l1) >> (8 * (i & 3)));
-            }
+        for (uint32_t k = 0; k < 8; ++k) {
+            const uint32_t u = k * 32 + uint32_t(lane), rr = u >> 3;
+            if (128u * rr + 128u > nv) continue;
+            *reinterpret_cast<uint4 *>(even + a + 16u * u) =
+                *reinterpret_cast<const uint4 *>(in + rr * kLbRow + 16 * (((u & 7u) ^ rr) & 15));
         }
         __syncwarp();
-        //    ... and the staging words zeroed (as many as any first bit needs)
+        // 5. what needs no first bit, while predecessors publish theirs: the
+        //    chunk's stream words staged in the rows (staging bit b is the
+        //    chunk's bit b), zeroed as far as any first bit needs, then each
+        //    lane shifts its run into place.  Word d0 + i is the run's words
+        //    i - 1 and i shifted right by lo % 32; the first and the last
+        //    (and a spill word) may be shared with neighbouring lanes
         {
             const uint32_t n_z = (total + 62u) >> 5;
             for (uint32_t k = lane; k < n_z; k += 32) sw[k] = 0u;
         }
-        // 5. the chunk's first bit within the stripe's stream: look-back
+        __syncwarp();
+        if (bits) {
+            const uint32_t d0 = lo >> 5, r = lo & 31u, kw = (bits + 31u) >> 5;
+            uint32_t *const dp = sw + d0;
+            uint32_t cur = run[0];
+            atomicOr(dp, cur >> r);
+            for (uint32_t i = 1; i + 1 < kw; ++i) {
+                const uint32_t nx = run[i];
+                dp[i] = __funnelshift_r(nx, cur, r);
+                cur = nx;
+            }
+            if (kw >= 2) {
+                const uint32_t nx = run[kw - 1];
+                atomicOr(dp + kw - 1, __funnelshift_r(nx, cur, r));
+                cur = nx;
+            }
+            if (((lo + bits - 1u) >> 5) == d0 + kw) atomicOr(dp + kw, __funnelshift_r(0u, cur, r));
+        }
+        __syncwarp();
+        uint32_t start = 0;
+        // 6. the chunk's first bit within the stripe's stream: look-back
         if (c != 0) {
             int64_t j = int64_t(c) - 1;
             uint32_t polls = 0;
@@ -783,7 +820,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             }
             if (lane == 0) atomicExch(rec + c, kLbIncl | (start + total));
         }
-        // 6. chunk index, sub-stream index (sub-stream k starts at lane 2k's
+        // 7. chunk index, sub-stream index (sub-stream k starts at lane 2k's
         //    first bit; one that starts at or past the chunk's end, at its
         //    end), the stripe header with the first chunk, the plan's total
         //    checked with the last
@@ -801,43 +838,28 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             h[7] = T.even_offset;
         }
         if (lane == 0 && c + 1 == T.n_chunks && uint64_t(start) + total != T.huff_bits) atomicOr(P.flag, 1u);
-        // 7. the rows take the chunk's stream words (staging bit b is stream
-        //    bit (start & ~31) + b): each lane shifts its run into place
-        const uint32_t sh = start & 31u, n_sw = (sh + total + 31u) >> 5;
-        __syncwarp();
-        if (bits) {
-            const uint32_t o = sh + lo, d0 = o >> 5, r = o & 31u, kw = (bits + 31u) >> 5;
-            uint32_t prev = 0;
-            for (uint32_t i = 0; i <= kw; ++i) {
-                const uint32_t cur = i < kw ? run[i] : 0u;
-                const uint32_t w = __funnelshift_r(cur, prev, r);   // (prev:cur) >> r, low word
-                prev = cur;
-                // (the word after the run's last one holds bits only when they spill over)
-                if (i == kw && (r == 0u || ((bits & 31u) != 0u && (bits & 31u) + r <= 32u))) break;
-                if (i == 0 || i + 1 >= kw) atomicOr(&sw[d0 + i], w);
-                else sw[d0 + i] = w;
-            }
-        }
-        __syncwarp();
-        // 8. the stream words out, in the stream's byte order (the staging
-        //    words hold their first bit at the top); the first and the last
-        //    may hold the neighbouring chunks' bits too
-        //    A word shared with a neighbouring chunk goes to the chunk's
-        //    edge pair instead; seam_kernel joins the two halves.  (Every
-        //    chunk but a stripe's last holds 4096 codes, so it spans more
-        //    than one word.)
-        const uint32_t w0 = start >> 5;
+        // 8. the stream words out, in the stream's byte order: stream word
+        //    (start >> 5) + k holds the chunk's bits [32 k - start % 32, + 32).
+        //    A word shared with a neighbouring chunk goes to the chunk's edge
+        //    pair instead; seam_kernel joins the two halves.  (Every chunk but
+        //    a stripe's last holds 4096 codes, so it spans more than one word.)
+        const uint32_t sh = start & 31u, n_sw = (sh + total + 31u) >> 5, w0 = start >> 5;
         const bool shared_head = sh != 0u;
         const bool shared_tail = ((start + total) & 31u) != 0u && c + 1 < T.n_chunks;
         if (lane == 0 && n_sw == 1 && shared_head && shared_tail) atomicOr(P.flag, 1u);
         uint32_t *const edge = P.edges + 2 * (size_t(T.chunk_begin) + c);
-        for (uint32_t k = lane; k < n_sw; k += 32) {
-            const uint32_t gw = w0 + k;
-            if (gw >= n_words) continue;
-            const uint32_t w = __byte_perm(sw[k], 0, 0x0123);
-            if (k == 0 && shared_head) edge[0] = w;
-            else if (k + 1 == n_sw && shared_tail) edge[1] = w;
-            else words[gw] = w;
+        const uint32_t k_lo = shared_head ? 1u : 0u, k_hi = shared_tail ? n_sw - 1u : n_sw;
+        if (w0 + n_sw <= n_words) {
+            uint32_t *const wp = words + w0;
+            for (uint32_t k = k_lo + uint32_t(lane); k < k_hi; k += 32)
+                wp[k] = __byte_perm(__funnelshift_r(sw[k], k ? sw[k - 1] : 0u, sh), 0, 0x0123);
+        } else if (lane == 0) {
+            atomicOr(P.flag, 1u);                     // (past the stream region: the plan disagrees)
+        }
+        if (lane == 0 && shared_head) edge[0] = __byte_perm(sw[0] >> sh, 0, 0x0123);
+        if (lane == 0 && shared_tail) {
+            const uint32_t k = n_sw - 1;
+            edge[1] = __byte_perm(__funnelshift_r(sw[k], k ? sw[k - 1] : 0u, sh), 0, 0x0123);
         }
         __syncwarp();                                 // the rows and the runs free again
     }
@@ -853,9 +875,12 @@ __global__ void __launch_bounds__(256) seam_kernel(EncParams P) {
     const uint32_t *chunk_idx = reinterpret_cast<const uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
     uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
     const uint32_t *edge = P.edges + 2 * size_t(T.chunk_begin);
+    const uint32_t n_words = (T.even_offset - T.bits_offset) / 4;
     for (uint32_t c = 1 + blockIdx.x * 256u + threadIdx.x; c < T.n_chunks; c += gridDim.x * 256u) {
         const uint32_t st = chunk_idx[c];
-        if (st & 31u) words[st >> 5] = edge[2 * (c - 1) + 1] | edge[2 * c];
+        // (a first bit past the stream region only comes with a packer that
+        // disagreed with the plan, which the call reports: nothing is written)
+        if ((st & 31u) && (st >> 5) < n_words) words[st >> 5] = edge[2 * (c - 1) + 1] | edge[2 * c];
     }
     if (blockIdx.x == 0) {
         const uint32_t p1a = K3HUF_STRIPE_HDR_BYTES + T.n_chunks * (4u + 2u * (P.S - 1u)), p1b = T.bits_offset;
