@@ -331,8 +331,8 @@ int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, con
  * counterpart: they encode offline on the CPU.
  * Its scratch is a fixed 32 MiB array inside the library, held by every GPU
  * that loads the library until the process exits; a layer whose
- * k3huf_encode_scratch_bytes exceeds 32 MiB (about 1.6 x 10^10 values in
- * 4096-value chunks) is refused with K3HUF_E_ARG.  Arguments, output and
+ * k3huf_encode_scratch_bytes exceeds 32 MiB (about 8.6 x 10^9 values in
+ * 4096-value chunks: 16 bytes of scratch per chunk) is refused with K3HUF_E_ARG.  Arguments, output and
  * errors otherwise as k3huf_encode_layer_gpu; nothing is allocated on the
  * device.  The first call on a device looks up the array's address on that
  * device (make that first call before any stream capture).  The array used
