@@ -192,6 +192,23 @@ int k3huf_decode_layer_ex(const void *h_layer_hdr, size_t hdr_bytes,
                           uint32_t *d_status, void *d_work, size_t work_bytes,
                           uint32_t flags, void *stream);
 
+/* Decode one tensor of a layer: its stripes only, in one launch (per
+ * launch of up to 64 stripes), for a caller that decodes each weight just
+ * before it is used.
+ *  tensor: index in the layer's tensor directory;
+ *  d_out / out_bytes: device, 16-byte aligned, at least 2 x the tensor's
+ *    values; receives the tensor's bf16 bytes from offset 0 (not at the
+ *    tensor's offset in the layer's output);
+ *  other arguments as for k3huf_decode_layer_ex (work area, flags, stream;
+ *    d_layer is the whole layer's container, as parsed from h_layer_hdr).
+ * Errors: K3HUF_E_ARG for a tensor index out of range or a short output,
+ * else as k3huf_decode_layer_ex. */
+int k3huf_decode_tensor(const void *h_layer_hdr, size_t hdr_bytes,
+                        const void *d_layer, size_t layer_bytes, uint32_t tensor,
+                        void *d_out, size_t out_bytes,
+                        uint32_t *d_status, void *d_work, size_t work_bytes,
+                        uint32_t flags, void *stream);
+
 /* Decode one stripe on the GPU (the article's per-stripe decode).
  *  codelen: host copy of the stripe's table (validated with k3huf_build);
  *  chunk_syms, sub_syms: values per indexed chunk and per sub-stream, as

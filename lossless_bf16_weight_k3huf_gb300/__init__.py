@@ -26,7 +26,7 @@ STRIPE_VALUES = 1 << 25
 
 EXPORTS = [
     "k3huf_build", "k3huf_layer_info", "k3huf_tensor_info", "k3huf_decode_layer", "k3huf_decode_layer_ws",
-    "k3huf_decode_layer_ex",
+    "k3huf_decode_layer_ex", "k3huf_decode_tensor",
     "k3huf_decode_stripe",
     "k3huf_set_decoder_variant", "k3huf_encode_layer", "k3huf_ring_create", "k3huf_ring_run",
     "k3huf_ring_destroy", "k3huf_last_cuda_error", "k3huf_strerror", "k3huf_feed_open", "k3huf_feed_direct",
@@ -93,6 +93,8 @@ def _lib():
             L.k3huf_decode_layer.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp, _vp]
             L.k3huf_decode_layer_ws.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp, _vp, _sz, _vp]
             L.k3huf_decode_layer_ex.argtypes = [_vp, _sz, _vp, _sz, _vp, _sz, _vp, _vp, _sz, ctypes.c_uint32, _vp]
+            L.k3huf_decode_tensor.argtypes = [_vp, _sz, _vp, _sz, ctypes.c_uint32, _vp, _sz, _vp, _vp, _sz,
+                                              ctypes.c_uint32, _vp]
             L.k3huf_decode_stripe.argtypes = [_vp, ctypes.c_uint32, ctypes.c_uint32, _vp, _sz, ctypes.c_uint32, _vp,
                                               _vp, _vp]
             L.k3huf_set_decoder_variant.argtypes = [ctypes.c_int]
@@ -307,6 +309,21 @@ def decode_layer(hdr, d_layer, d_out, d_status, stream=None, layer_bytes: int | 
         _check(_lib().k3huf_decode_layer_ws(h.ctypes.data, h.size, _dptr(d_layer), lb, _dptr(d_out), ob,
                                             _dptr(d_status), _dptr(work), _nbytes(work), _stream(stream)),
                "k3huf_decode_layer_ws")
+
+
+def decode_tensor(hdr, d_layer, tensor: int, d_out, d_status, stream=None, layer_bytes: int | None = None,
+                  out_bytes: int | None = None, work=None, early_start: bool = False) -> None:
+    """Launch the decode of one tensor of a layer (k3huf_decode_tensor):
+    ``d_out`` receives its bf16 bytes from offset 0.  ``work`` and
+    ``early_start`` as for decode_layer."""
+    h = _host(hdr)
+    lb = _nbytes(d_layer) if layer_bytes is None else layer_bytes
+    ob = _nbytes(d_out) if out_bytes is None else out_bytes
+    _check(_lib().k3huf_decode_tensor(h.ctypes.data, h.size, _dptr(d_layer), lb, int(tensor), _dptr(d_out), ob,
+                                      _dptr(d_status), None if work is None else _dptr(work),
+                                      0 if work is None else _nbytes(work),
+                                      DECODE_EARLY_START if early_start else 0, _stream(stream)),
+           "k3huf_decode_tensor")
 
 
 GEMV_ZERO_Y = 2

@@ -1293,14 +1293,27 @@ extern "C" int k3huf_set_decoder_variant(int variant) {
 }
 
 namespace {
+// The layer's stripes [0, n) into d_out at the layer's output offsets, or,
+// with tensor >= 0, that tensor's stripes into d_out from its first value
 int decode_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes, void *d_out,
-                      size_t out_bytes, uint32_t *d_status, uint32_t *d_work, bool early, void *stream) {
+                      size_t out_bytes, uint32_t *d_status, uint32_t *d_work, bool early, void *stream,
+                      int64_t tensor = -1) {
     if (!h_layer_hdr || !d_layer || !d_out || !d_status) return K3HUF_E_ARG;
     if (!aligned16(d_layer) || !aligned16(d_out) || (reinterpret_cast<uintptr_t>(d_status) & 3u)) return K3HUF_E_ARG;
     Layer L;
     int rc = parse_layer(h_layer_hdr, hdr_bytes, &L);
     if (rc) return rc;
-    if (layer_bytes < L.info.blob_bytes || out_bytes < L.info.out_bytes) return K3HUF_E_ARG;
+    size_t s_begin = 0, s_end = L.stripes.size();
+    uint64_t out_shift = 0, need = L.info.out_bytes;
+    if (tensor >= 0) {
+        if (uint64_t(tensor) >= L.tensors.size()) return K3HUF_E_ARG;
+        const TensorEntry &te = L.tensors[size_t(tensor)];
+        s_begin = te.first_stripe;
+        s_end = size_t(te.first_stripe) + te.n_stripes;
+        out_shift = te.out_offset;
+        need = 2 * te.n_values;
+    }
+    if (layer_bytes < L.info.blob_bytes || out_bytes < need) return K3HUF_E_ARG;
     const uint8_t *blob = static_cast<const uint8_t *>(d_layer);
     uint8_t *out = static_cast<uint8_t *>(d_out);
     DecodeParams P{};
@@ -1308,15 +1321,15 @@ int decode_layer_impl(const void *h_layer_hdr, size_t hdr_bytes, const void *d_l
     P.status = d_status;
     P.chunk_syms = L.info.chunk_syms;
     P.sub_syms = L.info.sub_syms;
-    for (size_t s0 = 0; s0 < L.stripes.size(); s0 += kMaxTasks) {
-        const size_t s1 = std::min(L.stripes.size(), s0 + kMaxTasks);
+    for (size_t s0 = s_begin; s0 < s_end; s0 += kMaxTasks) {
+        const size_t s1 = std::min(s_end, s0 + kMaxTasks);
         uint32_t items = 0;
         P.n_tasks = uint32_t(s1 - s0);
         for (size_t s = s0; s < s1; ++s) {
             const StripeEntry &e = L.stripes[s];
             StripeTask &t = P.task[s - s0];
             t.stripe = blob + e.blob_offset;
-            t.out = out + e.out_offset;
+            t.out = out + (e.out_offset - out_shift);
             t.stripe_bytes = e.stripe_bytes;
             t.n_values = e.n_values;
             t.table = e.table;
@@ -1354,6 +1367,16 @@ extern "C" int k3huf_decode_layer_ex(const void *h_layer_hdr, size_t hdr_bytes, 
     if (d_work && (work_bytes < K3HUF_WORK_BYTES || (reinterpret_cast<uintptr_t>(d_work) & 3u))) return K3HUF_E_ARG;
     return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status,
                              static_cast<uint32_t *>(d_work), (flags & K3HUF_DECODE_EARLY_START) != 0, stream);
+}
+
+extern "C" int k3huf_decode_tensor(const void *h_layer_hdr, size_t hdr_bytes, const void *d_layer, size_t layer_bytes,
+                                   uint32_t tensor, void *d_out, size_t out_bytes, uint32_t *d_status, void *d_work,
+                                   size_t work_bytes, uint32_t flags, void *stream) {
+    if (flags & ~uint32_t(K3HUF_DECODE_EARLY_START)) return K3HUF_E_ARG;
+    if (d_work && (work_bytes < K3HUF_WORK_BYTES || (reinterpret_cast<uintptr_t>(d_work) & 3u))) return K3HUF_E_ARG;
+    return decode_layer_impl(h_layer_hdr, hdr_bytes, d_layer, layer_bytes, d_out, out_bytes, d_status,
+                             static_cast<uint32_t *>(d_work), (flags & K3HUF_DECODE_EARLY_START) != 0, stream,
+                             int64_t(tensor));
 }
 
 extern "C" int k3huf_decode_stripe(const uint8_t codelen[256], uint32_t chunk_syms, uint32_t sub_syms,

@@ -249,6 +249,45 @@ def test_many_stripes_span_launches():
     check_parity(ts)
 
 
+def test_decode_tensor_alone():
+    """k3huf_decode_tensor: every tensor of a layer (one of them two stripes
+    long; per-tensor and shared tables) decoded alone into a buffer of its own
+    size with guard bytes after it, plainly and with a work area and early
+    start back to back: its bytes equal the input and the guard bytes stay.
+    A tensor index out of range and a short output are refused."""
+    tensors = [workloads.normal_tensor((300, 4097), 0.02, 7),
+               workloads.normal_tensor(((1 << 25) + 12_345,), 0.05, 8),
+               workloads.uniform_bytes(100_003, seed=9),
+               workloads.normal_tensor((5,), 0.3, 10)]
+    work = torch.zeros(k3.WORK_BYTES // 4, dtype=torch.int32, device="cuda")
+    for shared in (False, True):
+        blob = k3.encode_layer(tensors, shared_table=shared)
+        info = k3.layer_info(blob)
+        hdr = blob[: info["hdr_bytes"]]
+        d_blob = torch.from_numpy(blob).cuda()
+        for t, x in enumerate(tensors):
+            nb = 2 * x.size
+            outs = [torch.full((nb + 256,), SENTINEL, dtype=torch.uint8, device="cuda") for _ in range(2)]
+            st = torch.zeros(2, dtype=torch.int32, device="cuda")
+            k3.decode_tensor(hdr, d_blob, t, outs[0], st[0:1], out_bytes=nb)
+            k3.decode_tensor(hdr, d_blob, t, outs[1], st[1:2], out_bytes=nb, work=work, early_start=True)
+            torch.cuda.synchronize()
+            assert int(st.abs().sum().item()) == 0, (shared, t)
+            want = torch.from_numpy(np.ascontiguousarray(x).reshape(-1).view(np.uint8)).cuda()
+            for o in outs:
+                assert torch.equal(o[:nb], want), (shared, t)
+                assert bool((o[nb:] == SENTINEL).all()), (shared, t)
+        assert int(work.abs().sum().item()) == 0
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.empty(2 * tensors[0].size, dtype=torch.uint8, device="cuda")
+        with pytest.raises(k3.K3HufError) as e:
+            k3.decode_tensor(hdr, d_blob, len(tensors), out, st)
+        assert e.value.code == k3.E_ARG
+        with pytest.raises(k3.K3HufError) as e:
+            k3.decode_tensor(hdr, d_blob, 0, out, st, out_bytes=2 * tensors[0].size - 16)
+        assert e.value.code == k3.E_ARG
+
+
 def test_decode_stripe_entry():
     n = (1 << 25) + 70_000
     x = np.tile(workloads.tiny(), n // (1 << 21) + 1)[:n]
