@@ -240,6 +240,16 @@ def test_decode_argument_checks_need_no_device():
     assert ex(bad.ctypes.data, bad.size, 4096, bad.size, 4096, 1 << 20, 4096, None, 0, 1, None) == k3.E_FORMAT
     assert ex(b.ctypes.data, b.size, 4096, b.size - 1, 4096, 1 << 20, 4096, 8192, 68, 0, None) == k3.E_ARG
     assert k3.DECODE_EARLY_START == 1
+    # one tensor of the layer: flags, work area, tensor index and its output
+    # size are checked before any CUDA call (each case fails before a launch)
+    dt = L.k3huf_decode_tensor
+    n0 = k3.tensor_info(b, 0)["n_values"]
+    assert dt(b.ctypes.data, b.size, 4096, b.size, 0, 4096, 2 * n0, 4096, None, 0, 2, None) == k3.E_ARG      # flag
+    assert dt(b.ctypes.data, b.size, 4096, b.size, 0, 4096, 2 * n0, 4096, 8194, 68, 0, None) == k3.E_ARG     # work
+    assert dt(b.ctypes.data, b.size, 4096, b.size, 99, 4096, 2 * n0, 4096, None, 0, 0, None) == k3.E_ARG     # tensor
+    assert dt(b.ctypes.data, b.size, 4096, b.size, 0, 4096, 2 * n0 - 2, 4096, None, 0, 0, None) == k3.E_ARG  # short
+    assert dt(b.ctypes.data, b.size, 4096, b.size, 0, 4104, 2 * n0, 4096, None, 0, 0, None) == k3.E_ARG     # unaligned
+    assert dt(bad.ctypes.data, bad.size, 4096, bad.size, 0, 4096, 2 * n0, 4096, None, 0, 0, None) == k3.E_FORMAT
     # the GEMV with options: an unknown flag is refused first
     gx = L.k3huf_gemv_layer_ex
     assert gx(b.ctypes.data, b.size, 4096, b.size, 0, 8192, 4096, 4096, 4096, 4, None) == k3.E_ARG
