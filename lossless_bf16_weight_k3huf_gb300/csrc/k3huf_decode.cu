@@ -27,9 +27,9 @@
 //  - every lockstep lookup emits exactly two codes from a double-symbol
 //    table indexed by the next 14 bits (the codes stay 12-bit limited; the
 //    wider window halves the pairs that do not fit): a window that does not
-//    hold two whole codes gives the first code and the second is read from
-//    the 12-bit single-code table, so all lanes of the warp advance by the
-//    same number of values per step.  The 64-bit window is a funnel shift
+//    hold two whole codes gives the first code and the second is the first
+//    code of a second lookup at the bits after it, so all lanes of the warp
+//    advance by the same number of values per step.  The 64-bit window is a funnel shift
 //    of three stream words kept in registers from one group of four lookups
 //    to the next, and each lookup's successor is issued before the
 //    fallback test;
@@ -77,31 +77,31 @@ constexpr int kMaxPools = 16;                 // ranges end in one code table)
 // per lookup, 12 for one): exactly kPer whole codes.
 //   [4:0] bits used by the kPer codes (the shift, taken straight from the
 //   entry by a wrapping funnel shift) [23:16] first symbol [31:24] second
-//   symbol.  0 in [4:0] when the window does not hold kPer whole codes: then
-//   [11:8] is the first code's length and the second code is read from the
-//   single-code table.
-// Single-code table: the 4096-entry (sym << 4) | length table, indexed by
-// the next 12 bits.
+//   symbol, [11:8] the first code's length.  0 in [4:0] when the window
+//   does not hold kPer whole codes: the second code is then the first code
+//   of the entry at the bits after the first code.  Any single code is read
+//   that way ([23:16] and [11:8] of the entry its window indexes); the
+//   4096-entry (sym << 4) | length table the lockstep table is built from
+//   lives in the warp slots only while the tables are built.
 // A window where no code starts decodes as symbol 0 of length 1 with
-// kBadCode set (bit 12 in both tables): the decoder ORs the entries it
-// falls back on into one word and tests that bit once per pass.
+// kBadCode set (bit 12): the decoder ORs the entries it falls back on into
+// one word and tests that bit once per pass.
 constexpr uint32_t kBadCode = 1u << 12;
 template <int kPer> __host__ __device__ constexpr int lock_bits() { return kPer == 2 ? 14 : 12; }
 constexpr size_t kSmemLut = (size_t(1) << 14) * sizeof(uint32_t);
-constexpr size_t kSmemL12 = 4096 * sizeof(uint16_t);
 // The CTA's shape (one CTA per SM): warps, and each warp's slot of staged
 // bit stream per pass.  Shared memory stays just under the 196 KB carve-out
 // step, which leaves 60 KB of L1 for the low-byte loads in flight.  The
 // decode takes 18 warps, which the register file allows at 96 registers per
-// thread, with 4560-byte slots (a smaller slot splits more items into two
+// thread, with 5024-byte slots (a smaller slot splits more items into two
 // passes); the fused GEMV keeps 16 warps and 5056-byte slots, its
 // per-vector accumulators needing the registers.
 template <int kGemv> struct Shape {
     static constexpr int warps = kGemv ? 16 : 18;
     static constexpr int threads = 32 * warps;
-    static constexpr uint32_t bitbuf = kGemv ? 5056 : 4560;
+    static constexpr uint32_t bitbuf = kGemv ? 5056 : 5024;
     static constexpr size_t slot = bitbuf + 16 + size_t(32) * kRowBytes;   // bits + rows of one warp
-    static constexpr size_t smem = kSmemLut + kSmemL12 + size_t(warps) * slot;
+    static constexpr size_t smem = kSmemLut + size_t(warps) * slot;
 };
 static_assert(Shape<0>::bitbuf % 16 == 0 && Shape<1>::bitbuf % 16 == 0, "16-byte bulk copies");
 static_assert(Shape<0>::smem + 6528 + 1024 <= 200704 && Shape<1>::smem + 6528 + 1024 <= 200704,
@@ -422,12 +422,12 @@ __device__ bool build_tables(uint32_t my_len, uint16_t *lut1, uint32_t *lut) {
             if (a & kBadCode) {
                 ent = kBadCode | (1u << 8);                        // read by the fallback
             } else if (kPer == 1) {
-                ent = ((a >> 4) << 16) | l1;
+                ent = ((a >> 4) << 16) | (l1 << 8) | l1;
             } else {
                 const uint32_t b = lut1[((e << l1) & ((1u << W) - 1u)) >> (W - L)];
                 const uint32_t l2 = b & 15u;
                 if (!(b & kBadCode) && l1 + l2 <= uint32_t(W))
-                    ent = ((a >> 4) << 16) | ((b >> 4) << 24) | (l1 + l2);
+                    ent = ((a >> 4) << 16) | ((b >> 4) << 24) | (l1 << 8) | (l1 + l2);
                 else
                     ent = ((a >> 4) << 16) | (l1 << 8);            // second code read separately
             }
@@ -500,7 +500,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     constexpr size_t kWarpSlot = Shape<kGemv>::slot;
     extern __shared__ __align__(128) uint8_t smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(smem);
-    uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemLut);
+    uint16_t *lut1 = reinterpret_cast<uint16_t *>(smem + kSmemLut);   // (in the warp slots, during the builds)
     __shared__ __align__(8) uint64_t s_bar[kWarps];
     __shared__ uint32_t s_heavy[kMaxHeavy];
     __shared__ uint32_t s_nheavy, s_next;
@@ -514,7 +514,7 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // (one CTA per SM: a next grid started early takes the SMs this one frees)
     grid_dep_launch();
-    uint8_t *wslot = smem + kSmemLut + kSmemL12 + size_t(warp) * kWarpSlot;
+    uint8_t *wslot = smem + kSmemLut + size_t(warp) * kWarpSlot;
     uint32_t *bitbuf = reinterpret_cast<uint32_t *>(wslot);
     uint8_t *wrows = wslot + kBitBuf + 16;
 
@@ -844,14 +844,14 @@ decode_kernel(const __grid_constant__ DecodeParams P) {
                     hi = __funnelshift_l(w1, w0, cur);
                     lo = __funnelshift_l(w2, w1, cur);
                 };
-                // one code from the 12-bit single-code table; an undecodable
-                // window gives symbol 0 and one bit, and sets kBadCode in `bad`.
-                // The symbol's bit 8 carries that flag: callers keep the low byte
+                // one code: the first code of the lockstep entry its window
+                // indexes; an undecodable window gives symbol 0 and one bit,
+                // and sets kBadCode in `bad`.  Callers keep the low byte
                 auto single = [&](uint32_t win, uint32_t &len_out) -> uint32_t {
-                    const uint32_t a = lut1[win >> 20];
+                    const uint32_t a = lut[win >> (32 - kW)];
                     bad |= a;
-                    len_out = a & 15u;
-                    return a >> 4;
+                    len_out = (a >> 8) & 15u;
+                    return a >> 16;
                 };
 
                 // full rounds (every sub-stream of the item has 64 more values in
