@@ -31,6 +31,7 @@ the bytes all ranks decoded.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import itertools
 import json
@@ -877,8 +878,12 @@ def bench_ring(args, rank, world, local, dev):
 
 def bench_encode(args, rank, world, local, dev):
     """GPU encoder on the heavy-tail tensor: the container built on the
-    device from a device-resident tensor (host wall time per call: the call
-    synchronises after its histogram pass and at the end).  The container is
+    device from a device-resident tensor.  The call plans the codes and the
+    layout on the device and synchronises once, at the end, so K calls in a
+    row are timed with CUDA events around them (the host's share of each
+    call included); they are made through the C ABI with their arguments
+    marshalled once, and the Python binding's time per call is reported
+    beside it.  The container is
     checked byte for byte against the CPU encoder's (which the host tests
     check against the oracle's)."""
     import torch
@@ -900,14 +905,36 @@ def bench_encode(args, rank, world, local, dev):
     for _ in range(max(0, args.warmup - 1)):
         k3.encode_layer_gpu([d_x], scratch=scratch, out=out_buf)
     torch.cuda.synchronize()
-    times = []
+    # the C ABI call, its arguments marshalled once
+    enc = k3._lib().k3huf_encode_layer_gpu
+    c_ptrs = (ctypes.c_void_p * 1)(d_x.data_ptr())
+    c_nv = (ctypes.c_uint64 * 1)(n)
+    c_size = ctypes.c_size_t(0)
+    c_args = (1, c_ptrs, c_nv, 4096, 256, 0, scratch.data_ptr(), scratch.numel(), out_buf.data_ptr(),
+              out_buf.numel(), ctypes.byref(c_size), torch.cuda.current_stream(dev).cuda_stream)
+    for _ in range(3):
+        if enc(*c_args) != 0:
+            raise SystemExit("k3huf_encode_layer_gpu failed")
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        ev0.record()
         for _ in range(args.steps):
-            t0 = time.perf_counter()
-            k3.encode_layer_gpu([d_x], scratch=scratch, out=out_buf)
-            torch.cuda.synchronize()
-            times.append(time.perf_counter() - t0)
-    t = sum(times) / len(times)
+            if enc(*c_args) != 0:
+                raise SystemExit("k3huf_encode_layer_gpu failed")
+        ev1.record()
+        torch.cuda.synchronize()
+    t = ev0.elapsed_time(ev1) / 1e3 / args.steps
+    if c_size.value != blob.numel():
+        raise SystemExit("container size changed between calls")
+    # the same calls through the Python binding (host wall time)
+    tb = []
+    for _ in range(max(3, args.steps // 2)):
+        t0 = time.perf_counter()
+        k3.encode_layer_gpu([d_x], scratch=scratch, out=out_buf)
+        torch.cuda.synchronize()
+        tb.append(time.perf_counter() - t0)
+    tb = sorted(tb)[len(tb) // 2]
     # end to end: input from pinned host memory, container back to pinned host memory
     h_blob = torch.empty(blob.numel(), dtype=torch.uint8).pin_memory()
     d_in = torch.empty_like(d_x)                   # the input's device buffer, reused every step
@@ -929,10 +956,13 @@ def bench_encode(args, rank, world, local, dev):
         "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
         "config": {**describe("encode"), "values": n, "raw_bytes": raw, "blob_bytes": int(blob.numel()),
                    "compression_ratio": round(raw / blob.numel(), 4),
-                   "passes": ("histogram; one pass per 4096-value chunk: bit counts, chunk and sub-stream index "
-                              "(decoupled look-back), packing, low bytes (2 reads of the input); the words "
-                              "neighbouring chunks share joined and the padding zeroed"),
-                   "call": "one k3huf_encode_layer_gpu per step into a buffer of k3huf_encode_bound bytes",
+                   "passes": ("histogram; code lengths, codes and layout planned on the device; one pass per "
+                              "4096-value chunk: bit counts, chunk and sub-stream index (decoupled look-back), "
+                              "packing, low bytes (2 reads of the input); the words neighbouring chunks share "
+                              "joined and the padding zeroed"),
+                   "call": ("one k3huf_encode_layer_gpu per step (C ABI, CUDA events around the steps) into a "
+                            "buffer of k3huf_encode_bound bytes"),
+                   "python_binding_ms_per_call": round(tb * 1e3, 3),
                    "cpu_encoder_gbs": round(raw / cpu_enc_s / 1e9, 3),
                    "cpu_encoder_threads": os.cpu_count(), "l2": "inputs larger than L2"},
         "roofline": {"bound": "hbm", "achieved": round(alg / t / 1e9, 1), "peak": peak, "unit": "GB/s",
@@ -940,7 +970,7 @@ def bench_encode(args, rank, world, local, dev):
                      "traffic": ncu_traffic("encode"), "algorithmic_bytes_per_call": alg},
         "e2e": {"value": round(raw / te / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": raw,
                 "d2h_bytes_per_step": int(blob.numel())},
-        "gpu_launches": 3 * args.steps,                 # histogram, one-pass packing, seams
+        "gpu_launches": 4 * args.steps,                 # histogram, planner, one-pass packing, seams
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:

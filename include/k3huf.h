@@ -314,8 +314,10 @@ int k3huf_gemv_layer_batch(const void *h_layer_hdr, size_t hdr_bytes, const void
  * high-byte histogram, 12-bit-capped Huffman lengths, canonical
  * longest-first codes, MSB-first bit packing per stripe, low bytes raw.
  * Here the passes over the values (histogram, bit counts, packing, low-byte
- * copy) run on the GPU; code lengths and the layout are decided on the host
- * with the CPU encoder's own functions between them.
+ * copy) run on the GPU.  With the default chunk and sub-stream sizes (4096
+ * and 256) the code lengths, codes and layout are decided on the GPU too,
+ * with the CPU encoder's choices (ties included); with any other sizes on
+ * the host, between the passes, with the CPU encoder's own functions.
  *  d_tensors[t]: device, 16-byte aligned, n_values[t] (>= 1) bf16 values;
  *  chunk_syms, sub_syms, shared_table: as for k3huf_encode_layer;
  *  d_scratch: device, 256-byte aligned, scratch_bytes >=
@@ -324,10 +326,15 @@ int k3huf_gemv_layer_batch(const void *h_layer_hdr, size_t hdr_bytes, const void
  *    *blob_bytes is set (the histogram pass still runs).  A buffer of
  *    k3huf_encode_bound(...) bytes always suffices, so one call encodes;
  *    the container fills its first *blob_bytes bytes.
- * Synchronises `stream` twice (after the histograms and at the end) and
- * returns when the container is complete.  K3HUF_E_ARG on a bad argument
- * or a short buffer, K3HUF_E_FORMAT if the packed bits disagree with the
- * planned layout (an internal check), K3HUF_E_CUDA on a CUDA error. */
+ * Synchronises `stream` once, at the end, with the default sizes (twice
+ * with others: after the histograms too) and returns when the container is
+ * complete.  With the default sizes the first call on a host thread
+ * allocates a 256 KB page-locked host buffer that the thread keeps for its
+ * later calls (the call's one upload and its outcome; like any page-locked
+ * allocation, that first one may synchronise the device).  K3HUF_E_ARG on a bad argument or a short buffer (nothing is
+ * written to d_blob then; *blob_bytes is still set), K3HUF_E_FORMAT if the
+ * packed bits disagree with the planned layout (an internal check),
+ * K3HUF_E_CUDA on a CUDA error. */
 int k3huf_encode_scratch_bytes(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms,
                                uint32_t sub_syms, int shared_table, size_t *scratch_bytes);
 /* Upper bound of the container's size for any values of these sizes: the
@@ -351,7 +358,7 @@ int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, con
  * k3huf_encode_scratch_bytes exceeds 32 MiB (about 8.6 x 10^9 values in
  * 4096-value chunks: 16 bytes of scratch per chunk) is refused with K3HUF_E_ARG.  Arguments, output and
  * errors otherwise as k3huf_encode_layer_gpu; nothing is allocated on the
- * device.  The first call on a device looks up the array's address on that
+ * device, and no page-locked host memory either.  The first call on a device looks up the array's address on that
  * device (make that first call before any stream capture).  The array used
  * is the current device's copy, so every tensor, the output and the stream
  * must belong to the current device: a host pointer, another device's

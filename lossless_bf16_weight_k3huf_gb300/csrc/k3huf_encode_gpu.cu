@@ -4,27 +4,31 @@
 // Huffman 压缩实验" (section 已实现的部分) packs the trunk offline: a
 // histogram of the odd (high) bytes, Huffman code lengths capped at 12 bits,
 // canonical longest-first codes, the high bytes' codes packed MSB-first per
-// stripe, the even (low) bytes stored raw.  Here the passes over the values
-// run on the GPU, and the small decisions between them on the host:
+// stripe, the even (low) bytes stored raw.  Here every pass runs on the GPU:
 //  1. per-stripe histograms of the high bytes (per-warp shared-memory bins);
-//  2. host: code lengths, codes and the container layout, with the same
-//     functions as the CPU encoder (k3huf_host.cpp), so both write the same
-//     bytes; the header is copied in and the gaps no pass writes whole are
-//     zeroed;
-//  3. the default layout (chunks of 4096 values, sub-streams of 256): one
-//     pass per chunk that counts, indexes and packs, the chunks' first bits
-//     found by decoupled look-back along each stripe (pack_lb_kernel), so
-//     the values are read from DRAM only here after the histogram;
-//  3'-5'. any other layout: bits of every chunk (one warp per chunk,
+//  2. the default layout (chunks of 4096 values, sub-streams of 256): code
+//     lengths, codes and the container layout on the device (plan_kernel:
+//     one CTA per code table, the last one to finish places the stripes and
+//     writes the header), the same choices as the CPU encoder's functions,
+//     so no host round trip sits between the passes;
+//  3. the default layout: one pass per chunk that counts, indexes and packs,
+//     the chunks' first bits found by decoupled look-back along each stripe
+//     (pack_lb_kernel), so the values are read from DRAM only here after
+//     the histogram;
+//  2'. any other layout: code lengths, codes and the layout on the host,
+//     with the CPU encoder's functions (k3huf_host.cpp); the header is
+//     copied in and the gaps no pass writes whole are zeroed;
+//  3'-5'. then bits of every chunk (one warp per chunk,
 //     coalesced 16-byte loads); per stripe, one CTA scans them into the
 //     chunk index, writes the stripe header and checks the total against
 //     the planned bit count; then packing MSB-first (one warp per chunk or
 //     one lane per sub-stream), writing the sub-stream index and the low
 //     bytes in the same pass.
 // Scratch (caller-owned device memory, k3huf_encode_scratch_bytes) holds
-// the stripe descriptors, code tables, two shared stream words per chunk,
-// histograms, per-stripe chunk tickets, two words per chunk and an error
-// flag.
+// the stripe descriptors, the layer header as it is built, code tables, two
+// shared stream words per chunk, histograms, per-stripe chunk tickets, two
+// words per chunk, an error flag, the planner's ticket and the container's
+// size.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -50,19 +54,36 @@ struct EncStripe {
 
 struct EncParams {
     const EncStripe *stripes;
+    EncStripe *plan_stripes;   // the same descriptors, completed by plan_kernel
     const uint32_t *codes;     // n_tables x 256: (code << 4) | length
+    uint32_t *plan_codes;      // the same tables, written by plan_kernel
+    uint8_t *hdr;              // the layer header: every field the histogram
+                               // does not decide, from the host
+    uint8_t *blob;             // the container (plan_kernel copies the header in)
+    unsigned long long *total; // the container's size, from plan_kernel
+    uint32_t *plan_ticket;     // plan_kernel's CTAs that have finished their table
+    uint64_t blob_cap;
+    uint32_t *result;          // pinned host memory: flag, 0, size (low, high), written by the
+                               // call's last kernel (default layout; null: read back by a copy)
+    uint4 *zero;               // the histogram pass zeroes zero[0, n_zero) (default layout)
+    uint32_t n_zero;
+    uint32_t hdr_bytes, n_stripes, n_tensors, n_tables;
     uint32_t *counts;          // n_stripes x 256 histogram bins
     uint32_t *tickets;         // n_stripes: the one-pass packer's per-stripe chunk counters
     uint32_t *edges;           // the one-pass packer: per chunk, its first and last stream
                                // words when a neighbouring chunk shares them
     uint32_t *chunk_bits;      // bits of every chunk (or, one-pass packer: 64-bit records)
     uint32_t *chunk_start;     // first bit of every chunk within its stripe's stream
-    uint32_t *flag;            // nonzero: the packed bits disagree with the plan
+    uint32_t *flag;            // kFlagPlan: the packed bits disagree with the plan;
+                               // kFlagShort: the container does not fit blob_cap
     uint32_t chunk_syms, sub_syms, S;
 };
 
+constexpr uint32_t kFlagPlan = 1u, kFlagShort = 2u;
+
 struct ScratchLayout {
-    size_t stripes, codes, edges, counts, tickets, chunk_bits, chunk_start, flag, total;
+    size_t stripes, hdr, codes, edges, counts, tickets, chunk_bits, chunk_start, flag, plan_ticket, total_bytes,
+        total;
 };
 
 constexpr int kHistThreads = 256;
@@ -71,7 +92,13 @@ constexpr int kPackThreads = 256;
 constexpr int kStageWords = 128;     // staging window of a packing warp (one step: <= 97 words)
 constexpr int kPackCtasPerSm = 4;    // packing CTAs per SM the register budget is set for
 
-ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_chunks) {
+// Bytes of the layer header: fixed fields, code lengths, tensor and stripe
+// directories, padded to 256
+size_t header_bytes(size_t n_stripes, size_t n_tables, size_t n_tensors) {
+    return size_t(align_up(K3HUF_LAYER_HDR_BYTES + 256ull * n_tables + 32ull * n_tensors + 32ull * n_stripes, 256));
+}
+
+ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, size_t n_tensors, uint64_t n_chunks) {
     ScratchLayout s{};
     size_t at = 0;
     auto take = [&](size_t bytes) {
@@ -79,18 +106,24 @@ ScratchLayout scratch_layout(size_t n_stripes, size_t n_tables, uint64_t n_chunk
         at = size_t(align_up(at + bytes, 256));
         return here;
     };
-    // the descriptors and code tables go up in one copy, and everything from
-    // the histograms on is zeroed in one memset
+    // the default layout uploads the descriptors, the header and zeroed
+    // histograms in one copy, and the histogram pass zeroes everything from
+    // the tickets on
     s.stripes = take(n_stripes * sizeof(EncStripe));
+    s.hdr = take(header_bytes(n_stripes, n_tables, n_tensors));
+    s.counts = take(n_stripes * 256 * sizeof(uint32_t));
     s.codes = take(n_tables * 256 * sizeof(uint32_t));
     s.edges = take(size_t(n_chunks) * 2 * sizeof(uint32_t));
-    s.counts = take(n_stripes * 256 * sizeof(uint32_t));
     s.tickets = take(n_stripes * sizeof(uint32_t));
     // two words per chunk: the bit count and first bit of each chunk, or,
     // for the one-pass packer, one 64-bit look-back record per chunk
     s.chunk_bits = take(size_t(n_chunks) * 2 * sizeof(uint32_t));
     s.chunk_start = s.chunk_bits + size_t(n_chunks) * sizeof(uint32_t);
-    s.flag = take(sizeof(uint32_t));
+    // the flag, the planner's ticket and the container's size, which come
+    // back in one copy
+    s.flag = take(16);
+    s.plan_ticket = s.flag + 4;
+    s.total_bytes = s.flag + 8;
     s.total = at;
     return s;
 }
@@ -106,13 +139,34 @@ __global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
     __shared__ uint32_t h[kHistThreads / 32][256];
     const EncStripe &T = P.stripes[blockIdx.y];
     const int tid = threadIdx.x;
+    // (default layout: the packer's tickets and look-back records, the flag,
+    // the planner's ticket and the size start at zero)
+    for (uint64_t u = (uint64_t(blockIdx.y) * gridDim.x + blockIdx.x) * kHistThreads + tid; u < P.n_zero;
+         u += uint64_t(gridDim.x) * gridDim.y * kHistThreads)
+        P.zero[u] = make_uint4(0u, 0u, 0u, 0u);
     for (int i = tid; i < (kHistThreads / 32) * 256; i += kHistThreads) (&h[0][0])[i] = 0;
     __syncthreads();
     uint32_t *hw = h[tid >> 5];
     const uint64_t per = ((uint64_t(T.n) + gridDim.x - 1) / gridDim.x + 7) / 8 * 8;
     const uint64_t a = min(uint64_t(T.n), uint64_t(blockIdx.x) * per), b = min(uint64_t(T.n), a + per);
     const uint64_t vend = a + (b - a) / 8 * 8;
-    for (uint64_t k = a + uint64_t(tid) * 8; k < vend; k += uint64_t(kHistThreads) * 8) {
+    // four 16-byte loads in flight per thread, then their 32 high bytes
+    uint64_t k = a + uint64_t(tid) * 8;
+    for (; k + uint64_t(kHistThreads) * 24 < vend; k += uint64_t(kHistThreads) * 32) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(T.src + 2 * (k + uint64_t(kHistThreads) * 8 * j));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                atomicAdd(&hw[(w[i] >> 8) & 0xFFu], 1u);
+                atomicAdd(&hw[w[i] >> 24], 1u);
+            }
+        }
+    }
+    for (; k < vend; k += uint64_t(kHistThreads) * 8) {
         const uint4 v = *reinterpret_cast<const uint4 *>(T.src + 2 * k);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -128,6 +182,271 @@ __global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
         for (int w = 0; w < kHistThreads / 32; ++w) c += h[w][s];
         if (c) atomicAdd(&P.counts[size_t(blockIdx.y) * 256 + s], c);
     }
+}
+
+// 2. code lengths, codes and layout on the device (default layout).  CTA b
+//    builds table b from the histograms of its stripes (a tensor's stripes,
+//    or all of them for a shared table, are consecutive), with the choices
+//    the CPU encoder makes (k3huf_host.cpp):
+//    - Huffman lengths, ties on (count, id), leaves id = symbol, internal
+//      nodes 256 + creation order.  Merged weights never decrease, so the
+//      heap's order is that of two queues: the leaves sorted by (count,
+//      symbol) and the internal nodes as they are made; a leaf goes first
+//      on equal weights (its id is the smaller);
+//    - the 12-bit cap: clamp, then while the Kraft sum is over-full lengthen
+//      the lowest-count code shorter than 12 bits (ties to the larger
+//      symbol).  That code stays the lowest until it reaches 12 bits, so the
+//      codes are taken in (count, larger symbol first) order, each lengthened
+//      until the sum fits or it reaches 12;
+//    - canonical longest-first codes (article "Kimi K3 纯 CPU 推理中的无损
+//      Trunk 压缩", section 规范码分配与 Kraft 校验).
+//    It then sizes its stripes.  The last CTA to finish (a ticket, no
+//    waiting) places every stripe at a 256-byte boundary after the header
+//    (a prefix sum of the rounded sizes), completes the header and copies
+//    it into the blob, or flags a blob too small for the container and
+//    writes nothing.
+constexpr int kPlanThreads = 256;
+
+__device__ __forceinline__ unsigned long long plan_align(unsigned long long x, unsigned long long a) {
+    return (x + a - 1) / a * a;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(EncParams P) {
+    __shared__ unsigned long long wl[258], wi[256], s_warp[kPlanThreads / 32];
+    __shared__ uint16_t par[512];
+    __shared__ uint8_t sym[256], len[256];
+    __shared__ uint32_t ord[256], lmask[kPlanThreads / 32][16], first[16], s_n, s_last;
+    const uint32_t s = threadIdx.x, tb = blockIdx.x;
+    const uint32_t lane = s & 31u, warp = s >> 5, lt = (1u << lane) - 1u;
+    // the table's stripes: all of them for one table, else tensor tb's (from
+    // the header's tensor directory: table, first stripe, stripes)
+    uint32_t lo = 0, hi = P.n_stripes;
+    if (P.n_tables > 1) {
+        const uint32_t *te = reinterpret_cast<const uint32_t *>(P.hdr + K3HUF_LAYER_HDR_BYTES +
+                                                                256ull * P.n_tables + 32ull * tb);
+        lo = te[1];
+        hi = lo + te[2];
+    }
+    unsigned long long c = 0;
+#pragma unroll 8
+    for (uint32_t i = lo; i < hi; ++i) c += P.counts[size_t(i) * 256 + s];
+    // the used symbols, then their (count, symbol) order
+    const uint32_t used = __ballot_sync(0xffffffffu, c != 0);
+    if (lane == 0) lmask[warp][0] = __popc(used);
+    __syncthreads();
+    uint32_t at = __popc(used & lt), n = 0;
+    for (uint32_t w = 0; w < kPlanThreads / 32; ++w) {
+        const uint32_t k = lmask[w][0];
+        at += w < warp ? k : 0u;
+        n += k;
+    }
+    if (c) {
+        wi[at] = c;                                // (scratch: the used counts, compacted)
+        ord[at] = s;
+    }
+    __syncthreads();
+    if (c) {
+        uint32_t r = 0;
+        for (uint32_t j = 0; j < n; ++j) {
+            const unsigned long long cj = wi[j];
+            r += uint32_t(cj < c) | (uint32_t(cj == c) & uint32_t(ord[j] < s));
+        }
+        wl[r] = c;
+        sym[r] = uint8_t(s);
+    }
+    if (s == 0) wl[n] = wl[n + 1] = ~0ull;         // (no leaf left)
+    __syncthreads();
+    // the tree: node 256 + k is made from the two lightest of the leaves not
+    // yet taken and the nodes made before it (weights cached in registers)
+    if (s == 0 && n > 1) {
+        // This loop is the planner's serial part: selects, no branches, and
+        // each queue's first two weights held in registers (L0, L1 leaves,
+        // I0, I1 nodes; ~0 where there is none yet), so the shared-memory
+        // load a pick issues is needed one pick later
+        uint32_t li = 0, qi = 0, S0 = sym[0], S1 = sym[1];
+        unsigned long long L0 = wl[0], L1 = wl[1], I0 = ~0ull, I1 = ~0ull;
+        for (uint32_t k = 0; k + 1 < n; ++k) {
+            unsigned long long w = 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const bool node = I0 < L0;
+                par[node ? 256 + qi : S0] = uint16_t(256 + k);
+                w += node ? I0 : L0;
+                const unsigned long long wl2 = wl[min(li + 2, 257u)], wi2 = qi + 2 < k ? wi[qi + 2] : ~0ull;
+                const uint32_t s2 = sym[min(li + 2, 255u)];
+                qi += node;
+                li += !node;
+                I0 = node ? I1 : I0;
+                I1 = node ? wi2 : I1;
+                L0 = node ? L0 : L1;
+                S0 = node ? S0 : S1;
+                L1 = node ? L1 : wl2;
+                S1 = node ? S1 : s2;
+            }
+            wi[k] = w;
+            I0 = qi == k ? w : I0;
+            I1 = qi + 1 == k ? w : I1;
+        }
+    }
+    __syncthreads();
+    // depths (a lone symbol gets one bit), clamped to 12
+    uint32_t d = 0;
+    if (c) {
+        if (n == 1) {
+            d = 1;
+        } else {
+            const uint32_t root = 256 + n - 2;
+            uint32_t x = s;
+            for (uint32_t g = 0; g < 256 && x != root; ++g, ++d) x = par[x];
+        }
+        d = min(d, uint32_t(K3HUF_MAXLEN));
+    }
+    len[s] = uint8_t(d);
+    // the Kraft sum in 2^-12 units (at most 256 x 2^11)
+    const uint32_t kw = __reduce_add_sync(0xffffffffu, c ? (1u << K3HUF_MAXLEN) >> d : 0u);
+    // codes shorter than 12 bits, in (count, larger symbol first) order
+    const bool short_code = c != 0 && d < uint32_t(K3HUF_MAXLEN);
+    const uint32_t sb = __ballot_sync(0xffffffffu, short_code);
+    __syncthreads();                               // (the tree's arrays are free again)
+    if (lane == 0) {
+        lmask[warp][1] = __popc(sb);
+        lmask[warp][2] = kw;
+    }
+    __syncthreads();
+    uint32_t sat = __popc(sb & lt), n_short = 0, kraft = 0;
+    for (uint32_t w = 0; w < kPlanThreads / 32; ++w) {
+        const uint32_t k = lmask[w][1];
+        sat += w < warp ? k : 0u;
+        n_short += k;
+        kraft += lmask[w][2];
+    }
+    if (short_code) {
+        wi[sat] = c;
+        ord[sat] = s;
+    }
+    __syncthreads();
+    uint32_t r2 = 0;
+    if (short_code)
+        for (uint32_t j = 0; j < n_short; ++j) {
+            const unsigned long long cj = wi[j];
+            r2 += uint32_t(cj < c) | (uint32_t(cj == c) & uint32_t(ord[j] > s));
+        }
+    __syncthreads();
+    if (short_code) ord[r2] = s;
+    __syncthreads();
+    if (s == 0) {
+        uint32_t k = kraft;
+        for (uint32_t r = 0; r < n_short && k > (1u << K3HUF_MAXLEN); ++r) {
+            const uint32_t t = ord[r];
+            uint32_t l = len[t];
+            for (; k > (1u << K3HUF_MAXLEN) && l < uint32_t(K3HUF_MAXLEN); ++l) k -= (1u << K3HUF_MAXLEN) >> (l + 1);
+            len[t] = uint8_t(l);
+        }
+    }
+    __syncthreads();
+    // canonical codes: per length, longest first, symbols in order
+    const uint32_t l = len[s];
+#pragma unroll
+    for (uint32_t q = 1; q <= uint32_t(K3HUF_MAXLEN); ++q) {
+        const uint32_t m = __ballot_sync(0xffffffffu, l == q);
+        if (lane == 0) lmask[warp][q] = m;
+    }
+    __syncthreads();
+    if (s == 0) {
+        uint32_t next = 0;
+        for (int q = K3HUF_MAXLEN; q >= 1; --q) {
+            uint32_t nq = 0;
+            for (uint32_t w = 0; w < kPlanThreads / 32; ++w) nq += __popc(lmask[w][q]);
+            first[q] = next;
+            next = (next + nq + 1) >> 1;
+        }
+    }
+    __syncthreads();
+    uint32_t code = 0;
+    if (l) {
+        code = first[l] + __popc(lmask[warp][l] & lt);
+        for (uint32_t w = 0; w < warp; ++w) code += __popc(lmask[w][l]);
+    }
+    P.plan_codes[size_t(tb) * 256 + s] = l ? (code << 4) | l : 0u;
+    P.hdr[K3HUF_LAYER_HDR_BYTES + size_t(tb) * 256 + s] = uint8_t(l);
+    // this table's stripes: bits, low bytes' offset and size (the size into
+    // the header's stripe directory); warp w takes stripes lo + w, lo + w + 8, ...
+    uint8_t *const sd = P.hdr + K3HUF_LAYER_HDR_BYTES + 256ull * P.n_tables + 32ull * P.n_tensors;
+    for (uint32_t i = lo + warp; i < hi; i += kPlanThreads / 32) {
+        unsigned long long b = 0;
+#pragma unroll
+        for (uint32_t q = lane; q < 256; q += 32) b += (unsigned long long)P.counts[size_t(i) * 256 + q] * len[q];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+        if (lane == 0) {
+            EncStripe &T = P.plan_stripes[i];
+            T.huff_bits = b;
+            T.even_offset = uint32_t(T.bits_offset + plan_align((b + 7) / 8, 16) + kBitsSlack);
+            *reinterpret_cast<unsigned long long *>(sd + 32ull * i + 8) = T.even_offset + plan_align(T.n, 16);
+        }
+    }
+    // with several tables, the last CTA to finish goes on
+    if (gridDim.x > 1) {
+        __threadfence();
+        __syncthreads();
+        if (s == 0) s_last = atomicAdd(P.plan_ticket, 1u) == gridDim.x - 1;
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+    } else {
+        __syncthreads();
+    }
+    // stripe i at hdr_bytes + the sum of the earlier stripes' sizes rounded
+    // up to 256 bytes; 256 stripes per round, the carry in s_warp[0]
+    unsigned long long carry = P.hdr_bytes;
+    for (uint32_t base = 0; base < P.n_stripes; base += kPlanThreads) {
+        const uint32_t i = base + s;
+        const unsigned long long bytes =
+            i < P.n_stripes ? *reinterpret_cast<volatile unsigned long long *>(sd + 32ull * i + 8) : 0ull;
+        const unsigned long long rounded = plan_align(bytes, 256);
+        unsigned long long incl = rounded;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= uint32_t(o)) incl += t;
+        }
+        __syncthreads();                           // (s_warp of the round before is read)
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        unsigned long long off = carry + incl - rounded, round_total = 0;
+        for (uint32_t w = 0; w < kPlanThreads / 32; ++w) {
+            off += w < warp ? s_warp[w] : 0ull;
+            round_total += s_warp[w];
+        }
+        if (i < P.n_stripes) {
+            EncStripe &T = P.plan_stripes[i];
+            *reinterpret_cast<unsigned long long *>(sd + 32ull * i) = off;
+            T.dst = P.blob ? P.blob + off : nullptr;
+            const bool last = i + 1 == P.n_stripes;
+            T.span = uint32_t(last ? bytes : rounded);
+            if (last) {
+                // the container ends with the last stripe's bytes
+                *reinterpret_cast<unsigned long long *>(P.hdr + 32) = off + bytes;
+                *P.total = off + bytes;
+                if (P.result && !P.blob) {                 // (no packing follows: the call's last kernel)
+                    volatile uint32_t *r = P.result;
+                    r[0] = 0u;
+                    r[1] = 0u;
+                    r[2] = uint32_t(off + bytes);
+                    r[3] = uint32_t((off + bytes) >> 32);
+                }
+                const bool fits = off + bytes <= P.blob_cap;
+                if (P.blob && !fits) atomicOr(P.flag, kFlagShort);
+                s_n = P.blob && fits;
+            }
+        }
+        carry += round_total;
+    }
+    __syncthreads();
+    if (!s_n) return;
+    // the header into the blob (other CTAs wrote parts of it: read from L2)
+    for (uint32_t q = s; q < P.hdr_bytes / 16; q += kPlanThreads)
+        reinterpret_cast<uint4 *>(P.blob)[q] = __ldcg(reinterpret_cast<const uint4 *>(P.hdr) + q);
 }
 
 // 3. bits of every chunk: one warp per chunk, 8 values per lane and step
@@ -235,7 +554,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(EncParams P) {
         P.chunk_start[T.chunk_begin + c] = uint32_t(off);
         off += bits[c];
     }
-    if (c_hi == nch && c_lo < c_hi && off != T.huff_bits) atomicOr(P.flag, 1u);
+    if (c_hi == nch && c_lo < c_hi && off != T.huff_bits) atomicOr(P.flag, kFlagPlan);
     if (tid == 0) {
         uint32_t *h = reinterpret_cast<uint32_t *>(T.dst);
         h[0] = kStripeMagic;
@@ -659,6 +978,7 @@ struct LbRun {
 };
 
 __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
+    if (*P.flag & kFlagShort) return;                // (the planner found the blob too small)
     extern __shared__ __align__(16) uint8_t lb_smem[];
     uint32_t(*code)[16] = reinterpret_cast<uint32_t(*)[16]>(lb_smem);   // entry s for lanes l, l + 16 at code[s][l % 16]
     const EncStripe &T = P.stripes[blockIdx.y];
@@ -806,7 +1126,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
                     idx >= 0 ? *reinterpret_cast<volatile unsigned long long *>(rec + idx) : kLbIncl;
                 if (__any_sync(0xffffffffu, (r >> 62) == 0)) {
                     if (++polls >= kLbSpin) {              // (a predecessor never published: give up)
-                        if (lane == 0) atomicOr(P.flag, 1u);
+                        if (lane == 0) atomicOr(P.flag, kFlagPlan);
                         break;
                     }
                     __nanosleep(32);
@@ -837,7 +1157,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             h[6] = T.bits_offset;
             h[7] = T.even_offset;
         }
-        if (lane == 0 && c + 1 == T.n_chunks && uint64_t(start) + total != T.huff_bits) atomicOr(P.flag, 1u);
+        if (lane == 0 && c + 1 == T.n_chunks && uint64_t(start) + total != T.huff_bits) atomicOr(P.flag, kFlagPlan);
         // 8. the stream words out, in the stream's byte order: stream word
         //    (start >> 5) + k holds the chunk's bits [32 k - start % 32, + 32).
         //    A word shared with a neighbouring chunk goes to the chunk's edge
@@ -846,7 +1166,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         const uint32_t sh = start & 31u, n_sw = (sh + total + 31u) >> 5, w0 = start >> 5;
         const bool shared_head = sh != 0u;
         const bool shared_tail = ((start + total) & 31u) != 0u && c + 1 < T.n_chunks;
-        if (lane == 0 && n_sw == 1 && shared_head && shared_tail) atomicOr(P.flag, 1u);
+        if (lane == 0 && n_sw == 1 && shared_head && shared_tail) atomicOr(P.flag, kFlagPlan);
         uint32_t *const edge = P.edges + 2 * (size_t(T.chunk_begin) + c);
         const uint32_t k_lo = shared_head ? 1u : 0u, k_hi = shared_tail ? n_sw - 1u : n_sw;
         if (w0 + n_sw <= n_words) {
@@ -854,7 +1174,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
             for (uint32_t k = k_lo + uint32_t(lane); k < k_hi; k += 32)
                 wp[k] = __byte_perm(__funnelshift_r(sw[k], k ? sw[k - 1] : 0u, sh), 0, 0x0123);
         } else if (lane == 0) {
-            atomicOr(P.flag, 1u);                     // (past the stream region: the plan disagrees)
+            atomicOr(P.flag, kFlagPlan);                     // (past the stream region: the plan disagrees)
         }
         if (lane == 0 && shared_head) edge[0] = __byte_perm(sw[0] >> sh, 0, 0x0123);
         if (lane == 0 && shared_tail) {
@@ -871,6 +1191,16 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
 // the stream region after its last word, and the low bytes' tail up to the
 // next stripe (a few hundred bytes per stripe).
 __global__ void __launch_bounds__(256) seam_kernel(EncParams P) {
+    if (P.result && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        // the call's outcome, straight into the host's memory
+        volatile uint32_t *r = P.result;
+        const unsigned long long total = *P.total;
+        r[0] = *P.flag;
+        r[1] = 0u;
+        r[2] = uint32_t(total);
+        r[3] = uint32_t(total >> 32);
+    }
+    if (*P.flag & kFlagShort) return;
     const EncStripe &T = P.stripes[blockIdx.y];
     const uint32_t *chunk_idx = reinterpret_cast<const uint32_t *>(T.dst + K3HUF_STRIPE_HDR_BYTES);
     uint32_t *words = reinterpret_cast<uint32_t *>(T.dst + T.bits_offset);
@@ -912,6 +1242,34 @@ int cuda_fail(cudaError_t e) {
     return K3HUF_E_CUDA;
 }
 
+// Pinned host staging for the default layout's one upload and one read
+// back, one buffer per host thread, allocated on the thread's first call
+// and never grown: a call whose upload does not fit goes through pageable
+// memory instead.  Every call synchronises its stream before it returns,
+// so the next call on the thread finds the buffer free.
+constexpr size_t kStageBytes = size_t(256) << 10;
+
+struct PinnedStage {
+    uint8_t *p = nullptr;
+    bool tried = false;
+    ~PinnedStage() {
+        if (p) (void)cudaFreeHost(p);
+    }
+};
+
+uint8_t *pinned_stage() {
+    thread_local PinnedStage t;
+    if (!t.tried) {
+        t.tried = true;
+        void *q = nullptr;
+        if (cudaMallocHost(&q, kStageBytes) == cudaSuccess)
+            t.p = static_cast<uint8_t *>(q);
+        else
+            (void)cudaGetLastError();
+    }
+    return t.p;
+}
+
 int check_inputs(uint32_t n_tensors, const uint64_t *n_values, uint32_t chunk_syms) {
     if (n_tensors == 0 || !n_values || chunk_syms == 0) return K3HUF_E_ARG;
     for (uint32_t t = 0; t < n_tensors; ++t)
@@ -947,17 +1305,22 @@ extern "C" int k3huf_encode_scratch_bytes(uint32_t n_tensors, const uint64_t *n_
     try {
         LayerPlan L;
         plan_stripes(n_tensors, n_values, chunk_syms, effective_sub_syms(chunk_syms, sub_syms), shared_table != 0, L);
-        *scratch_bytes = scratch_layout(L.stripes.size(), L.n_tables, count_chunks(L)).total;
+        *scratch_bytes = scratch_layout(L.stripes.size(), L.n_tables, L.n_tensors, count_chunks(L)).total;
         return K3HUF_OK;
     } catch (const std::bad_alloc &) {
         return K3HUF_E_NOMEM;
     }
 }
 
-extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
-                                      uint32_t chunk_syms, uint32_t sub_syms_req, int shared_table,
-                                      void *d_scratch, size_t scratch_bytes, void *d_blob, size_t blob_cap,
-                                      size_t *blob_bytes, void *stream) {
+namespace k3huf {
+namespace {
+
+// The GPU encoder; `may_pin`: the default layout may stage through the
+// thread's pinned host buffer (allocating it on the thread's first call)
+int encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
+                     uint32_t chunk_syms, uint32_t sub_syms_req, int shared_table, void *d_scratch,
+                     size_t scratch_bytes, void *d_blob, size_t blob_cap, size_t *blob_bytes, void *stream,
+                     bool may_pin) {
     int rc = check_inputs(n_tensors, n_values, chunk_syms);
     if (rc) return rc;
     if (!d_tensors || !d_scratch || !blob_bytes || (reinterpret_cast<uintptr_t>(d_scratch) & 255u)) return K3HUF_E_ARG;
@@ -972,7 +1335,7 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         const size_t ns = L.stripes.size();
         const uint64_t n_chunks = count_chunks(L);
         if (ns > 65535 || n_chunks > 0xFFFFFFFFull) return K3HUF_E_ARG;
-        const ScratchLayout SL = scratch_layout(ns, L.n_tables, n_chunks);
+        const ScratchLayout SL = scratch_layout(ns, L.n_tables, L.n_tensors, n_chunks);
         if (scratch_bytes < SL.total) return K3HUF_E_ARG;
         uint8_t *scr = static_cast<uint8_t *>(d_scratch);
         EncParams P{};
@@ -987,6 +1350,17 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         P.chunk_syms = chunk_syms;
         P.sub_syms = sub_syms;
         P.S = chunk_syms / sub_syms;
+        P.plan_stripes = reinterpret_cast<EncStripe *>(scr + SL.stripes);
+        P.plan_codes = reinterpret_cast<uint32_t *>(scr + SL.codes);
+        P.hdr = scr + SL.hdr;
+        P.blob = static_cast<uint8_t *>(d_blob);
+        P.total = reinterpret_cast<unsigned long long *>(scr + SL.total_bytes);
+        P.plan_ticket = reinterpret_cast<uint32_t *>(scr + SL.plan_ticket);
+        P.blob_cap = blob_cap;
+        P.hdr_bytes = uint32_t(header_bytes(ns, L.n_tables, L.n_tensors));
+        P.n_stripes = uint32_t(ns);
+        P.n_tensors = L.n_tensors;
+        P.n_tables = L.n_tables;
 
         std::vector<EncStripe> desc(ns);
         uint32_t max_n = 0, max_chunks = 0;
@@ -1003,12 +1377,68 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
             max_n = std::max(max_n, d.n);
             max_chunks = std::max(max_chunks, p.n_chunks);
         }
-        // 1. histograms
-        cudaError_t e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
-        // histograms, tickets, look-back records and the flag start at zero
-        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.counts, 0, SL.total - SL.counts, st);
-        if (e != cudaSuccess) return cuda_fail(e);
         const uint32_t gx = std::min<uint32_t>(512, std::max<uint32_t>(1, (max_n + 65535) / 65536));
+        cudaError_t e = cudaSuccess;
+        if (chunk_syms == 4096 && sub_syms == 256) {
+            // the default layout, planned on the device: the header's fields
+            // that no histogram decides and each stripe's index size go up
+            // with the descriptors; no host step sits between the passes
+            // (with zeroed histograms after them: one copy, no memset)
+            place_stripes(L);                          // (no bits yet: header size, bit offsets)
+            L.codelen.assign(256ull * L.n_tables, 0);
+            for (size_t i = 0; i < ns; ++i) desc[i].bits_offset = L.stripes[i].bits_offset;
+            const size_t up_bytes = SL.codes - SL.stripes;
+            uint8_t *const stage = may_pin ? pinned_stage() : nullptr;
+            const bool pinned = stage && up_bytes + 16 <= kStageBytes;
+            std::vector<uint8_t> pageable(pinned ? 0 : up_bytes + 16);
+            uint8_t *const up = pinned ? stage : pageable.data();
+            std::memset(up, 0, up_bytes);
+            std::memcpy(up, desc.data(), ns * sizeof(EncStripe));
+            write_layer_header(L, up + (SL.hdr - SL.stripes));
+            uint32_t *const back = reinterpret_cast<uint32_t *>(up + up_bytes);   // flag, 0, size
+            P.result = pinned ? back : nullptr;
+            back[0] = kFlagPlan;                       // (until the last kernel reports)
+            back[1] = back[2] = back[3] = 0u;
+            // a failure after the upload is queued waits for it, so that the
+            // staging is free when the call returns
+            auto fail = [&](cudaError_t err) {
+                (void)cudaStreamSynchronize(st);
+                return cuda_fail(err);
+            };
+            P.zero = reinterpret_cast<uint4 *>(scr + SL.tickets);
+            P.n_zero = uint32_t((SL.total - SL.tickets) / 16);
+            e = cudaMemcpyAsync(scr + SL.stripes, up, up_bytes, cudaMemcpyHostToDevice, st);
+            if (e != cudaSuccess) return fail(e);
+            hist_kernel<<<dim3(gx, uint32_t(ns)), kHistThreads, 0, st>>>(P);
+            plan_kernel<<<L.n_tables, kPlanThreads, 0, st>>>(P);
+            if (d_blob) {
+                int sms = 0;
+                if ((e = pack_lb_setup(&sms)) != cudaSuccess) return fail(e);
+                const uint32_t per = std::max<uint32_t>(1, (2u * uint32_t(std::max(1, sms)) + uint32_t(ns) - 1) / uint32_t(ns));
+                const uint32_t gl = std::min<uint32_t>(per, std::max<uint32_t>(1, (max_chunks + kLbWarps - 1) / kLbWarps));
+                pack_lb_kernel<<<dim3(gl, uint32_t(ns)), kLbThreads, kLbSmem, st>>>(P);
+                const uint32_t gsm = std::min<uint32_t>(64, std::max<uint32_t>(1, (max_chunks + 255) / 256));
+                seam_kernel<<<dim3(gsm, uint32_t(ns)), 256, 0, st>>>(P);
+            }
+            if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+            if (!pinned) {
+                e = cudaMemcpyAsync(back, scr + SL.flag, 16, cudaMemcpyDeviceToHost, st);
+                if (e != cudaSuccess) return fail(e);
+            }
+            if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e);
+            const volatile uint32_t *r = back;
+            const uint32_t flag = r[0];
+            *blob_bytes = size_t(uint64_t(r[2]) | (uint64_t(r[3]) << 32));
+            if (!d_blob) return K3HUF_OK;
+            if (flag & kFlagShort) return K3HUF_E_ARG;
+            return flag ? K3HUF_E_FORMAT : K3HUF_OK;
+        }
+        // any other layout: 1. histograms
+        e = cudaMemcpyAsync(scr + SL.stripes, desc.data(), ns * sizeof(EncStripe), cudaMemcpyHostToDevice, st);
+        // histograms, tickets, chunk words and the flag start at zero
+        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.counts, 0, SL.codes - SL.counts, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.tickets, 0, SL.total - SL.tickets, st);
+        if (e != cudaSuccess) return cuda_fail(e);
         hist_kernel<<<dim3(gx, uint32_t(ns)), kHistThreads, 0, st>>>(P);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
         std::vector<uint32_t> counts(ns * 256);
@@ -1037,8 +1467,8 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
             desc[i].even_offset = p.even_offset;
             desc[i].span = uint32_t((i + 1 < ns ? L.stripes[i + 1].blob_offset : L.total) - p.blob_offset);
         }
-        // the default layout (256-value sub-streams, 1-16 per chunk) packs
-        // one sub-stream per lane; any other layout one chunk per warp
+        // 256-value sub-streams, 1-16 per chunk: one sub-stream per lane;
+        // any other layout one chunk per warp
         const bool per_sub = sub_syms == 256 && chunk_syms % 256 == 0 && P.S <= 16 && (P.S & (P.S - 1)) == 0;
         std::vector<uint8_t> head(size_t(L.hdr));
         write_layer_header(L, head.data());
@@ -1049,8 +1479,7 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         if (e == cudaSuccess && !per_sub) e = cudaMemsetAsync(blob, 0, size_t(L.total), st);
         if (e == cudaSuccess) e = cudaMemcpyAsync(blob, head.data(), head.size(), cudaMemcpyHostToDevice, st);
         if (e != cudaSuccess) return cuda_fail(e);
-        const bool one_pass = per_sub && chunk_syms == 4096;
-        if (per_sub && !one_pass) {
+        if (per_sub) {
             uint64_t max_units = 1;
             for (size_t i = 0; i < ns; ++i)
                 max_units = std::max<uint64_t>(max_units, (desc[i].span - (desc[i].n & ~15u)) / 16u);
@@ -1060,16 +1489,7 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
         // 3-5. chunk bits, chunk index, packing
         const uint32_t wpb = kPackThreads / 32;
         const uint32_t gp = std::min<uint32_t>(1024, std::max<uint32_t>(1, (max_chunks + wpb - 1) / wpb));
-        if (one_pass) {
-            // (tickets and look-back records were zeroed before the histogram)
-            int sms = 0;
-            if ((e = pack_lb_setup(&sms)) != cudaSuccess) return cuda_fail(e);
-            const uint32_t per = std::max<uint32_t>(1, (2u * uint32_t(std::max(1, sms)) + uint32_t(ns) - 1) / uint32_t(ns));
-            const uint32_t gl = std::min<uint32_t>(per, std::max<uint32_t>(1, (max_chunks + kLbWarps - 1) / kLbWarps));
-            pack_lb_kernel<<<dim3(gl, uint32_t(ns)), kLbThreads, kLbSmem, st>>>(P);
-            const uint32_t gsm = std::min<uint32_t>(64, std::max<uint32_t>(1, (max_chunks + 255) / 256));
-            seam_kernel<<<dim3(gsm, uint32_t(ns)), 256, 0, st>>>(P);
-        } else if (per_sub) {
+        if (per_sub) {
             sub_bits_kernel<<<dim3(gp, uint32_t(ns)), kPackThreads, 0, st>>>(P);
             scan_kernel<<<uint32_t(ns), kScanThreads, 0, st>>>(P);
             const uint64_t max_sub = uint64_t(max_chunks) * P.S;
@@ -1089,6 +1509,17 @@ extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_t
     } catch (const std::bad_alloc &) {
         return K3HUF_E_NOMEM;
     }
+}
+
+}  // namespace
+}  // namespace k3huf
+
+extern "C" int k3huf_encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uint64_t *n_values,
+                                      uint32_t chunk_syms, uint32_t sub_syms, int shared_table,
+                                      void *d_scratch, size_t scratch_bytes, void *d_blob, size_t blob_cap,
+                                      size_t *blob_bytes, void *stream) {
+    return encode_layer_gpu(n_tensors, d_tensors, n_values, chunk_syms, sub_syms, shared_table, d_scratch,
+                            scratch_bytes, d_blob, blob_cap, blob_bytes, stream, true);
 }
 
 // ---------------------------------------------------------------------------
@@ -1157,6 +1588,7 @@ extern "C" int k3huf_encode_layer_gpu_noalloc(uint32_t n_tensors, const void *co
         }
         if (sdev != dev) return K3HUF_E_ARG;
     }
-    return k3huf_encode_layer_gpu(n_tensors, d_tensors, n_values, chunk_syms, sub_syms, shared_table, scratch,
-                                  kFixedScratchBytes, d_blob, blob_cap, blob_bytes, stream);
+    // (no pinned staging either: a page-locked allocation can synchronise the device)
+    return encode_layer_gpu(n_tensors, d_tensors, n_values, chunk_syms, sub_syms, shared_table, scratch,
+                            kFixedScratchBytes, d_blob, blob_cap, blob_bytes, stream, false);
 }

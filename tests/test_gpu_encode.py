@@ -141,3 +141,33 @@ def test_gpu_encoder_random_layers():
         got = k3.encode_layer_gpu([dev(x) for x in tensors], out=buf, **kw)
         torch.cuda.synchronize()
         assert np.array_equal(got.cpu().numpy(), oracle.encode_layer(tensors, **kw)), case
+
+
+@pytest.mark.parametrize("chunk_syms", [4096, 1024])
+def test_gpu_encoder_short_buffer_writes_nothing(chunk_syms):
+    """A buffer one byte shorter than the container: K3HUF_E_ARG, the size
+    still reported, and not one byte of the buffer written (with the default
+    layout the GPU finds the shortfall, with another the host)."""
+    import ctypes
+    ts = CASES["multi"]()
+    ref = oracle.encode_layer(ts, chunk_syms=chunk_syms)
+    d = [dev(x) for x in ts]
+    scratch = torch.full((k3.encode_scratch_bytes([t.size for t in ts], chunk_syms=chunk_syms),), 0xA5,
+                         dtype=torch.uint8, device="cuda")
+    buf = torch.full((ref.size + 4096,), 0xA5, dtype=torch.uint8, device="cuda")
+    L = k3._lib()
+    ptrs = (ctypes.c_void_p * len(d))(*[t.data_ptr() for t in d])
+    nv = (ctypes.c_uint64 * len(d))(*[t.numel() for t in d])
+    size = ctypes.c_size_t(0)
+    rc = L.k3huf_encode_layer_gpu(len(d), ptrs, nv, chunk_syms, 256, 0, scratch.data_ptr(), scratch.numel(),
+                                  buf.data_ptr(), ref.size - 1, ctypes.byref(size), None)
+    torch.cuda.synchronize()
+    assert rc == k3.E_ARG
+    assert size.value == ref.size
+    assert bool((buf == 0xA5).all())
+    # the same scratch, uncleared, then serves a call with room
+    rc = L.k3huf_encode_layer_gpu(len(d), ptrs, nv, chunk_syms, 256, 0, scratch.data_ptr(), scratch.numel(),
+                                  buf.data_ptr(), buf.numel(), ctypes.byref(size), None)
+    torch.cuda.synchronize()
+    assert rc == 0 and size.value == ref.size
+    assert np.array_equal(buf[: ref.size].cpu().numpy(), ref)
