@@ -134,9 +134,17 @@ uint64_t count_chunks(const LayerPlan &L) {
     return n;
 }
 
+// Programmatic dependent launch (default layout): the planner, the packer
+// and the seams are launched while the kernel before them runs, and wait
+// for its completion (and its writes) before they read anything it wrote,
+// so that each one's launch and CTA start-up overlap the one before.
+__device__ __forceinline__ void enc_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void enc_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 1. histogram of the high bytes of one stripe's values, per CTA a slice
 __global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
     __shared__ uint32_t h[kHistThreads / 32][256];
+    enc_dep_launch();
     const EncStripe &T = P.stripes[blockIdx.y];
     const int tid = threadIdx.x;
     // (default layout: the packer's tickets and look-back records, the flag,
@@ -216,6 +224,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(EncParams P) {
     __shared__ uint16_t par[512];
     __shared__ uint8_t sym[256], len[256];
     __shared__ uint32_t ord[256], lmask[kPlanThreads / 32][16], first[16], s_n, s_last;
+    enc_dep_wait();
+    enc_dep_launch();
     const uint32_t s = threadIdx.x, tb = blockIdx.x;
     const uint32_t lane = s & 31u, warp = s >> 5, lt = (1u << lane) - 1u;
     // the table's stripes: all of them for one table, else tensor tb's (from
@@ -978,6 +988,7 @@ struct LbRun {
 };
 
 __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
+    enc_dep_wait();
     if (*P.flag & kFlagShort) return;                // (the planner found the blob too small)
     extern __shared__ __align__(16) uint8_t lb_smem[];
     uint32_t(*code)[16] = reinterpret_cast<uint32_t(*)[16]>(lb_smem);   // entry s for lanes l, l + 16 at code[s][l % 16]
@@ -1183,6 +1194,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
         }
         __syncwarp();                                 // the rows and the runs free again
     }
+    enc_dep_launch();
 }
 
 // After the one-pass packer: each stream word that two chunks share is the
@@ -1191,6 +1203,7 @@ __global__ void __launch_bounds__(kLbThreads, 1) pack_lb_kernel(EncParams P) {
 // the stream region after its last word, and the low bytes' tail up to the
 // next stripe (a few hundred bytes per stripe).
 __global__ void __launch_bounds__(256) seam_kernel(EncParams P) {
+    enc_dep_wait();
     if (P.result && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
         // the call's outcome, straight into the host's memory
         volatile uint32_t *r = P.result;
@@ -1410,15 +1423,28 @@ int encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uin
             e = cudaMemcpyAsync(scr + SL.stripes, up, up_bytes, cudaMemcpyHostToDevice, st);
             if (e != cudaSuccess) return fail(e);
             hist_kernel<<<dim3(gx, uint32_t(ns)), kHistThreads, 0, st>>>(P);
-            plan_kernel<<<L.n_tables, kPlanThreads, 0, st>>>(P);
+            auto early = [&](auto kern, dim3 g, dim3 b, size_t sm) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = g;
+                cfg.blockDim = b;
+                cfg.dynamicSmemBytes = sm;
+                cfg.stream = st;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                return cudaLaunchKernelEx(&cfg, kern, P);
+            };
+            if ((e = early(plan_kernel, dim3(L.n_tables), dim3(kPlanThreads), 0)) != cudaSuccess) return fail(e);
             if (d_blob) {
                 int sms = 0;
                 if ((e = pack_lb_setup(&sms)) != cudaSuccess) return fail(e);
                 const uint32_t per = std::max<uint32_t>(1, (2u * uint32_t(std::max(1, sms)) + uint32_t(ns) - 1) / uint32_t(ns));
                 const uint32_t gl = std::min<uint32_t>(per, std::max<uint32_t>(1, (max_chunks + kLbWarps - 1) / kLbWarps));
-                pack_lb_kernel<<<dim3(gl, uint32_t(ns)), kLbThreads, kLbSmem, st>>>(P);
+                if ((e = early(pack_lb_kernel, dim3(gl, uint32_t(ns)), dim3(kLbThreads), kLbSmem)) != cudaSuccess) return fail(e);
                 const uint32_t gsm = std::min<uint32_t>(64, std::max<uint32_t>(1, (max_chunks + 255) / 256));
-                seam_kernel<<<dim3(gsm, uint32_t(ns)), 256, 0, st>>>(P);
+                if ((e = early(seam_kernel, dim3(gsm, uint32_t(ns)), dim3(256), 0)) != cudaSuccess) return fail(e);
             }
             if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
             if (!pinned) {

@@ -171,3 +171,50 @@ def test_gpu_encoder_short_buffer_writes_nothing(chunk_syms):
     torch.cuda.synchronize()
     assert rc == 0 and size.value == ref.size
     assert np.array_equal(buf[: ref.size].cpu().numpy(), ref)
+
+
+def _with_counts(counts, seed):
+    """bf16 values whose high bytes have exactly these counts (symbol s
+    `counts[s]` times), shuffled, with random low bytes."""
+    rng = np.random.default_rng(seed)
+    hi = np.repeat(np.arange(256, dtype=np.uint16), np.asarray(counts, dtype=np.int64))
+    rng.shuffle(hi)
+    return (hi << 8) | rng.integers(0, 256, size=hi.size, dtype=np.uint16)
+
+
+def _fib(n):
+    a, b, out = 1, 1, []
+    for _ in range(n):
+        out.append(a)
+        a, b = b, a + b
+    return out
+
+
+PLANNER_COUNTS = {
+    # Fibonacci counts: a Huffman tree 26 levels deep, cut to 12 bits
+    "fibonacci": lambda: [0] * 230 + _fib(26),
+    # every symbol equally often: 255 merges, every weight tied
+    "all_equal": lambda: [37] * 256,
+    # pairs of equal counts doubling: leaves tie with the nodes made from
+    # the pairs before them
+    "doubling_pairs": lambda: sum(([1 << k, 1 << k] for k in range(12)), []) + [0] * 232,
+    # many symbols seen once beside a few heavy ones: the cap lengthens a
+    # long run of equal-count codes (ties to the larger symbol)
+    "heavy_and_singletons": lambda: [200_000, 150_000, 90_000, 40_000] + [1] * 252,
+}
+
+
+@pytest.mark.parametrize("name", sorted(PLANNER_COUNTS))
+@pytest.mark.parametrize("chunk_syms", [4096, 1024])
+def test_gpu_encoder_tie_and_limiter_alphabets(name, chunk_syms):
+    """Histograms built to exercise the code-length choices: ties between
+    leaves, between internal nodes and across the two, a deep tree cut to
+    12 bits, and a long run of equal counts for the cap to lengthen.  The
+    default layout decides lengths, codes and layout on the GPU, chunk
+    size 1024 on the host; both containers equal the oracle's byte for
+    byte, alone and as tables of a two-tensor layer."""
+    counts = PLANNER_COUNTS[name]()
+    x = _with_counts(counts, 7)
+    y = _with_counts(list(reversed(counts)), 8)
+    for ts in ([x], [x, y]):
+        assert np.array_equal(gpu_blob(ts, chunk_syms=chunk_syms), oracle.encode_layer(ts, chunk_syms=chunk_syms))
