@@ -218,3 +218,38 @@ def test_gpu_encoder_tie_and_limiter_alphabets(name, chunk_syms):
     y = _with_counts(list(reversed(counts)), 8)
     for ts in ([x], [x, y]):
         assert np.array_equal(gpu_blob(ts, chunk_syms=chunk_syms), oracle.encode_layer(ts, chunk_syms=chunk_syms))
+
+
+def test_gpu_encoder_concurrent_host_threads():
+    """Two host threads encode at once, each on its own stream with its own
+    scratch and output (the call stages its upload and its outcome in a
+    pinned buffer of the calling thread): every container equals the
+    oracle's."""
+    import threading
+    layers = [[workloads.normal_tensor((200_003,), 0.02, 40 + i)] for i in range(2)]
+    refs = [oracle.encode_layer(ts) for ts in layers]
+    errors = []
+
+    def worker(i):
+        try:
+            stream = torch.cuda.Stream()
+            d = [dev(x) for x in layers[i]]
+            scratch = torch.empty(k3.encode_scratch_bytes([x.size for x in layers[i]]), dtype=torch.uint8,
+                                  device="cuda")
+            out = torch.empty(k3.encode_bound([x.size for x in layers[i]]), dtype=torch.uint8, device="cuda")
+            torch.cuda.synchronize()
+            for _ in range(20):
+                got = k3.encode_layer_gpu(d, stream=stream, scratch=scratch, out=out)
+                stream.synchronize()
+                if not np.array_equal(got.cpu().numpy(), refs[i]):
+                    errors.append(i)
+                    return
+        except Exception as e:          # reported below, with the thread's index
+            errors.append((i, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
