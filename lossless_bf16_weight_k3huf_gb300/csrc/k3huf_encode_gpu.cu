@@ -141,11 +141,16 @@ uint64_t count_chunks(const LayerPlan &L) {
 __device__ __forceinline__ void enc_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void enc_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// 1. histogram of the high bytes of one stripe's values, per CTA a slice
+// 1. histogram of the high bytes of one stripe's values, per CTA a slice.
+//    The grid runs stripe-fastest and takes each stripe's slices last to
+//    first, so that its last wave reads the start of every stripe, which
+//    the packer reads first (much of it still in L2 then: 0.4-0.8% off a
+//    1 GiB encode, measured)
 __global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
     __shared__ uint32_t h[kHistThreads / 32][256];
     enc_dep_launch();
-    const EncStripe &T = P.stripes[blockIdx.y];
+    const uint32_t stripe = blockIdx.x, slice = gridDim.y - 1 - blockIdx.y, n_slices = gridDim.y;
+    const EncStripe &T = P.stripes[stripe];
     const int tid = threadIdx.x;
     // (default layout: the packer's tickets and look-back records, the flag,
     // the planner's ticket and the size start at zero)
@@ -155,8 +160,8 @@ __global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
     for (int i = tid; i < (kHistThreads / 32) * 256; i += kHistThreads) (&h[0][0])[i] = 0;
     __syncthreads();
     uint32_t *hw = h[tid >> 5];
-    const uint64_t per = ((uint64_t(T.n) + gridDim.x - 1) / gridDim.x + 7) / 8 * 8;
-    const uint64_t a = min(uint64_t(T.n), uint64_t(blockIdx.x) * per), b = min(uint64_t(T.n), a + per);
+    const uint64_t per = ((uint64_t(T.n) + n_slices - 1) / n_slices + 7) / 8 * 8;
+    const uint64_t a = min(uint64_t(T.n), uint64_t(slice) * per), b = min(uint64_t(T.n), a + per);
     const uint64_t vend = a + (b - a) / 8 * 8;
     // four 16-byte loads in flight per thread, then their 32 high bytes
     uint64_t k = a + uint64_t(tid) * 8;
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kHistThreads) hist_kernel(EncParams P) {
     for (int s = tid; s < 256; s += kHistThreads) {
         uint32_t c = 0;
         for (int w = 0; w < kHistThreads / 32; ++w) c += h[w][s];
-        if (c) atomicAdd(&P.counts[size_t(blockIdx.y) * 256 + s], c);
+        if (c) atomicAdd(&P.counts[size_t(stripe) * 256 + s], c);
     }
 }
 
@@ -1422,7 +1427,7 @@ int encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uin
             P.n_zero = uint32_t((SL.total - SL.tickets) / 16);
             e = cudaMemcpyAsync(scr + SL.stripes, up, up_bytes, cudaMemcpyHostToDevice, st);
             if (e != cudaSuccess) return fail(e);
-            hist_kernel<<<dim3(gx, uint32_t(ns)), kHistThreads, 0, st>>>(P);
+            hist_kernel<<<dim3(uint32_t(ns), gx), kHistThreads, 0, st>>>(P);
             auto early = [&](auto kern, dim3 g, dim3 b, size_t sm) {
                 cudaLaunchConfig_t cfg = {};
                 cfg.gridDim = g;
@@ -1465,7 +1470,7 @@ int encode_layer_gpu(uint32_t n_tensors, const void *const *d_tensors, const uin
         if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.counts, 0, SL.codes - SL.counts, st);
         if (e == cudaSuccess) e = cudaMemsetAsync(scr + SL.tickets, 0, SL.total - SL.tickets, st);
         if (e != cudaSuccess) return cuda_fail(e);
-        hist_kernel<<<dim3(gx, uint32_t(ns)), kHistThreads, 0, st>>>(P);
+        hist_kernel<<<dim3(uint32_t(ns), gx), kHistThreads, 0, st>>>(P);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
         std::vector<uint32_t> counts(ns * 256);
         e = cudaMemcpyAsync(counts.data(), scr + SL.counts, counts.size() * sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
