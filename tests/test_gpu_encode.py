@@ -253,3 +253,13 @@ def test_gpu_encoder_concurrent_host_threads():
     for t in threads:
         t.join()
     assert not errors, errors
+
+
+@pytest.mark.parametrize("shared_table", [False, True])
+def test_gpu_encoder_more_stripes_than_planner_threads(shared_table):
+    """300 small tensors make 300 stripes, more than the planner's 256
+    threads place in one round, so the stripes' offsets are summed over two
+    rounds (and 300 tables are planned by 300 CTAs, or one table over all
+    stripes): the container equals the oracle's byte for byte."""
+    ts = [workloads.normal_tensor((97 + 31 * i,), 0.01 + 0.001 * (i % 7), 900 + i) for i in range(300)]
+    assert np.array_equal(gpu_blob(ts, shared_table=shared_table), oracle.encode_layer(ts, shared_table=shared_table))
